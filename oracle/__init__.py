@@ -1,0 +1,116 @@
+"""CPU oracle for the prefix sum -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never touches it and
+it never touches the CUDA library: the two share no code.
+
+The arithmetic lives in ``scan_oracle.c`` (a plain sequential running sum,
+written from the definition y[i] = x[0] + ... + x[i] on the cumsum page
+"CUDA-Operators-6-Cumsum", section 1, and the inclusive/exclusive conversion
+section of the RTX 4090 scan tutorial).  This module only compiles that file
+with gcc and marshals numpy arrays into it.
+
+Every function here is pinned by ``tests/test_oracle_pins.py``; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+SOURCE = _HERE / "scan_oracle.c"
+LIBRARY = _HERE / "_scan_oracle.so"
+
+_lock = threading.Lock()
+_lib = None
+
+_INT_TYPES = {
+    np.dtype(np.int32): ("i32", ctypes.c_int32),
+    np.dtype(np.int64): ("i64", ctypes.c_int64),
+}
+
+
+def build(force: bool = False, source: Path | None = None, target: Path | None = None) -> Path:
+    """Compile the oracle with gcc into a shared object (no-op when fresh).
+
+    ``source``/``target`` let a test compile a modified copy elsewhere.
+    """
+    src = Path(source) if source is not None else SOURCE
+    out = Path(target) if target is not None else LIBRARY
+    if not force and out.exists() and out.stat().st_mtime >= src.stat().st_mtime:
+        return out
+    tmp = out.with_name(out.name + f".{os.getpid()}.tmp")
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-fPIC", "-shared",
+           "-o", str(tmp), str(src)]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    for name in ("oracle_inclusive_i32", "oracle_exclusive_i32",
+                 "oracle_inclusive_i64", "oracle_exclusive_i64",
+                 "oracle_inclusive_f32", "oracle_exclusive_f32"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, sz, vp]
+        fn.restype = None
+    lib.oracle_abs_prefix_f32.argtypes = [vp, sz, ctypes.c_int, vp]
+    lib.oracle_abs_prefix_f32.restype = None
+    return lib
+
+
+def load(path: Path | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) the compiled oracle."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(str(path)))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(str(build())))
+        return _lib
+
+
+def _ptr(a: np.ndarray) -> ctypes.c_void_p:
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _scan(x: np.ndarray, exclusive: bool, lib: ctypes.CDLL | None) -> np.ndarray:
+    lib = lib if lib is not None else load()
+    x = np.ascontiguousarray(x)
+    kind = "exclusive" if exclusive else "inclusive"
+    if x.dtype == np.float32:
+        y = np.empty(x.shape[0], dtype=np.float64)
+        getattr(lib, f"oracle_{kind}_f32")(_ptr(x), x.shape[0], _ptr(y))
+        return y
+    if x.dtype not in _INT_TYPES:
+        raise TypeError(f"oracle: unsupported dtype {x.dtype}")
+    tag, _ = _INT_TYPES[x.dtype]
+    y = np.empty_like(x)
+    getattr(lib, f"oracle_{kind}_{tag}")(_ptr(x), x.shape[0], _ptr(y))
+    return y
+
+
+def inclusive(x: np.ndarray, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """y[i] = x[0] + ... + x[i]; int32/int64 wrap modulo 2^w, fp32 -> float64."""
+    return _scan(x, False, lib)
+
+
+def exclusive(x: np.ndarray, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """y[0] = 0, y[i] = x[0] + ... + x[i-1]; same types as :func:`inclusive`."""
+    return _scan(x, True, lib)
+
+
+def abs_prefix(x: np.ndarray, exclusive_: bool, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Prefix sums of |x| in float64 (the scale of the fp32 error bound)."""
+    lib = lib if lib is not None else load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    a = np.empty(x.shape[0], dtype=np.float64)
+    lib.oracle_abs_prefix_f32(_ptr(x), x.shape[0], int(bool(exclusive_)), _ptr(a))
+    return a
