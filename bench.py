@@ -1,0 +1,534 @@
+#!/usr/bin/env python3
+"""Benchmark of the single-pass decoupled look-back prefix sum on GB300.
+
+One "step" is one scan call (workspace reset + the single-pass kernel) over
+the whole input of the chosen workload, inputs resident in HBM.  Prints ONE
+JSON line (rank 0).  Metric: achieved bandwidth in GB/s with the algorithmic
+traffic 2 * n * sizeof(T) (read every input once, write every output once),
+plus Gelem/s and the ratio to a device-to-device memcpy of the same bytes
+timed in the same run.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--sweep] [--compare]
+
+--impl reference times the CPU oracle (the plain sequential scan) on the
+host cores on a bounded sample of the same workload.  With N > 1 (torchrun)
+each rank runs an independent replica of the workload on its own GPU (the
+scan has no data-parallel exchange to shard): "scaling": "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from prefix_scan_gb300 import workloads  # noqa: E402
+
+L2_BYTES = 129 * 1000 * 1000
+FLUSH_BYTES = 512 << 20
+METRIC = "scan Gelem/s and achieved HBM GB/s (2n·sizeof(T)) vs same-run memcpy, 1×GB300"
+DEFAULT_WORKLOAD = workloads.I32_EXCL_2P28.name
+DTYPE_TAG = {"int32": "int32", "int64": "int64", "float32": "f32"}
+
+
+# ----------------------------------------------------------------- peaks ----
+
+def hbm_peak() -> tuple[float, str]:
+    p = ROOT / "MEASURED_PEAKS.json"
+    try:
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons during a region.
+
+    NVML through ctypes (read-only queries) every few milliseconds; falls
+    back to ``nvidia-smi -lms`` when NVML cannot be opened.
+    """
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device_index: int = 0, period_s: float = 0.005):
+        self.period = period_s
+        self.samples: list[tuple[int, int, int]] = []   # (sm_mhz, reasons_mask, power_mw)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._smi = None
+        self._smi_path = None
+        self._nvml = None
+        self._handle = None
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(torch_device_index)
+            bus = (f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:"
+                   f"{props.pci_device_id:02X}.0")
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                raise RuntimeError("no NVML handle for " + bus)
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._handle = nv, h
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception:
+            self._nvml = None
+
+    def _sample_nvml(self):
+        nv, h = self._nvml, self._handle
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))
+            nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            self._reasons_fn(h, ctypes.byref(rs))
+            self.samples.append((clk.value, rs.value, pw.value))
+            time.sleep(self.period)
+
+    def __enter__(self):
+        self._stop.clear()
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._sample_nvml, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                import tempfile
+                fd, self._smi_path = tempfile.mkstemp(suffix=".csv")
+                os.close(fd)
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", "-i", os.environ.get("LOCAL_RANK", "0"),
+                     "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "100", "-f", self._smi_path])
+            except Exception:
+                self._smi = None
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+        if self._smi is not None:
+            time.sleep(0.15)
+            self._smi.terminate()
+            self._smi.wait()
+            for line in Path(self._smi_path).read_text().splitlines():
+                try:
+                    sm, mx, pw, act = [v.strip() for v in line.split(",")]
+                    self.samples.append((int(float(sm)), int(act, 16), int(float(pw) * 1000)))
+                    self.max_mhz = int(float(mx))
+                except ValueError:
+                    continue
+            os.unlink(self._smi_path)
+        return False
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml" if self._nvml is not None else "nvidia-smi"}
+        mask = 0
+        for _, r, _ in self.samples:
+            mask |= r
+        reasons = [name for bit, name in self.REASONS.items() if mask & bit]
+        return {"sm_mhz": int(statistics.median(s[0] for s in self.samples)),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
+                "power_w_max": round(max(s[2] for s in self.samples) / 1000.0, 1),
+                "source": "nvml" if self._nvml is not None else "nvidia-smi"}
+
+
+# -------------------------------------------------------------- helpers ----
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def cpu_baseline(w: workloads.Workload, target_s: float = 10.0, sample_n: int = 1 << 26) -> dict:
+    """The oracle as it stands, single-threaded, on a bounded sample."""
+    import oracle
+    n = min(sample_n, w.n)
+    x = w.make(n)
+    fn = oracle.exclusive if w.exclusive else oracle.inclusive
+    fn(x[:1024])  # load/compile outside the timing
+    reps, t0 = 0, time.perf_counter()
+    best = float("inf")
+    while True:
+        t = time.perf_counter()
+        fn(x)
+        best = min(best, time.perf_counter() - t)
+        reps += 1
+        if time.perf_counter() - t0 >= target_s:
+            break
+    elems_s = n / best
+    gbs = 2.0 * n * w.itemsize / best / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "gelem_per_s": round(elems_s / 1e9, 4),
+            "cores": 1, "kind": "oracle",
+            "sample": f"first {n} elements of the {w.name} input, best of {reps} runs "
+                      f"({time.perf_counter() - t0:.1f} s of single-threaded CPU work)",
+            "cpu": _cpu_model()}
+
+
+def _cpu_model() -> str:
+    try:
+        for line in Path("/proc/cpuinfo").read_text().splitlines():
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+# ------------------------------------------------------------ reference ----
+
+def run_reference(args, rank: int, world: int) -> None:
+    """--impl reference: the CPU oracle, timed on the host cores."""
+    if rank != 0:
+        return
+    w = workloads.BY_NAME[args.workload]
+    import oracle
+    n = min(args.ref_sample, w.n)
+    x = w.make(n)
+    fn = oracle.exclusive if w.exclusive else oracle.inclusive
+    fn(x[:1024])
+    for _ in range(max(args.warmup, 0)):
+        fn(x)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        fn(x)
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    gbs = 2.0 * n * w.itemsize * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_TAG[w.dtype], "data": "synthetic",
+        "config": _config(w, world, n, note="bounded sample of the workload"),
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {n} of {w.n} elements per step", "cpu": _cpu_model()},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gelem_per_s": round(n * args.steps / total / 1e9, 4),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w: workloads.Workload, world: int, n: int, note: str = "") -> dict:
+    c = {"workload": w.describe() if n == w.n else w.describe().replace(f"n={w.n}", f"n={n}"),
+         "name": w.name, "n": n, "elem_bytes": w.itemsize,
+         "algorithmic_bytes_per_step": 2 * n * w.itemsize,
+         "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+         "l2": "inputs larger than L2" if n * w.itemsize > 2 * L2_BYTES else "L2 flushed between steps"}
+    if note:
+        c["note"] = note
+    return c
+
+
+# ------------------------------------------------------------------ ours ----
+
+class Harness:
+    def __init__(self, w: workloads.Workload, n: int, dev):
+        import torch
+        from prefix_scan_gb300 import api
+        self.torch, self.api, self.w, self.n, self.dev = torch, api, w, n, dev
+        tdt = {"int32": torch.int32, "int64": torch.int64, "float32": torch.float32}[w.dtype]
+        self.tdt = tdt
+        self.host_in = torch.empty(n, dtype=tdt, pin_memory=True)
+        w.make(n, out=self.host_in.numpy())
+        self.host_out = torch.empty(n, dtype=tdt, pin_memory=True)
+        self.d_in = self.host_in.to(dev)
+        self.pristine = None
+        self.d_out = self.d_in if w.inplace else torch.empty_like(self.d_in)
+        self.ws = api.alloc_workspace(tdt, n, dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.flush = None
+        if n * w.itemsize <= 2 * L2_BYTES:
+            self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.launches_per_step = 1
+
+    def step(self, algo="decoupled"):
+        self.api.scan(self.d_in, exclusive=self.w.exclusive, out=self.d_out,
+                      workspace=self.ws, algo=algo)
+
+    def timed(self, steps: int, fn, world: int) -> tuple[float, list[float]]:
+        """Seconds for ``steps`` calls of fn, events on the launching stream."""
+        torch = self.torch
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        per = []
+        if self.flush is None:
+            ev[0].record(self.stream)
+            for _ in range(steps):
+                fn()
+            ev[1].record(self.stream)
+            torch.cuda.synchronize()
+            total = ev[0].elapsed_time(ev[1]) / 1e3
+            per = [total / steps] * steps
+        else:
+            for k in range(steps):
+                self.flush.fill_(k & 0xFF)        # evict the data from L2
+                ev[2 * k].record(self.stream)
+                fn()
+                ev[2 * k + 1].record(self.stream)
+            torch.cuda.synchronize()
+            per = [ev[2 * k].elapsed_time(ev[2 * k + 1]) / 1e3 for k in range(steps)]
+            total = sum(per)
+        barrier(world)
+        return total, per
+
+    def memcpy(self):
+        dst = self.d_out if not self.w.inplace else self._scratch()
+        dst.copy_(self.d_in)
+
+    def _scratch(self):
+        if getattr(self, "_scr", None) is None:
+            self._scr = self.torch.empty_like(self.d_in)
+        return self._scr
+
+    def e2e_step(self):
+        """User-level call on host buffers: H2D, scan, D2H on one stream."""
+        d = self.d_out
+        d.copy_(self.host_in, non_blocking=True)
+        self.api.scan(d, exclusive=self.w.exclusive, inplace=True, workspace=self.ws)
+        self.host_out.copy_(d, non_blocking=True)
+
+    def property_check(self) -> bool:
+        """Cheap self-check of a fresh output (no oracle): prefixes at a few
+        sampled positions against running sums of the host input."""
+        torch = self.torch
+        src = self.d_in
+        if self.w.inplace:
+            src = self.d_out.copy_(self.host_in.to(self.dev))
+        self.api.scan(src, exclusive=self.w.exclusive, out=self.d_out, workspace=self.ws)
+        torch.cuda.synchronize()
+        y = self.d_out.cpu().numpy()
+        x = self.host_in.numpy()
+        idx = sorted(set([0, self.n - 1] + list(np.linspace(0, self.n - 1, 9).astype(np.int64))))
+        ok, pos = True, 0
+        acc, acc_abs = 0, 0.0
+        for i in idx:
+            hi = i if self.w.exclusive else i + 1
+            seg = x[pos:hi]
+            if self.w.dtype == "float32":
+                acc += float(np.sum(seg, dtype=np.float64))
+                acc_abs += float(np.sum(np.abs(seg), dtype=np.float64))
+                ok &= abs(float(y[i]) - acc) <= 1e-5 * acc_abs + 1e-6
+            else:
+                bits = 32 if self.w.dtype == "int32" else 64
+                acc += int(np.sum(seg, dtype=np.int64)) if bits == 32 else \
+                    int(np.sum(seg.view(np.uint64), dtype=np.uint64))
+                ok &= (int(y[i]) - acc) % (1 << bits) == 0
+            pos = hi
+        return bool(ok)
+
+
+def run_ours(args, rank: int, world: int, local: int) -> None:
+    import torch
+    from prefix_scan_gb300 import build as nvbuild
+    if not nvbuild.is_fresh():
+        nvbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.BY_NAME[args.workload]
+    n = args.n or w.n
+    h = Harness(w, n, dev)
+    bytes_step = 2 * n * w.itemsize
+    peak, peak_kind = hbm_peak()
+
+    for _ in range(args.warmup):
+        h.step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    with sampler:
+        t_scan, per = h.timed(args.steps, h.step, world)
+    t_scan = max_over_ranks(t_scan, world)
+    # same-run device-to-device copy of the same bytes, same protocol
+    for _ in range(max(3, args.warmup)):
+        h.memcpy()
+    t_copy, _ = h.timed(args.steps, h.memcpy, world)
+    t_copy = max_over_ranks(t_copy, world)
+    # end to end through the public API on pinned host buffers
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        h.e2e_step()
+    torch.cuda.synchronize()
+    saved = h.flush
+    h.flush = None
+    t_e2e, _ = h.timed(e2e_steps, h.e2e_step, world)
+    h.flush = saved
+    t_e2e = max_over_ranks(t_e2e, world)
+    ok = h.property_check()
+
+    units_total = sum_over_ranks(float(n * args.steps), world)
+    gbs = 2.0 * w.itemsize * units_total / t_scan / 1e9
+    per_launch = statistics.median(per)
+    achieved = bytes_step / per_launch / 1e9
+    copy_gbs = 2.0 * n * w.itemsize * args.steps / t_copy / 1e9
+    e2e_gbs = 2.0 * w.itemsize * sum_over_ranks(float(n * e2e_steps), world) / t_e2e / 1e9
+
+    extra = {}
+    if args.compare and world == 1:
+        for algo in ("reduce_then_scan", "chained"):
+            k = max(3, min(args.steps, 20))
+            h.step(algo)
+            torch.cuda.synchronize()
+            t, _ = h.timed(k, lambda: h.step(algo), 1)
+            extra[algo] = {"gbs": round(bytes_step * k / t / 1e9, 2),
+                           "ms_per_step": round(1000 * t / k, 4)}
+    sweep = []
+    if args.sweep and world == 1:
+        sweep = run_sweep(args)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * t_scan / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_TAG[w.dtype], "data": "synthetic",
+        "config": _config(w, world, n),
+        "gelem_per_s": round(units_total / t_scan / 1e9, 3),
+        "memcpy_gbs": round(copy_gbs, 2), "vs_memcpy": round(gbs / copy_gbs, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "per_launch_ms": round(per_launch * 1000, 4),
+                     "note": "per-launch time spans the workspace reset + the single-pass kernel"},
+        "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": n * w.itemsize, "d2h_bytes_per_step": n * w.itemsize,
+                "steps": e2e_steps, "path": "pinned host -> device copy, scan, device -> pinned host"},
+        "gpu_launches": args.steps * h.launches_per_step,
+        "clocks": sampler.summary(),
+        "parity_spot_check": ok,
+    }
+    if extra:
+        line["comparison_paths"] = extra
+    if sweep:
+        line["sweep"] = sweep
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def run_sweep(args) -> list[dict]:
+    import torch
+    out = []
+    for w in workloads.ALL:
+        sizes = w.sweep if w.sweep else (w.n,)
+        for n in sizes:
+            h = Harness(w, n, torch.device("cuda", 0))
+            for _ in range(3):
+                h.step()
+            k = 20
+            t, per = h.timed(k, h.step, 1)
+            for _ in range(3):
+                h.memcpy()
+            tc, _ = h.timed(k, h.memcpy, 1)
+            b = 2 * n * w.itemsize
+            med = statistics.median(per)
+            out.append({"name": w.name, "n": n, "ms": round(med * 1000, 4),
+                        "gbs": round(b / med / 1e9, 2), "gelem_per_s": round(n / med / 1e9, 3),
+                        "memcpy_gbs": round(b * k / tc / 1e9, 2),
+                        "vs_memcpy": round((b / med) / (b * k / tc), 4),
+                        "l2": "flushed" if h.flush is not None else "larger than L2",
+                        "spot_check": h.property_check()})
+            del h
+            torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.BY_NAME))
+    ap.add_argument("--n", type=int, default=0, help="override the workload length")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--compare", action="store_true", help="also time the comparison paths")
+    ap.add_argument("--sweep", action="store_true", help="also time every workload (extra key)")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of the current kernel")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-sample", type=int, default=1 << 25)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    try:
+        run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+/*
+ * prefix_scan.h -- C ABI of the GB300 (sm_103a) device-wide prefix sum.
+ *
+ * The operation (problem statement of the RTX 4090 scan tutorial,
+ * "smarter.xin/posts/bcb510f9", section 1; "Prefix Sum" definition of the
+ * page "CUDA-Operators-6-Cumsum", section 1):
+ *
+ *     inclusive   y[i] = x[0] + x[1] + ... + x[i]          0 <= i < n
+ *     exclusive   y[0] = 0,  y[i] = x[0] + ... + x[i-1]
+ *                 (conversion section "Inclusive 与 Exclusive 的转换" of the
+ *                  same tutorial)
+ *
+ * computed in ONE pass over the data by the single-pass scan with decoupled
+ * look-back ("Single-pass Parallel Prefix Scan with Decoupled Look-back",
+ * Merrill & Garland, summary page, sections 4.1 and 4.4): every input
+ * element is read once and every output element written once (~2n words).
+ *
+ * Arithmetic:
+ *   int32 / int64  two's-complement wraparound, i.e. the exact sum modulo
+ *                  2^32 / 2^64; results are bit-exact and deterministic.
+ *   fp32           IEEE single-precision additions.  The association order
+ *                  depends on run-time scheduling (section A6 of the paper
+ *                  summary), so results may differ in the last bits from run
+ *                  to run; NaN and Inf propagate as in IEEE arithmetic.
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers (in, out, ws) are DEVICE pointers owned by the
+ *     caller; the library allocates no device memory and keeps no state
+ *     between calls.
+ *   - `in`/`out` are contiguous arrays of n elements, aligned to their
+ *     element size.  16-byte aligned arrays take the vectorised path.
+ *   - in == out is an in-place scan and is allowed.  Any other overlap of
+ *     the two arrays, or of either with the workspace, is rejected with
+ *     PS_ERR_OVERLAP before anything is enqueued.
+ *   - `ws` is a scratch workspace of at least ps_scan_workspace_size(dtype,
+ *     n) bytes, 256-byte aligned.  It is reset by every call (an
+ *     asynchronous memset enqueued on `stream` before the kernel); two
+ *     calls that may run at the same time must not share one.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without waiting for it.
+ *   - n == 0 returns PS_OK, touches nothing and accepts NULL pointers.
+ *   - Errors detected on the host are returned before anything is
+ *     enqueued.  A failed CUDA runtime call yields PS_ERR_CUDA; its
+ *     cudaError_t is kept per thread and read with ps_last_cuda_error().
+ *   - A look-back that waits too long for a predecessor (which a correct
+ *     launch never does) gives up instead of hanging: the kernel records
+ *     PS_ERR_LOOKBACK_TIMEOUT in the workspace, writes unspecified output
+ *     and finishes.  Read it with ps_get_device_status().
+ */
+#ifndef PREFIX_SCAN_H
+#define PREFIX_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that the header needs no CUDA
+ * headers. */
+struct CUstream_st;
+typedef struct CUstream_st *ps_stream_t;
+
+typedef enum ps_status {
+    PS_OK = 0,
+    PS_ERR_INVALID_ARG = 1,         /* NULL pointer with n > 0, bad enum, misaligned pointer */
+    PS_ERR_WORKSPACE_TOO_SMALL = 2, /* ws_bytes < ps_scan_workspace_size(dtype, n) */
+    PS_ERR_OVERLAP = 3,             /* partial overlap of in/out, or ws overlapping either */
+    PS_ERR_CUDA = 4,                /* a CUDA runtime call failed: see ps_last_cuda_error() */
+    PS_ERR_LOOKBACK_TIMEOUT = 5     /* device side: a look-back gave up waiting */
+} ps_status;
+
+typedef enum ps_dtype { PS_INT32 = 0, PS_INT64 = 1, PS_FLOAT32 = 2 } ps_dtype;
+
+/*
+ * Bytes of workspace a scan of n elements of `dtype` needs (0 for n == 0):
+ * a 256-byte header (tile counter, status word) plus one status descriptor
+ * per tile (section 4.1, "partition descriptor": status flag X/A/P plus a
+ * value).  About n/512 bytes for 32-bit types.  The same size serves every
+ * algorithm below.
+ */
+size_t ps_scan_workspace_size(ps_dtype dtype, size_t n);
+
+/*
+ * Single-pass decoupled look-back scans (the product path).
+ * in   : device array of n input elements (read once)
+ * out  : device array of n output elements (written once; may equal in)
+ * n    : number of elements (any value up to 2^62)
+ * ws   : device workspace of ws_bytes >= ps_scan_workspace_size(...)
+ * stream: CUDA stream the work is enqueued on
+ */
+ps_status ps_scan_inclusive_i32(const int32_t *in, int32_t *out, size_t n,
+                                void *ws, size_t ws_bytes, ps_stream_t stream);
+ps_status ps_scan_exclusive_i32(const int32_t *in, int32_t *out, size_t n,
+                                void *ws, size_t ws_bytes, ps_stream_t stream);
+ps_status ps_scan_inclusive_i64(const int64_t *in, int64_t *out, size_t n,
+                                void *ws, size_t ws_bytes, ps_stream_t stream);
+ps_status ps_scan_exclusive_i64(const int64_t *in, int64_t *out, size_t n,
+                                void *ws, size_t ws_bytes, ps_stream_t stream);
+ps_status ps_scan_inclusive_f32(const float *in, float *out, size_t n,
+                                void *ws, size_t ws_bytes, ps_stream_t stream);
+ps_status ps_scan_exclusive_f32(const float *in, float *out, size_t n,
+                                void *ws, size_t ws_bytes, ps_stream_t stream);
+
+/*
+ * Global scan strategies.  PS_ALGO_DECOUPLED_LOOKBACK is the product path
+ * (the six named entry points above).  The other two exist for comparison
+ * only (paper summary, section 3.2 "global scan strategies"):
+ *   PS_ALGO_REDUCE_THEN_SCAN  three kernels -- tile reductions, a scan of
+ *                             the tile aggregates, a seeded re-scan of the
+ *                             input -- about 3n words of traffic;
+ *   PS_ALGO_CHAINED           single pass whose look-back waits for the
+ *                             immediate predecessor's inclusive prefix only
+ *                             (the "domino" scan with adjacent
+ *                             synchronisation of the PMPP single-pass page).
+ */
+typedef enum ps_algo {
+    PS_ALGO_DECOUPLED_LOOKBACK = 0,
+    PS_ALGO_REDUCE_THEN_SCAN = 1,
+    PS_ALGO_CHAINED = 2
+} ps_algo;
+
+/*
+ * Generic form of the scans above: `exclusive` selects the scan kind
+ * (0 = inclusive), in/out point to n elements of `dtype`.  Same
+ * conventions and errors; PS_ERR_INVALID_ARG for an unknown algo/dtype.
+ */
+ps_status ps_scan(ps_algo algo, ps_dtype dtype, int exclusive, const void *in, void *out,
+                  size_t n, void *ws, size_t ws_bytes, ps_stream_t stream);
+
+/*
+ * Waits for `stream`, then reads the device-side status the last scan
+ * that used `ws` left there (PS_OK or PS_ERR_LOOKBACK_TIMEOUT) into *out.
+ * Returns PS_ERR_CUDA if the wait or the copy fails.
+ */
+ps_status ps_get_device_status(const void *ws, ps_stream_t stream, ps_status *out);
+
+/* Static, human-readable name of a status code. */
+const char *ps_status_string(ps_status status);
+
+/* cudaError_t of the last PS_ERR_CUDA returned on the calling thread. */
+int ps_last_cuda_error(void);
+
+/* Elements per tile (one CTA's share) the decoupled look-back path uses. */
+size_t ps_tile_elements(ps_dtype dtype);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PREFIX_SCAN_H */

@@ -1,0 +1,112 @@
+"""PyTorch-facing wrappers of the C ABI.
+
+PyTorch only supplies device memory and streams here: tensors are passed to
+the library as raw device pointers with the current (or given) CUDA stream,
+and every step of the scan runs in ``libprefixscan.so``.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (PS_ALGO_CHAINED, PS_ALGO_DECOUPLED_LOOKBACK, PS_ALGO_REDUCE_THEN_SCAN,
+                   PS_FLOAT32, PS_INT32, PS_INT64)
+
+DTYPE_CODES = {torch.int32: PS_INT32, torch.int64: PS_INT64, torch.float32: PS_FLOAT32}
+_SUFFIX = {PS_INT32: "i32", PS_INT64: "i64", PS_FLOAT32: "f32"}
+ALGOS = {"decoupled": PS_ALGO_DECOUPLED_LOOKBACK,
+         "reduce_then_scan": PS_ALGO_REDUCE_THEN_SCAN,
+         "chained": PS_ALGO_CHAINED}
+
+
+def dtype_code(dtype: torch.dtype) -> int:
+    try:
+        return DTYPE_CODES[dtype]
+    except KeyError:
+        raise TypeError(f"prefix scan supports int32, int64 and float32, not {dtype}") from None
+
+
+def workspace_size(dtype: torch.dtype, n: int) -> int:
+    """Bytes of device workspace a scan of ``n`` elements needs."""
+    return int(_lib.load().ps_scan_workspace_size(dtype_code(dtype), n))
+
+
+def tile_elements(dtype: torch.dtype) -> int:
+    return int(_lib.load().ps_tile_elements(dtype_code(dtype)))
+
+
+def alloc_workspace(dtype: torch.dtype, n: int, device=None) -> torch.Tensor:
+    """A uint8 device tensor large enough for a scan of ``n`` elements."""
+    return torch.empty(max(workspace_size(dtype, n), 1), dtype=torch.uint8, device=device or "cuda")
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def scan(x: torch.Tensor, *, exclusive: bool = False, out: torch.Tensor | None = None,
+         inplace: bool = False, workspace: torch.Tensor | None = None, stream=None,
+         algo: str = "decoupled") -> torch.Tensor:
+    """Inclusive/exclusive sum scan of a contiguous 1-D CUDA tensor.
+
+    ``inplace=True`` writes the result over ``x``.  ``workspace`` (uint8,
+    on the same device) is allocated when not given.  The call is
+    asynchronous on ``stream`` (default: the current stream).
+    """
+    if not x.is_cuda:
+        raise ValueError("prefix scan: input must be a CUDA tensor (there is no CPU path)")
+    if x.dim() != 1 or not x.is_contiguous():
+        raise ValueError("prefix scan: input must be a contiguous 1-D tensor")
+    code = dtype_code(x.dtype)
+    n = x.numel()
+    if inplace:
+        if out is not None and out.data_ptr() != x.data_ptr():
+            raise ValueError("prefix scan: inplace=True and a distinct `out` are exclusive")
+        out = x
+    elif out is None:
+        out = torch.empty_like(x)
+    elif out.dtype != x.dtype or out.numel() != n or not out.is_contiguous() or out.device != x.device:
+        raise ValueError("prefix scan: `out` must match the input's dtype, length and device")
+    if n == 0:
+        return out
+    lib = _lib.load()
+    need = int(lib.ps_scan_workspace_size(code, n))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    elif workspace.numel() * workspace.element_size() < need or workspace.device != x.device:
+        raise ValueError(f"prefix scan: workspace needs {need} bytes on {x.device}")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    s = _stream_handle(stream, x.device)
+    if algo == "decoupled":
+        kind = "exclusive" if exclusive else "inclusive"
+        name = f"ps_scan_{kind}_{_SUFFIX[code]}"
+        st = getattr(lib, name)(x.data_ptr(), out.data_ptr(), n, workspace.data_ptr(), ws_bytes, s)
+    else:
+        name = "ps_scan"
+        st = lib.ps_scan(ALGOS[algo], code, int(exclusive), x.data_ptr(), out.data_ptr(), n,
+                         workspace.data_ptr(), ws_bytes, s)
+    _lib.check(name, st)
+    return out
+
+
+def scan_inclusive(x: torch.Tensor, out: torch.Tensor | None = None, **kw) -> torch.Tensor:
+    """y[i] = x[0] + ... + x[i] (device-wide, single pass)."""
+    return scan(x, exclusive=False, out=out, **kw)
+
+
+def scan_exclusive(x: torch.Tensor, out: torch.Tensor | None = None, **kw) -> torch.Tensor:
+    """y[0] = 0, y[i] = x[0] + ... + x[i-1] (device-wide, single pass)."""
+    return scan(x, exclusive=True, out=out, **kw)
+
+
+def device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Waits for the stream, returns the status the last scan left in ``workspace``."""
+    lib = _lib.load()
+    st = ctypes.c_int(0)
+    _lib.check("ps_get_device_status",
+               lib.ps_get_device_status(workspace.data_ptr(), _stream_handle(stream, workspace.device),
+                                        ctypes.byref(st)))
+    return st.value

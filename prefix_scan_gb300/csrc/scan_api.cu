@@ -1,0 +1,185 @@
+// scan_api.cu -- the library's C ABI: argument checks, workspace sizing,
+// dispatch to the launchers, status reporting.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+
+#include "prefix_scan.h"
+#include "prefix_scan_testing.h"
+#include "scan_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+ps_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return PS_ERR_CUDA;
+}
+
+bool valid_dtype(int dt) { return dt == PS_INT32 || dt == PS_INT64 || dt == PS_FLOAT32; }
+
+// Do byte ranges [a, a+an) and [b, b+bn) intersect?
+bool ranges_overlap(const void *a, size_t an, const void *b, size_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+ps_status check_args(ps_dtype dt, const void *in, const void *out, size_t n, const void *ws,
+                     size_t ws_bytes) {
+    if (!valid_dtype(dt)) return PS_ERR_INVALID_ARG;
+    if (in == nullptr || out == nullptr || ws == nullptr) return PS_ERR_INVALID_ARG;
+    const size_t es = ps::elem_bytes(dt);
+    if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % es != 0)
+        return PS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) % 16 != 0) return PS_ERR_INVALID_ARG;
+    if (n > (SIZE_MAX / 2) / es) return PS_ERR_INVALID_ARG;
+    if (ps::num_tiles(dt, n) > (size_t)INT_MAX) return PS_ERR_INVALID_ARG;
+    if (ws_bytes < ps::workspace_bytes(dt, n)) return PS_ERR_WORKSPACE_TOO_SMALL;
+    const size_t bytes = n * es;
+    if (in != out && ranges_overlap(in, bytes, out, bytes)) return PS_ERR_OVERLAP;
+    const size_t wsb = ps::workspace_bytes(dt, n);
+    if (ranges_overlap(ws, wsb, in, bytes) || ranges_overlap(ws, wsb, out, bytes)) return PS_ERR_OVERLAP;
+    return PS_OK;
+}
+
+template <typename T>
+ps_status run(ps_algo algo, bool exclusive, const void *in, void *out, size_t n, void *ws,
+              cudaStream_t s) {
+    cudaError_t e;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    switch (algo) {
+    case PS_ALGO_DECOUPLED_LOOKBACK:
+    case PS_ALGO_CHAINED: {
+        ps::PassArgs a{in, out, (unsigned long long)n, w, nullptr, nullptr, ps::kDefaultMaxPolls};
+        e = ps::launch_single_pass<T>(a, exclusive,
+                                      algo == PS_ALGO_CHAINED ? ps::Lookback::Chained
+                                                              : ps::Lookback::Decoupled, s);
+        break;
+    }
+    case PS_ALGO_REDUCE_THEN_SCAN:
+        e = ps::launch_reduce_then_scan<T>(in, out, (unsigned long long)n, w, exclusive, s);
+        break;
+    default:
+        return PS_ERR_INVALID_ARG;
+    }
+    return e == cudaSuccess ? PS_OK : cuda_fail(e);
+}
+
+ps_status dispatch(ps_algo algo, ps_dtype dt, int exclusive, const void *in, void *out, size_t n,
+                   void *ws, size_t ws_bytes, cudaStream_t s) {
+    if (!valid_dtype(dt)) return PS_ERR_INVALID_ARG;
+    if (algo != PS_ALGO_DECOUPLED_LOOKBACK && algo != PS_ALGO_REDUCE_THEN_SCAN && algo != PS_ALGO_CHAINED)
+        return PS_ERR_INVALID_ARG;
+    if (n == 0) return PS_OK;
+    const ps_status st = check_args(dt, in, out, n, ws, ws_bytes);
+    if (st != PS_OK) return st;
+    switch (dt) {
+    case PS_INT32: return run<int32_t>(algo, exclusive != 0, in, out, n, ws, s);
+    case PS_INT64: return run<int64_t>(algo, exclusive != 0, in, out, n, ws, s);
+    case PS_FLOAT32: return run<float>(algo, exclusive != 0, in, out, n, ws, s);
+    }
+    return PS_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ps_scan_workspace_size(ps_dtype dtype, size_t n) {
+    if (!valid_dtype(dtype)) return 0;
+    return ps::workspace_bytes(dtype, n);
+}
+
+size_t ps_tile_elements(ps_dtype dtype) {
+    if (!valid_dtype(dtype)) return 0;
+    return ps::tile_elems(dtype);
+}
+
+ps_status ps_scan(ps_algo algo, ps_dtype dtype, int exclusive, const void *in, void *out, size_t n,
+                  void *ws, size_t ws_bytes, ps_stream_t stream) {
+    return dispatch(algo, dtype, exclusive, in, out, n, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+#define PS_DEFINE_ENTRY(NAME, CTYPE, DT, EXCL)                                                   \
+    ps_status NAME(const CTYPE *in, CTYPE *out, size_t n, void *ws, size_t ws_bytes,             \
+                   ps_stream_t stream) {                                                         \
+        return dispatch(PS_ALGO_DECOUPLED_LOOKBACK, DT, EXCL, in, out, n, ws, ws_bytes,          \
+                        (cudaStream_t)stream);                                                   \
+    }
+PS_DEFINE_ENTRY(ps_scan_inclusive_i32, int32_t, PS_INT32, 0)
+PS_DEFINE_ENTRY(ps_scan_exclusive_i32, int32_t, PS_INT32, 1)
+PS_DEFINE_ENTRY(ps_scan_inclusive_i64, int64_t, PS_INT64, 0)
+PS_DEFINE_ENTRY(ps_scan_exclusive_i64, int64_t, PS_INT64, 1)
+PS_DEFINE_ENTRY(ps_scan_inclusive_f32, float, PS_FLOAT32, 0)
+PS_DEFINE_ENTRY(ps_scan_exclusive_f32, float, PS_FLOAT32, 1)
+#undef PS_DEFINE_ENTRY
+
+ps_status ps_get_device_status(const void *ws, ps_stream_t stream, ps_status *out) {
+    if (ws == nullptr || out == nullptr) return PS_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int st = 0;
+    e = cudaMemcpy(&st, static_cast<const unsigned char *>(ws) + offsetof(ps::Header, status),
+                   sizeof(st), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *out = (ps_status)st;
+    return PS_OK;
+}
+
+const char *ps_status_string(ps_status status) {
+    switch (status) {
+    case PS_OK: return "PS_OK";
+    case PS_ERR_INVALID_ARG: return "PS_ERR_INVALID_ARG";
+    case PS_ERR_WORKSPACE_TOO_SMALL: return "PS_ERR_WORKSPACE_TOO_SMALL";
+    case PS_ERR_OVERLAP: return "PS_ERR_OVERLAP";
+    case PS_ERR_CUDA: return "PS_ERR_CUDA";
+    case PS_ERR_LOOKBACK_TIMEOUT: return "PS_ERR_LOOKBACK_TIMEOUT";
+    }
+    return "PS_ERR_UNKNOWN";
+}
+
+int ps_last_cuda_error(void) { return g_last_cuda_error; }
+
+// ---- test hooks -------------------------------------------------------------
+
+size_t ps_testing_descriptor_bytes(ps_dtype dtype) {
+    if (!valid_dtype(dtype)) return 0;
+    return ps::desc_bytes(dtype);
+}
+
+ps_status ps_testing_encode_descriptor(ps_dtype dtype, int flag, const void *value, void *out) {
+    if (!valid_dtype(dtype) || value == nullptr || out == nullptr) return PS_ERR_INVALID_ARG;
+    if (flag != PS_FLAG_X && flag != PS_FLAG_A && flag != PS_FLAG_P) return PS_ERR_INVALID_ARG;
+    const uint64_t f = (uint64_t)flag << 32;
+    if (dtype == PS_INT64) {
+        uint64_t v;
+        std::memcpy(&v, value, 8);
+        const uint64_t w[2] = {f | (v & 0xffffffffull), f | (v >> 32)};
+        std::memcpy(out, w, 16);
+    } else {
+        uint32_t v;
+        std::memcpy(&v, value, 4);
+        const uint64_t w = f | v;
+        std::memcpy(out, &w, 8);
+    }
+    return PS_OK;
+}
+
+ps_status ps_testing_lookback(ps_dtype dtype, const void *desc, int64_t tile, uint32_t max_polls,
+                              void *result, uint32_t *status, ps_stream_t stream) {
+    if (!valid_dtype(dtype) || desc == nullptr || result == nullptr || status == nullptr || tile < 1)
+        return PS_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
+    switch (dtype) {
+    case PS_INT32: e = ps::launch_lookback_probe<int32_t>(desc, tile, max_polls, result, status, s); break;
+    case PS_INT64: e = ps::launch_lookback_probe<int64_t>(desc, tile, max_polls, result, status, s); break;
+    default: e = ps::launch_lookback_probe<float>(desc, tile, max_polls, result, status, s); break;
+    }
+    return e == cudaSuccess ? PS_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,257 @@
+// scan_single_pass.cu -- the single-pass scan kernel (decoupled look-back,
+// and the chained variant kept for comparison) and its launcher.
+//
+// One CTA scans one tile of kThreads * ITEMS consecutive elements:
+//   a1  the tile id comes from an atomic counter, not blockIdx, so a CTA
+//       only ever waits on tiles whose CTAs are already running (dynamic
+//       block index assignment, PMPP single-pass page, section "Dynamic
+//       Block Index Assignment"; "virtual processors", section 4.4 of the
+//       decoupled look-back paper summary);
+//   a2  warp w loads a contiguous 32*ITEMS-element segment with 16-byte
+//       loads: row r of the segment is 32 lanes x VEC elements, lane l
+//       holding elements r*32*VEC + l*VEC .. +VEC-1 (coalesced);
+//   a3  each thread scans its VEC elements of a row sequentially (the
+//       serial phase of the three-phase coarsened scan, PMPP
+//       work-efficient scan page, "Thread Coarsening");
+//   a4  a shuffle-based Kogge-Stone warp scan of the per-lane totals gives
+//       each lane its offset within the row; rows are chained in registers;
+//   a5  warp totals go through shared memory; each warp sums the totals of
+//       the warps before it, and every thread gets the tile aggregate;
+//   a6  warp 0 publishes the aggregate (A), or the inclusive prefix (P) for
+//       tile 0;
+//   a7  warp 0 runs the warp-parallel look-back to get the tile's exclusive
+//       prefix;
+//   a8  warp 0 publishes the inclusive prefix (P);
+//   a9  every thread adds tile prefix + warp offset + row/lane offset and
+//       stores its elements with 16-byte streaming stores.
+// Steps 1-6 of section 4.1 of the paper summary map to a0 (host memset of
+// the descriptors), a1..a5, a6, a7, a8 and a9.
+#include "scan_device.cuh"
+
+namespace ps {
+
+template <typename T, int THREADS, int ITEMS, bool EXCL, bool VEC_IO, Lookback LB>
+__global__ void __launch_bounds__(THREADS)
+single_pass_kernel(PassArgs a) {
+    using Tr = Traits<T>;
+    using U = typename Tr::U;
+    using V = typename Tr::V;
+    constexpr int VEC = Tr::VEC;
+    constexpr int ROWS = ITEMS / VEC;
+    constexpr int NW = THREADS / 32;
+    constexpr long long TILE = (long long)THREADS * ITEMS;
+    static_assert(ITEMS % VEC == 0, "ITEMS must be a multiple of the vector width");
+
+    __shared__ long long s_tile;
+    __shared__ U s_warp[NW];
+    __shared__ U s_excl;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    Header *hdr = reinterpret_cast<Header *>(a.ws);
+    void *desc = a.ws + kHeaderBytes;
+
+    // a1: dynamic tile id
+    long long tile;
+    if (LB == Lookback::Precomputed) {
+        tile = blockIdx.x;
+    } else {
+        if (tid == 0) s_tile = (long long)atomicAdd(&hdr->tile_counter, 1ull);
+        __syncthreads();
+        tile = s_tile;
+    }
+    const unsigned long long n = a.n;
+    const unsigned long long seg = (unsigned long long)tile * TILE + (unsigned long long)warp * 32 * ITEMS;
+    const T *in = reinterpret_cast<const T *>(a.in);
+    T *out = reinterpret_cast<T *>(a.out);
+    const bool full = (unsigned long long)(tile + 1) * TILE <= n;
+
+    // a2: load
+    U v[ROWS][VEC];
+    if (VEC_IO && full) {
+        const V *src = reinterpret_cast<const V *>(in + seg) + lane;
+        V buf[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) buf[r] = ld_stream(src + r * 32);
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) v[r][k] = (U)vget(buf[r], k);
+    } else {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) {
+                const unsigned long long i = seg + (unsigned long long)(r * 32 + lane) * VEC + k;
+                v[r][k] = i < n ? (U)in[i] : U(0);
+            }
+    }
+
+    // a3 + a4: per-thread sequential scan of each row chunk, warp scan of the
+    // chunk totals, rows chained in registers.
+    U off[ROWS];
+    U running = U(0);
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        U t;
+        if (EXCL) {
+            U acc = U(0);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) {
+                const U x = v[r][k];
+                v[r][k] = acc;
+                acc = acc + x;
+            }
+            t = acc;
+        } else {
+#pragma unroll
+            for (int k = 1; k < VEC; ++k) v[r][k] = v[r][k - 1] + v[r][k];
+            t = v[r][VEC - 1];
+        }
+        const U s = warp_inclusive<U>(t, lane);
+        U le = __shfl_up_sync(kFull, s, 1);
+        if (lane == 0) le = U(0);
+        const U row_total = __shfl_sync(kFull, s, 31);
+        off[r] = running + le;
+        running = running + row_total;
+    }
+
+    // a5: cross-warp scan through shared memory
+    if (lane == 0) s_warp[warp] = running;
+    __syncthreads();
+    U warp_excl = U(0), agg = U(0);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const U t = s_warp[w];
+        if (w < warp) warp_excl = warp_excl + t;
+        agg = agg + t;
+    }
+
+    // a6..a8: publish, look back, publish
+    if (LB == Lookback::Precomputed) {
+        if (tid == 0) s_excl = reinterpret_cast<const U *>(desc)[tile];
+    } else if (warp == 0) {
+        U excl;
+        if (tile == 0) {
+            excl = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
+            if (lane == 0) Desc<U, Tr::DW>::store(desc, 0, kFlagP, excl + agg);
+        } else {
+            if (LB == Lookback::Decoupled && lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg);
+            excl = look_back<U, Tr::DW, LB == Lookback::Chained>(desc, tile, a.max_polls, &hdr->status);
+            if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg);
+        }
+        if (lane == 0) {
+            s_excl = excl;
+            const long long last = (long long)((n + TILE - 1) / TILE) - 1;
+            if (a.carry_out && tile == last) *reinterpret_cast<U *>(a.carry_out) = excl + agg;
+        }
+    }
+    __syncthreads();
+
+    // a9: seeded output
+    const U base = s_excl + warp_excl;
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const U o = base + off[r];
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) v[r][k] = o + v[r][k];
+    }
+    if (VEC_IO && full) {
+        V *dst = reinterpret_cast<V *>(out + seg) + lane;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            V w;
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) vset(w, k, v[r][k]);
+            st_stream(dst + r * 32, w);
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) {
+                const unsigned long long i = seg + (unsigned long long)(r * 32 + lane) * VEC + k;
+                if (i < n) out[i] = (T)v[r][k];
+            }
+    }
+}
+
+template <typename T> struct ItemsOf { static constexpr int value = kItems32; };
+template <> struct ItemsOf<int64_t> { static constexpr int value = kItems64; };
+
+template <typename T, bool EXCL, bool VEC_IO, Lookback LB>
+cudaError_t launch_variant(const PassArgs &a, size_t tiles, cudaStream_t s) {
+    constexpr int ITEMS = ItemsOf<T>::value;
+    single_pass_kernel<T, kThreads, ITEMS, EXCL, VEC_IO, LB>
+        <<<(unsigned int)tiles, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, bool EXCL, Lookback LB>
+cudaError_t launch_kind(const PassArgs &a, bool vec_io, size_t tiles, cudaStream_t s) {
+    return vec_io ? launch_variant<T, EXCL, true, LB>(a, tiles, s)
+                  : launch_variant<T, EXCL, false, LB>(a, tiles, s);
+}
+
+template <typename T> constexpr ps_dtype dtype_of();
+template <> constexpr ps_dtype dtype_of<int32_t>() { return PS_INT32; }
+template <> constexpr ps_dtype dtype_of<int64_t>() { return PS_INT64; }
+template <> constexpr ps_dtype dtype_of<float>() { return PS_FLOAT32; }
+
+template <typename T>
+cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s) {
+    constexpr ps_dtype dt = dtype_of<T>();
+    const size_t tiles = num_tiles(dt, a.n);
+    // a0: every descriptor to X, tile counter and status to zero
+    cudaError_t e = cudaMemsetAsync(a.ws, 0, kHeaderBytes + tiles * desc_bytes(dt), s);
+    if (e != cudaSuccess) return e;
+    const bool vec_io = ((reinterpret_cast<uintptr_t>(a.in) | reinterpret_cast<uintptr_t>(a.out)) & 15u) == 0;
+    if (lb == Lookback::Decoupled)
+        return exclusive ? launch_kind<T, true, Lookback::Decoupled>(a, vec_io, tiles, s)
+                         : launch_kind<T, false, Lookback::Decoupled>(a, vec_io, tiles, s);
+    return exclusive ? launch_kind<T, true, Lookback::Chained>(a, vec_io, tiles, s)
+                     : launch_kind<T, false, Lookback::Chained>(a, vec_io, tiles, s);
+}
+
+// The seeded tile scan of the reduce-then-scan comparison path (its third
+// kernel) is this kernel with Lookback::Precomputed.
+template <typename T>
+cudaError_t launch_seeded_tile_scan(const PassArgs &a, bool exclusive, cudaStream_t s) {
+    const size_t tiles = num_tiles(dtype_of<T>(), a.n);
+    const bool vec_io = ((reinterpret_cast<uintptr_t>(a.in) | reinterpret_cast<uintptr_t>(a.out)) & 15u) == 0;
+    return exclusive ? launch_kind<T, true, Lookback::Precomputed>(a, vec_io, tiles, s)
+                     : launch_kind<T, false, Lookback::Precomputed>(a, vec_io, tiles, s);
+}
+template cudaError_t launch_seeded_tile_scan<int32_t>(const PassArgs &, bool, cudaStream_t);
+template cudaError_t launch_seeded_tile_scan<int64_t>(const PassArgs &, bool, cudaStream_t);
+template cudaError_t launch_seeded_tile_scan<float>(const PassArgs &, bool, cudaStream_t);
+
+template cudaError_t launch_single_pass<int32_t>(const PassArgs &, bool, Lookback, cudaStream_t);
+template cudaError_t launch_single_pass<int64_t>(const PassArgs &, bool, Lookback, cudaStream_t);
+template cudaError_t launch_single_pass<float>(const PassArgs &, bool, Lookback, cudaStream_t);
+
+// ---- test hook: the look-back alone -----------------------------------------
+template <typename T>
+__global__ void lookback_probe_kernel(const void *desc, long long tile, uint32_t max_polls,
+                                      void *result, unsigned int *status) {
+    using U = typename Traits<T>::U;
+    const U excl = look_back<U, Traits<T>::DW, false>(desc, tile, max_polls, status);
+    if (threadIdx.x == 0) *reinterpret_cast<U *>(result) = excl;
+}
+
+template <typename T>
+cudaError_t launch_lookback_probe(const void *desc, long long tile, uint32_t max_polls,
+                                  void *result, unsigned int *status, cudaStream_t s) {
+    lookback_probe_kernel<T><<<1, 32, 0, s>>>(desc, tile, max_polls, result, status);
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_lookback_probe<int32_t>(const void *, long long, uint32_t, void *,
+                                                    unsigned int *, cudaStream_t);
+template cudaError_t launch_lookback_probe<int64_t>(const void *, long long, uint32_t, void *,
+                                                    unsigned int *, cudaStream_t);
+template cudaError_t launch_lookback_probe<float>(const void *, long long, uint32_t, void *,
+                                                  unsigned int *, cudaStream_t);
+
+}  // namespace ps

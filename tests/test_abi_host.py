@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function the headers declare, sizes workspaces as documented, and
+rejects bad arguments before it enqueues anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from prefix_scan_gb300 import _lib
+from prefix_scan_gb300 import build as nvbuild
+
+INCLUDE = Path(__file__).resolve().parents[1] / "include"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not nvbuild.is_fresh():
+        try:
+            nvbuild.build()
+        except RuntimeError as e:  # pragma: no cover - toolchain missing
+            pytest.skip(f"cannot build the CUDA library here: {e}")
+    return _lib.load()
+
+
+def declared_functions() -> set[str]:
+    names = set()
+    for h in INCLUDE.glob("*.h"):
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(ps_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "ps_scan_inclusive_i32" in names and len(names) >= 15
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding declares exactly what the headers declare
+    assert names == set(_lib.SIGNATURES), names ^ set(_lib.SIGNATURES)
+
+
+def test_workspace_size(lib):
+    assert lib.ps_scan_workspace_size(0, 0) == 0
+    for code in (0, 1, 2):
+        T = lib.ps_tile_elements(code)
+        db = lib.ps_testing_descriptor_bytes(code)
+        assert T > 0 and T % 32 == 0
+        for n in (1, T, T + 1, 1 << 30):
+            tiles = -(-n // T)
+            need = lib.ps_scan_workspace_size(code, n)
+            assert need >= 256 + tiles * db and need % 256 == 0
+    assert lib.ps_scan_workspace_size(7, 100) == 0
+
+
+FAKE = 1 << 40  # never dereferenced: every call below fails validation first
+
+
+def test_argument_errors(lib):
+    ws_need = lib.ps_scan_workspace_size(0, 1000)
+    f = lib.ps_scan_inclusive_i32
+    assert f(None, None, 0, None, 0, None) == _lib.PS_OK                       # n == 0: no-op
+    assert f(None, FAKE, 1000, FAKE + (1 << 20), ws_need, None) == _lib.PS_ERR_INVALID_ARG
+    assert f(FAKE, None, 1000, FAKE + (1 << 20), ws_need, None) == _lib.PS_ERR_INVALID_ARG
+    assert f(FAKE, FAKE + 8192, 1000, None, ws_need, None) == _lib.PS_ERR_INVALID_ARG
+    assert f(FAKE + 2, FAKE + 8192, 1000, FAKE + (1 << 20), ws_need, None) == _lib.PS_ERR_INVALID_ARG
+    assert f(FAKE, FAKE + 8192, 1000, FAKE + (1 << 20) + 8, ws_need, None) == _lib.PS_ERR_INVALID_ARG
+    assert f(FAKE, FAKE + 8192, 1000, FAKE + (1 << 20), ws_need - 1, None) == \
+        _lib.PS_ERR_WORKSPACE_TOO_SMALL
+    # partial overlap of in/out, and workspace overlapping the data
+    assert f(FAKE, FAKE + 400, 1000, FAKE + (1 << 20), ws_need, None) == _lib.PS_ERR_OVERLAP
+    assert f(FAKE, FAKE + 8192, 1000, FAKE + 8192 + 3200, ws_need, None) == _lib.PS_ERR_OVERLAP
+    assert f(FAKE, FAKE + 8192, 1000, FAKE + 256, ws_need, None) == _lib.PS_ERR_OVERLAP
+    # generic entry: bad enums
+    g = lib.ps_scan
+    assert g(9, 0, 0, FAKE, FAKE + 8192, 1000, FAKE + (1 << 20), ws_need, None) == _lib.PS_ERR_INVALID_ARG
+    assert g(0, 9, 0, FAKE, FAKE + 8192, 1000, FAKE + (1 << 20), ws_need, None) == _lib.PS_ERR_INVALID_ARG
+    # int64 misalignment is checked against 8 bytes
+    ws64 = lib.ps_scan_workspace_size(1, 1000)
+    assert lib.ps_scan_inclusive_i64(FAKE + 4, FAKE + 16384, 1000, FAKE + (1 << 20), ws64, None) == \
+        _lib.PS_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for code, name in [(0, b"PS_OK"), (1, b"PS_ERR_INVALID_ARG"), (2, b"PS_ERR_WORKSPACE_TOO_SMALL"),
+                       (3, b"PS_ERR_OVERLAP"), (4, b"PS_ERR_CUDA"), (5, b"PS_ERR_LOOKBACK_TIMEOUT")]:
+        assert lib.ps_status_string(code) == name
+
+
+def test_descriptor_encoding(lib):
+    # flag in the high half of each 64-bit word, value bits in the low half
+    import numpy as np
+    buf = (ctypes.c_char * 16)()
+    v32 = np.array([-7], dtype=np.int32)
+    assert lib.ps_testing_encode_descriptor(0, 2, v32.ctypes.data, buf) == 0
+    w = np.frombuffer(bytes(buf)[:8], dtype=np.uint64)[0]
+    assert int(w) >> 32 == 2 and int(w) & 0xFFFFFFFF == (-7) & 0xFFFFFFFF
+    v64 = np.array([-(1 << 40) - 3], dtype=np.int64)
+    assert lib.ps_testing_encode_descriptor(1, 1, v64.ctypes.data, buf) == 0
+    w0, w1 = np.frombuffer(bytes(buf), dtype=np.uint64)
+    u = int(v64.view(np.uint64)[0])
+    assert int(w0) >> 32 == 1 and int(w1) >> 32 == 1
+    assert (int(w0) & 0xFFFFFFFF) | ((int(w1) & 0xFFFFFFFF) << 32) == u
+    assert lib.ps_testing_encode_descriptor(0, 3, v32.ctypes.data, buf) == _lib.PS_ERR_INVALID_ARG
+
+
+def test_python_layer_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    from prefix_scan_gb300 import api
+    with pytest.raises(ValueError, match="CUDA"):
+        api.scan_inclusive(torch.arange(10, dtype=torch.int32))

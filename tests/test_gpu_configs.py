@@ -1,0 +1,56 @@
+"""GPU parity at the full workload sizes, through the same C-ABI call the
+bench times: int32 2^20, fp32 2^24, int32 exclusive 2^28 (0/1 flags),
+int64 2^29, and the in-place int32 length sweep up to 2^30.  Every output
+element is compared with the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import fp32_ok
+from prefix_scan_gb300 import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from prefix_scan_gb300 import api  # noqa: E402
+
+DEV = torch.device("cuda:0")
+
+
+def _run_and_check(w: workloads.Workload, n: int) -> None:
+    x = w.make(n)
+    t = torch.from_numpy(x).to(DEV)
+    y = api.scan(t, exclusive=w.exclusive, inplace=w.inplace)
+    if w.inplace:
+        assert y.data_ptr() == t.data_ptr()
+    got = y.cpu().numpy()
+    del t, y
+    if x.dtype == np.float32:
+        bad = np.flatnonzero(~fp32_ok(got, x, w.exclusive))
+        assert bad.size == 0, f"{w.name} n={n}: {bad.size} fp32 elements out of bound"
+    else:
+        ref = oracle.exclusive(x) if w.exclusive else oracle.inclusive(x)
+        bad = np.flatnonzero(got != ref)
+        assert bad.size == 0, f"{w.name} n={n}: {bad.size} mismatches, first at {bad[:5]}"
+    if w.dist == "bern" and w.exclusive:
+        # compaction offsets: non-decreasing, last + last flag = popcount
+        assert np.all(np.diff(got) >= 0)
+        assert int(got[-1]) + int(x[-1]) == int(x.sum())
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("w", [workloads.SMALL_I32, workloads.F32_2P24, workloads.I32_EXCL_2P28,
+                               workloads.I64_2P29], ids=lambda w: w.name)
+def test_workload_full_size(w):
+    _run_and_check(w, w.n)
+
+
+@pytest.mark.parametrize("n", workloads.I32_INPLACE_SWEEP.sweep)
+def test_inplace_length_sweep(n):
+    _run_and_check(workloads.I32_INPLACE_SWEEP, n)
