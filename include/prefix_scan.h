@@ -145,6 +145,38 @@ int ps_last_cuda_error(void);
 /* Elements per tile (one CTA's share) the decoupled look-back path uses. */
 size_t ps_tile_elements(ps_dtype dtype);
 
+/*
+ * Allocation-free int32 inclusive scan.  The pages have no counterpart: it
+ * exists for callers that cannot allocate device memory at all -- code
+ * running inside an allocator or memory-pool callback, plug-ins whose host
+ * application owns every device allocation, paths that must never reach
+ * the allocator -- and so cannot supply the workspace the entry points
+ * above take.
+ *
+ * Same computation and conventions as ps_scan_inclusive_i32, except that the
+ * look-back scratch lives in a fixed array inside the library's device
+ * memory (PS_NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library
+ * until the process exits) instead of a caller workspace.  Nothing is
+ * allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - n > PS_NOALLOC_MAX_ELEMENTS returns PS_ERR_WORKSPACE_TOO_SMALL before
+ *     anything is enqueued (the fixed scratch holds descriptors for at most
+ *     that many elements).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.  A failed look-up returns PS_ERR_CUDA
+ *     (see ps_last_cuda_error).
+ *   - All calls on a device share the one array and every call clears it on
+ *     `stream` before use.  Calls whose GPU work can overlap (other streams,
+ *     unordered host threads) race on it and produce wrong results; calls
+ *     ordered on one stream are safe.
+ *   - Device-side timeouts can be read with ps_get_device_status only
+ *     through the regular entry points (there is no caller workspace here).
+ */
+#define PS_NOALLOC_MAX_ELEMENTS 536870912u /* 2^29 elements */
+#define PS_NOALLOC_SCRATCH_BYTES (256u + 8u * (PS_NOALLOC_MAX_ELEMENTS / 4096u))
+ps_status ps_scan_inclusive_i32_noalloc(const int32_t *in, int32_t *out, size_t n,
+                                        ps_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

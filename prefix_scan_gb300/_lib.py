@@ -37,6 +37,9 @@ SIGNATURES = {
     "ps_testing_encode_descriptor": (_int, [_int, _int, _vp, _vp]),
     "ps_testing_lookback": (_int, [_int, _vp, _i64, _u32, _vp, _vp, _vp]),
 }
+SIGNATURES["ps_scan_inclusive_i32_noalloc"] = (_int, [_vp, _vp, _sz, _vp])
+PS_NOALLOC_MAX_ELEMENTS = 1 << 29
+
 for _kind in ("inclusive", "exclusive"):
     for _t in ("i32", "i64", "f32"):
         SIGNATURES[f"ps_scan_{_kind}_{_t}"] = (_int, [_vp, _vp, _sz, _vp, _sz, _vp])

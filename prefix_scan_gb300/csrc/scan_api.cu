@@ -86,6 +86,8 @@ ps_status dispatch(ps_algo algo, ps_dtype dt, int exclusive, const void *in, voi
 
 }  // namespace
 
+void ps::note_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
 extern "C" {
 
 size_t ps_scan_workspace_size(ps_dtype dtype, size_t n) {

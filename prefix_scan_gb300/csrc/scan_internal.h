@@ -85,4 +85,7 @@ template <typename T>
 cudaError_t launch_lookback_probe(const void *desc, long long tile, uint32_t max_polls,
                                   void *result, unsigned int *status, cudaStream_t s);
 
+// Records `e` as the calling thread's last CUDA error (ps_last_cuda_error).
+void note_cuda_error(cudaError_t e);
+
 }  // namespace ps
