@@ -116,11 +116,13 @@ template <typename U, int DW> struct Desc;
 template <typename U> struct Desc<U, 1> {
     static __device__ __forceinline__ void store(void *base, long long i, uint32_t flag, U v) {
         unsigned long long w = ((unsigned long long)flag << 32) | to_bits(v);
-        unsigned long long *p = reinterpret_cast<unsigned long long *>(base) + i;
+        unsigned long long *p = reinterpret_cast<unsigned long long *>(
+            reinterpret_cast<unsigned char *>(base) + i * kDescStride32);
         asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(w) : "memory");
     }
     static __device__ __forceinline__ void load(const void *base, long long i, uint32_t &flag, U &v) {
-        const unsigned long long *p = reinterpret_cast<const unsigned long long *>(base) + i;
+        const unsigned long long *p = reinterpret_cast<const unsigned long long *>(
+            reinterpret_cast<const unsigned char *>(base) + i * kDescStride32);
         unsigned long long w;
         asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
         flag = (uint32_t)(w >> 32);
@@ -133,12 +135,14 @@ template <> struct Desc<unsigned long long, 2> {
     static __device__ __forceinline__ void store(void *base, long long i, uint32_t flag, U v) {
         unsigned long long f = (unsigned long long)flag << 32;
         unsigned long long w0 = f | (v & 0xffffffffull), w1 = f | (v >> 32);
-        unsigned long long *p = reinterpret_cast<unsigned long long *>(base) + 2 * i;
+        unsigned long long *p = reinterpret_cast<unsigned long long *>(
+            reinterpret_cast<unsigned char *>(base) + i * kDescStride64);
         asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1,%2};" :: "l"(p), "l"(w0), "l"(w1)
                      : "memory");
     }
     static __device__ __forceinline__ void load(const void *base, long long i, uint32_t &flag, U &v) {
-        const unsigned long long *p = reinterpret_cast<const unsigned long long *>(base) + 2 * i;
+        const unsigned long long *p = reinterpret_cast<const unsigned long long *>(
+            reinterpret_cast<const unsigned char *>(base) + i * kDescStride64);
         unsigned long long w0, w1;
         asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p)
                      : "memory");
@@ -170,24 +174,32 @@ template <> __device__ __forceinline__ uint32_t warp_sum<uint32_t>(uint32_t v) {
     return __reduce_add_sync(kFull, v);
 }
 
+// Sleep between polls of a descriptor that is not ready yet.
+__device__ __forceinline__ void poll_backoff(uint32_t polls) {
+    if (polls > PS_SPIN_POLLS)
+        __nanosleep(polls > PS_SLEEP_AFTER_LONG ? PS_SLEEP_NS_LONG : PS_SLEEP_NS_SHORT);
+}
+
 // ---- look-back ---------------------------------------------------------------
 // Warp-parallel decoupled look-back (section 4.1 step "determine the
-// exclusive prefix" with the parallelised form of section 4.4): lane k
-// inspects the descriptor of tile base-k.  The warp polls until no lane sees
-// X; if some lane sees P, the nearest such tile ends the look-back and the
-// values of the tiles from it up to base are summed (the segmented reduction
-// with the P tile as head); otherwise all 32 aggregates are summed and the
-// window slides back by 32 tiles.  Lanes before tile 0 read as P with the
-// identity, which never decides anything because tile 0 only ever publishes
-// P.
-//
-// CHAINED restricts the window to the immediate predecessor and waits for
-// its P (the chained scan of section 3.2; comparison path only).
+// exclusive prefix", in the parallelised form of section 4.4), widened so
+// that each lane inspects K consecutive predecessors: position p = lane*K + j
+// of the window is tile base - p.  Per round the warp finds the nearest X and
+// the nearest P in the window:
+//   - an X nearer than every P: re-poll the X descriptors (bounded);
+//   - otherwise, a P exists: the values at positions up to and including the
+//     nearest P are summed (the segmented reduction with the P tile as the
+//     head) and the look-back ends -- X descriptors beyond that P are
+//     irrelevant and are not waited for;
+//   - otherwise all 32*K are A: they are summed and the window slides back
+//     32*K tiles.
+// Tiles before tile 0 read as P with the identity; they never decide
+// anything because tile 0 only ever publishes P.
 //
 // A poll cap bounds every wait.  When it is exceeded the status word gets
-// PS_ERR_LOOKBACK_TIMEOUT and still-missing tiles count as P with the
+// PS_ERR_LOOKBACK_TIMEOUT and the missing tiles count as P with the
 // identity, so the warp finishes (with a wrong value) instead of hanging.
-template <typename U, int DW, bool CHAINED>
+template <typename U, int DW, int K>
 __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_t max_polls,
                                        unsigned int *status) {
     const int lane = threadIdx.x & 31;
@@ -196,34 +208,92 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
     uint32_t polls = 0;
     bool gave_up = false;
     while (true) {
-        const long long idx = base - lane;
-        const bool active = CHAINED ? (lane == 0) : true;
-        uint32_t flag = kFlagP;
-        U val = U(0);
-        if (active && idx >= 0) Desc<U, DW>::load(desc, idx, flag, val);
-        // poll until every inspected tile has published something
-        // (CHAINED: until the predecessor has published its prefix)
-        unsigned pending;
-        while ((pending = __ballot_sync(kFull, CHAINED ? (flag != kFlagP) : (flag == kFlagX))) != 0u) {
-            if (++polls > max_polls) {
-                gave_up = true;
-                if (pending & (1u << lane)) { flag = kFlagP; val = U(0); }
-                break;
-            }
-            if (polls > 8) __nanosleep(polls > 64 ? 512 : 32);
-            if (pending & (1u << lane)) Desc<U, DW>::load(desc, idx, flag, val);
+        uint32_t f[K];
+        U v[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const long long idx = base - (long long)(lane * K + j);
+            f[j] = kFlagP;
+            v[j] = U(0);
+            if (idx >= 0) Desc<U, DW>::load(desc, idx, f[j], v[j]);
         }
-        const unsigned pmask = __ballot_sync(kFull, flag == kFlagP);
-        if (pmask != 0u) {
-            const int first = __ffs(pmask) - 1;
-            excl = warp_sum<U>(lane <= first ? val : U(0)) + excl;
+        bool done;
+        while (true) {
+            int px = K, pp = K;   // nearest X / P of this lane (K = none)
+#pragma unroll
+            for (int j = K - 1; j >= 0; --j) {
+                if (f[j] == kFlagX) px = j;
+                if (f[j] == kFlagP) pp = j;
+            }
+            const unsigned mx = __ballot_sync(kFull, px < K);
+            const unsigned mp = __ballot_sync(kFull, pp < K);
+            int pos_x = 0x7fffffff, pos_p = 0x7fffffff;
+            if (mx) {
+                const int l = __ffs(mx) - 1;
+                pos_x = l * K + __shfl_sync(kFull, px, l);
+            }
+            if (mp) {
+                const int l = __ffs(mp) - 1;
+                pos_p = l * K + __shfl_sync(kFull, pp, l);
+            }
+            if (pos_x < pos_p) {   // a nearer tile has not published yet
+                if (++polls > max_polls) {
+                    gave_up = true;
+#pragma unroll
+                    for (int j = 0; j < K; ++j)
+                        if (f[j] == kFlagX) { f[j] = kFlagP; v[j] = U(0); }
+                    continue;
+                }
+                poll_backoff(polls);
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    const int pos = lane * K + j;
+                    if (f[j] == kFlagX && pos < pos_p)
+                        Desc<U, DW>::load(desc, base - (long long)pos, f[j], v[j]);
+                }
+                continue;
+            }
+            // no X before the nearest P (or neither X nor P in the window)
+            const int limit = mp ? pos_p : 0x7fffffff;
+            U part = U(0);
+#pragma unroll
+            for (int j = K - 1; j >= 0; --j)   // farther tiles on the left
+                if (lane * K + j <= limit) part = v[j] + part;
+            excl = warp_sum<U>(part) + excl;
+            done = (mp != 0u);
             break;
         }
-        excl = warp_sum<U>(val) + excl;
-        base -= 32;
+        if (done) break;
+        base -= 32 * K;
     }
     if (gave_up && lane == 0) atomicMax(status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
     return excl;
+}
+
+// Chained scan (section 3.2 of the paper summary; the adjacent
+// synchronisation of the PMPP single-pass page): wait for the immediate
+// predecessor's inclusive prefix.  Comparison path only; bounded like the
+// look-back.
+template <typename U, int DW>
+__device__ __forceinline__ U chained_wait(const void *desc, long long tile, uint32_t max_polls,
+                                          unsigned int *status) {
+    const int lane = threadIdx.x & 31;
+    uint32_t flag = kFlagX;
+    U val = U(0);
+    uint32_t polls = 0;
+    if (lane == 0) {
+        Desc<U, DW>::load(desc, tile - 1, flag, val);
+        while (flag != kFlagP) {
+            if (++polls > max_polls) {
+                atomicMax(status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+                val = U(0);
+                break;
+            }
+            poll_backoff(polls);
+            Desc<U, DW>::load(desc, tile - 1, flag, val);
+        }
+    }
+    return __shfl_sync(kFull, val, 0);
 }
 
 }  // namespace ps

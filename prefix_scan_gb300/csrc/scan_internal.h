@@ -25,20 +25,71 @@ struct Header {
 constexpr size_t kHeaderBytes = 256;
 static_assert(sizeof(Header) <= kHeaderBytes, "header too large");
 
-// Tile geometry of the decoupled look-back path: THREADS threads per CTA,
-// ITEMS consecutive-in-rows elements per thread.
-constexpr int kThreads = 256;
-constexpr int kItems32 = 16;   // int32 / fp32: 4096-element tiles (16 KiB)
-constexpr int kItems64 = 8;    // int64: 2048-element tiles (16 KiB)
+// Tile geometry: THREADS scanning threads per tile, ITEMS elements per
+// thread (in rows of 16-byte vectors): 8192-element tiles for 32-bit types,
+// 4096 for int64 -- 32 KiB either way.  The look-back window is 32 lanes x
+// LOOKBACK_K descriptors.  The persistent kernel keeps STAGES tiles of
+// shared memory per CTA and runs CTAS_PER_SM CTAs per SM.  The macros only
+// exist so that a tuning sweep can rebuild with other values.
+#ifndef PS_THREADS
+#define PS_THREADS 256
+#endif
+#ifndef PS_ITEMS32
+#define PS_ITEMS32 32
+#endif
+#ifndef PS_ITEMS64
+#define PS_ITEMS64 16
+#endif
+#ifndef PS_PERSIST_STAGES
+#define PS_PERSIST_STAGES 3
+#endif
+#ifndef PS_PERSIST_CTAS_PER_SM
+#define PS_PERSIST_CTAS_PER_SM 2
+#endif
+#ifndef PS_LOOKBACK_K
+#define PS_LOOKBACK_K 1
+#endif
+// Poll back-off of the look-back: spin PS_SPIN_POLLS polls, then sleep
+// PS_SLEEP_NS_SHORT per poll, and PS_SLEEP_NS_LONG once past
+// PS_SLEEP_AFTER_LONG polls.  Sleeping keeps hundreds of spinning warps from
+// saturating the L2 slices that hold neighbouring descriptors.
+#ifndef PS_SPIN_POLLS
+#define PS_SPIN_POLLS 8
+#endif
+#ifndef PS_SLEEP_NS_SHORT
+#define PS_SLEEP_NS_SHORT 32
+#endif
+#ifndef PS_SLEEP_AFTER_LONG
+#define PS_SLEEP_AFTER_LONG 64
+#endif
+#ifndef PS_SLEEP_NS_LONG
+#define PS_SLEEP_NS_LONG 512
+#endif
+// Bytes between consecutive tile descriptors.  Packed 8-byte descriptors
+// put 16 neighbouring tiles on one 128-byte L2 line, which every publish
+// and every look-back of those tiles then contends for; one descriptor per
+// 32-byte sector measured fastest on GB300.  64-bit types use at least 16.
+#ifndef PS_DESC_STRIDE
+#define PS_DESC_STRIDE 32
+#endif
+constexpr int kDescStride32 = PS_DESC_STRIDE;
+constexpr int kDescStride64 = PS_DESC_STRIDE < 16 ? 16 : PS_DESC_STRIDE;
+static_assert(PS_DESC_STRIDE % 8 == 0, "descriptor stride must be a multiple of 8");
+constexpr int kThreads = PS_THREADS;
+constexpr int kItems32 = PS_ITEMS32;   // int32 / fp32 elements per thread
+constexpr int kItems64 = PS_ITEMS64;   // int64 elements per thread
+constexpr int kLookbackK = PS_LOOKBACK_K;
+constexpr int kPStages = PS_PERSIST_STAGES;
+constexpr int kPCtasPerSm = PS_PERSIST_CTAS_PER_SM;
 
-inline size_t tile_elems(ps_dtype dt) {
+constexpr size_t tile_elems(ps_dtype dt) {
     return (size_t)kThreads * (dt == PS_INT64 ? kItems64 : kItems32);
 }
-inline size_t elem_bytes(ps_dtype dt) { return dt == PS_INT64 ? 8 : 4; }
-inline size_t desc_bytes(ps_dtype dt) { return dt == PS_INT64 ? 16 : 8; }
-inline size_t num_tiles(ps_dtype dt, size_t n) { return (n + tile_elems(dt) - 1) / tile_elems(dt); }
-inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-inline size_t workspace_bytes(ps_dtype dt, size_t n) {
+constexpr size_t elem_bytes(ps_dtype dt) { return dt == PS_INT64 ? 8 : 4; }
+constexpr size_t desc_bytes(ps_dtype dt) { return dt == PS_INT64 ? kDescStride64 : kDescStride32; }
+constexpr size_t num_tiles(ps_dtype dt, size_t n) { return (n + tile_elems(dt) - 1) / tile_elems(dt); }
+constexpr size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+constexpr size_t workspace_bytes(ps_dtype dt, size_t n) {
     if (n == 0) return 0;
     return kHeaderBytes + round_up(num_tiles(dt, n) * desc_bytes(dt), 256);
 }
@@ -65,8 +116,13 @@ struct PassArgs {
     uint32_t max_polls;
 };
 
+// Enqueue the persistent TMA-fed single-pass kernel (16-byte aligned in/out).
+template <typename T>
+cudaError_t launch_persistent(const PassArgs &a, bool exclusive, cudaStream_t s);
+
 // Enqueue one single-pass scan (workspace reset + kernel).  T is int32_t,
-// int64_t or float.
+// int64_t or float.  Decoupled look-back on 16-byte aligned arrays runs the
+// persistent kernel; otherwise one CTA per tile.
 template <typename T>
 cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s);
 

@@ -6,13 +6,13 @@
 // or a memory-pool callback, in a plug-in whose host application owns all
 // device memory, in a hot path that must never touch the allocator), or a
 // caller that simply cannot size and keep a workspace buffer.  For them this
-// file keeps the look-back scratch (the 256-byte header plus one 8-byte
-// status descriptor per 4096-element tile) in a fixed array in the
-// library's own device memory, so the call needs only the input and output.
+// file keeps the look-back scratch (the 256-byte header plus one status
+// descriptor slot per tile) in a fixed array in the library's own device
+// memory, so the call needs only the input and output.
 //
 // Consequences of a file-scope device array:
-//   - every GPU that loads this library holds the array (1 MiB + 256 bytes)
-//     until the process exits;
+//   - every GPU that loads this library holds the array
+//     (PS_NOALLOC_SCRATCH_BYTES, 2 MiB + 256 bytes) until the process exits;
 //   - all calls on a device share it: two calls whose work overlaps on the
 //     GPU (different streams, or different host threads without ordering)
 //     race on it and give wrong results; calls on one stream are ordered and
@@ -29,14 +29,16 @@
 
 namespace {
 
-constexpr size_t kNoallocMaxTiles = (size_t)PS_NOALLOC_MAX_ELEMENTS / 4096;
-constexpr size_t kNoallocScratchBytes = ps::kHeaderBytes + 8 * kNoallocMaxTiles;
-static_assert(ps::kThreads * ps::kItems32 == 4096, "int32 tile size changed: resize the scratch");
+// The regular workspace size for the largest accepted n, so that the two
+// can never drift apart; the header states the same number.
+constexpr size_t kNoallocScratchBytes = ps::workspace_bytes(PS_INT32, (size_t)PS_NOALLOC_MAX_ELEMENTS);
+static_assert(kNoallocScratchBytes <= (size_t)PS_NOALLOC_SCRATCH_BYTES,
+              "the tile geometry changed: update PS_NOALLOC_SCRATCH_BYTES");
 
 // The scratch itself.  Host code must not pass this name to a kernel: on
 // the host it is only a stand-in symbol, not a device address.  The device
 // address comes from cudaGetSymbolAddress below.
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PS_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
@@ -74,5 +76,5 @@ extern "C" ps_status ps_scan_inclusive_i32_noalloc(const int32_t *in, int32_t *o
         ps::note_cuda_error(e);  // readable with ps_last_cuda_error()
         return PS_ERR_CUDA;
     }
-    return ps_scan_inclusive_i32(in, out, n, scratch, kNoallocScratchBytes, stream);
+    return ps_scan_inclusive_i32(in, out, n, scratch, PS_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -1,0 +1,359 @@
+// scan_persistent.cu -- the single-pass decoupled look-back scan as a
+// persistent, TMA-fed kernel for sm_103a.
+//
+// One CTA per SM slot runs until the tiles run out.  Its warps split into
+//   - CW compute warps, which scan tiles and store the results;
+//   - one producer warp, whose elected lane takes the next tile id from the
+//     global counter (dynamic tile ids: "virtual processors", section 4.4 of
+//     the decoupled look-back paper summary; "Dynamic Block Index
+//     Assignment" on the PMPP single-pass page) and copies the tile into a
+//     ring of STAGES shared-memory buffers with one bulk asynchronous copy
+//     (cp.async.bulk, completion counted in bytes on an mbarrier);
+//   - one aggregator warp, which reduces each tile as soon as its copy has
+//     landed and publishes the aggregate (A; P for tile 0) at once (step 3
+//     of section 4.1).
+// The producer runs up to STAGES-1 tiles ahead, so the HBM reads of later
+// tiles stay in flight while the compute warps wait on the look-back of the
+// current one, and the tile-id atomic leaves the critical path.  Because a
+// tile id is taken before its CTA is ready to scan it, publishing A only
+// when the compute warps reach the tile would make every successor wait for
+// the slowest CTA; the aggregator publishes it when the data arrives.
+//
+// Per tile the compute warps do steps a2-a9 exactly as the one-tile-per-CTA
+// kernel (scan_single_pass.cu): read the tile from shared memory in rows of
+// 16-byte vectors (conflict-free), release the buffer, scan in registers,
+// combine warp totals, let compute warp 0 publish A (P for tile 0), run the
+// look-back and publish P, then add the prefix and store with 16-byte
+// streaming stores.
+//
+// A tile that is cut by the end of the array is not copied; the compute
+// warps read it from global memory with bounds checks.  Every wait on an
+// mbarrier is bounded; a wait that runs out records PS_ERR_LOOKBACK_TIMEOUT
+// and the loop moves on (results are then unspecified, but the kernel ends).
+#include "scan_device.cuh"
+
+namespace ps {
+
+constexpr int kPCW = kThreads / 32;   // compute warps per CTA
+constexpr uint32_t kMbarSpinCap = 1u << 24;
+
+// ---- mbarrier and bulk-copy helpers (inline PTX) ----------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false if it ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kMbarSpinCap; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_u32(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
+template <typename T> struct PItems { static constexpr int value = kItems32; };
+template <> struct PItems<int64_t> { static constexpr int value = kItems64; };
+
+template <typename T>
+constexpr long long persistent_tile_elems() {
+    return (long long)kPCW * 32 * PItems<T>::value;
+}
+
+template <typename T>
+constexpr size_t persistent_smem_bytes() {
+    return (size_t)kPStages * persistent_tile_elems<T>() * sizeof(T) + 256;
+}
+
+static_assert(kThreads % 32 == 0 && kThreads <= 960, "compute threads per CTA");
+
+template <typename T, bool EXCL>
+__global__ void __launch_bounds__((kPCW + 2) * 32, kPCtasPerSm)
+persistent_kernel(PassArgs a, long long num_tiles) {
+    using Tr = Traits<T>;
+    using U = typename Tr::U;
+    using V = typename Tr::V;
+    constexpr int VEC = Tr::VEC;
+    constexpr int ITEMS = PItems<T>::value;
+    constexpr int ROWS = ITEMS / VEC;
+    constexpr long long TILE = persistent_tile_elems<T>();
+    constexpr uint32_t TILE_BYTES = (uint32_t)(TILE * sizeof(T));
+    constexpr int CT = kPCW * 32;   // compute threads
+    static_assert(ITEMS % VEC == 0, "ITEMS must be a multiple of the vector width");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    T *stage_data = reinterpret_cast<T *>(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kPStages * TILE_BYTES);
+    uint64_t *empty = full + kPStages;
+    uint64_t *agg_done = empty + kPStages;
+    long long *tile_of = reinterpret_cast<long long *>(agg_done + kPStages);
+    __shared__ U s_warp[kPCW];
+    __shared__ U s_excl;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    Header *hdr = reinterpret_cast<Header *>(a.ws);
+    void *desc = a.ws + kHeaderBytes;
+    const unsigned long long n = a.n;
+    const T *in = reinterpret_cast<const T *>(a.in);
+    T *out = reinterpret_cast<T *>(a.out);
+
+    if (tid == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kPCW + 1);     // compute warps + aggregator
+            mbar_init(&agg_done[s], 1);
+            tile_of[s] = num_tiles;   // end marker until the producer fills the stage
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kPCW) {
+        // ---------------- producer warp ----------------
+        if (lane == 0) {
+            for (long long k = 0;; ++k) {
+                const int s = (int)(k % kPStages);
+                if (k >= kPStages) {
+                    const uint32_t parity = (uint32_t)((k / kPStages - 1) & 1);
+                    if (!mbar_wait(&empty[s], parity)) {   // never in a correct run
+                        atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+                        break;
+                    }
+                }
+                const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
+                tile_of[s] = t;
+                if (t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
+                    mbar_arrive_expect_tx(&full[s], TILE_BYTES);
+                    bulk_load(stage_data + (size_t)s * TILE, in + t * TILE, TILE_BYTES, &full[s]);
+                } else {
+                    mbar_arrive(&full[s]);   // end marker, or a cut tile read from global
+                }
+                if (t >= num_tiles) break;
+            }
+        }
+        return;
+    }
+
+    if (warp == kPCW + 1) {
+        // ---------------- aggregator warp ----------------
+        for (long long k = 0;; ++k) {
+            const int s = (int)(k % kPStages);
+            if (!mbar_wait(&full[s], (uint32_t)((k / kPStages) & 1))) {   // never in a correct run
+                atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+                break;
+            }
+            const long long tile = tile_of[s];
+            if (tile < 0 || tile >= num_tiles) break;
+            const unsigned long long tile_base = (unsigned long long)tile * TILE;
+            U acc = U(0);
+            if (tile_base + TILE <= n) {
+                const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE);
+#pragma unroll 8
+                for (int i = lane; i < (int)(TILE / VEC); i += 32) {
+                    const V x = src[i];
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) acc = acc + (U)vget(x, j);
+                }
+            } else {
+                for (unsigned long long i = tile_base + lane; i < n; i += 32) acc = acc + (U)in[i];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            const U agg = warp_sum<U>(acc);
+            if (lane == 0) {
+                if (tile == 0) {
+                    const U c = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
+                    Desc<U, Tr::DW>::store(desc, 0, kFlagP, c + agg);
+                } else {
+                    Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg);
+                }
+                mbar_arrive(&agg_done[s]);
+            }
+        }
+        return;
+    }
+
+    // ---------------- compute warps ----------------
+    for (long long k = 0;; ++k) {
+        const int s = (int)(k % kPStages);
+        if (!mbar_wait(&full[s], (uint32_t)((k / kPStages) & 1))) {   // never in a correct run
+            atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+            break;
+        }
+        const long long tile = tile_of[s];
+        if (tile < 0 || tile >= num_tiles) break;
+        const unsigned long long tile_base = (unsigned long long)tile * TILE;
+        const bool cut = tile_base + TILE > n;
+        const int seg = warp * 32 * ITEMS;   // element offset of this warp in the tile
+
+        // a2: rows of 16-byte vectors from the stage (or bounded global loads)
+        U v[ROWS][VEC];
+        if (!cut) {
+            const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE + seg) + lane;
+            V buf[ROWS];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) buf[r] = src[r * 32];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) v[r][j] = (U)vget(buf[r], j);
+        } else {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const unsigned long long i = tile_base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
+                    v[r][j] = i < n ? (U)in[i] : U(0);
+                }
+        }
+        // a3 + a4
+        U off[ROWS];
+        U running = U(0);
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            U t;
+            if (EXCL) {
+                U acc = U(0);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const U x = v[r][j];
+                    v[r][j] = acc;
+                    acc = acc + x;
+                }
+                t = acc;
+            } else {
+#pragma unroll
+                for (int j = 1; j < VEC; ++j) v[r][j] = v[r][j - 1] + v[r][j];
+                t = v[r][VEC - 1];
+            }
+            const U sc = warp_inclusive<U>(t, lane);
+            U le = __shfl_up_sync(kFull, sc, 1);
+            if (lane == 0) le = U(0);
+            const U row_total = __shfl_sync(kFull, sc, 31);
+            off[r] = running + le;
+            running = running + row_total;
+        }
+
+        // a5
+        if (lane == 0) s_warp[warp] = running;
+        named_barrier(1, CT);
+        U warp_excl = U(0), agg = U(0);
+#pragma unroll
+        for (int w = 0; w < kPCW; ++w) {
+            const U t = s_warp[w];
+            if (w < warp) warp_excl = warp_excl + t;
+            agg = agg + t;
+        }
+
+        // a6..a8 (A, and P of tile 0, come from the aggregator warp)
+        if (warp == 0) {
+            U excl;
+            if (tile == 0) {
+                excl = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
+            } else {
+                excl = look_back<U, Tr::DW, kLookbackK>(desc, tile, a.max_polls, &hdr->status);
+                // P must land after the aggregator's A, never before it
+                if (!mbar_wait(&agg_done[s], (uint32_t)((k / kPStages) & 1)))
+                    atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+                if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg);
+            }
+            if (lane == 0) {
+                s_excl = excl;
+                if (a.carry_out && tile == num_tiles - 1) *reinterpret_cast<U *>(a.carry_out) = excl + agg;
+            }
+        }
+        named_barrier(1, CT);
+
+        // a9
+        const U base = s_excl + warp_excl;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const U o = base + off[r];
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) v[r][j] = o + v[r][j];
+        }
+        if (!cut) {
+            V *dst = reinterpret_cast<V *>(out + tile_base + seg) + lane;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                V w;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) vset(w, j, v[r][j]);
+                st_stream(dst + r * 32, w);
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const unsigned long long i = tile_base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
+                    if (i < n) out[i] = (T)v[r][j];
+                }
+        }
+        // Release the stage only now: the aggregator cannot then run a whole
+        // ring ahead on it, so agg_done[s] completes exactly one phase per
+        // use and the parity wait above cannot alias.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+template <typename T, bool EXCL>
+cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
+    constexpr size_t smem = persistent_smem_bytes<T>();
+    const long long tiles = (long long)((a.n + persistent_tile_elems<T>() - 1) / persistent_tile_elems<T>());
+    // the dynamic shared-memory opt-in, once per device and template instance
+    // (a repeated call from a racing thread is harmless)
+    static volatile int configured[64] = {};
+    cudaError_t e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(persistent_kernel<T, EXCL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = 1;
+    }
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    long long grid = (long long)sms * kPCtasPerSm;
+    if (grid > tiles) grid = tiles;
+    persistent_kernel<T, EXCL><<<(unsigned int)grid, (kPCW + 2) * 32, smem, s>>>(a, tiles);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_persistent(const PassArgs &a, bool exclusive, cudaStream_t s) {
+    return exclusive ? launch_persistent_kind<T, true>(a, s) : launch_persistent_kind<T, false>(a, s);
+}
+
+template cudaError_t launch_persistent<int32_t>(const PassArgs &, bool, cudaStream_t);
+template cudaError_t launch_persistent<int64_t>(const PassArgs &, bool, cudaStream_t);
+template cudaError_t launch_persistent<float>(const PassArgs &, bool, cudaStream_t);
+
+}  // namespace ps

@@ -30,8 +30,12 @@
 
 namespace ps {
 
+#ifndef PS_MIN_BLOCKS
+#define PS_MIN_BLOCKS 1
+#endif
+
 template <typename T, int THREADS, int ITEMS, bool EXCL, bool VEC_IO, Lookback LB>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, PS_MIN_BLOCKS)
 single_pass_kernel(PassArgs a) {
     using Tr = Traits<T>;
     using U = typename Tr::U;
@@ -138,7 +142,9 @@ single_pass_kernel(PassArgs a) {
             if (lane == 0) Desc<U, Tr::DW>::store(desc, 0, kFlagP, excl + agg);
         } else {
             if (LB == Lookback::Decoupled && lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg);
-            excl = look_back<U, Tr::DW, LB == Lookback::Chained>(desc, tile, a.max_polls, &hdr->status);
+            excl = (LB == Lookback::Chained)
+                       ? chained_wait<U, Tr::DW>(desc, tile, a.max_polls, &hdr->status)
+                       : look_back<U, Tr::DW, kLookbackK>(desc, tile, a.max_polls, &hdr->status);
             if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg);
         }
         if (lane == 0) {
@@ -207,9 +213,11 @@ cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, c
     cudaError_t e = cudaMemsetAsync(a.ws, 0, kHeaderBytes + tiles * desc_bytes(dt), s);
     if (e != cudaSuccess) return e;
     const bool vec_io = ((reinterpret_cast<uintptr_t>(a.in) | reinterpret_cast<uintptr_t>(a.out)) & 15u) == 0;
-    if (lb == Lookback::Decoupled)
+    if (lb == Lookback::Decoupled) {
+        if (vec_io) return launch_persistent<T>(a, exclusive, s);
         return exclusive ? launch_kind<T, true, Lookback::Decoupled>(a, vec_io, tiles, s)
                          : launch_kind<T, false, Lookback::Decoupled>(a, vec_io, tiles, s);
+    }
     return exclusive ? launch_kind<T, true, Lookback::Chained>(a, vec_io, tiles, s)
                      : launch_kind<T, false, Lookback::Chained>(a, vec_io, tiles, s);
 }
@@ -236,7 +244,7 @@ template <typename T>
 __global__ void lookback_probe_kernel(const void *desc, long long tile, uint32_t max_polls,
                                       void *result, unsigned int *status) {
     using U = typename Traits<T>::U;
-    const U excl = look_back<U, Traits<T>::DW, false>(desc, tile, max_polls, status);
+    const U excl = look_back<U, Traits<T>::DW, kLookbackK>(desc, tile, max_polls, status);
     if (threadIdx.x == 0) *reinterpret_cast<U *>(result) = excl;
 }
 

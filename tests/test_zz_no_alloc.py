@@ -61,6 +61,18 @@ def test_noalloc_in_place_and_empty():
     assert _noalloc(e, e) == _lib.PS_OK
 
 
+def test_noalloc_largest_accepted_size():
+    # n exactly at the limit must fit the fixed scratch
+    n = _lib.PS_NOALLOC_MAX_ELEMENTS
+    x = torch.from_numpy(inputs.uniform_int(n, -3, 3, 99)).to(DEV)
+    want = api.scan_inclusive(x)
+    assert _noalloc(x, x) == _lib.PS_OK
+    torch.cuda.synchronize()
+    assert torch.equal(x, want)
+    del x, want
+    torch.cuda.empty_cache()
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     n = _lib.PS_NOALLOC_MAX_ELEMENTS + 1
     # a real buffer of that length, so nothing could go out of bounds even if
