@@ -75,10 +75,10 @@ typedef enum ps_dtype { PS_INT32 = 0, PS_INT64 = 1, PS_FLOAT32 = 2 } ps_dtype;
 
 /*
  * Bytes of workspace a scan of n elements of `dtype` needs (0 for n == 0):
- * a 256-byte header (tile counter, status word) plus one 32-byte slot per
+ * a 256-byte header (tile counter, status word) plus one 64-byte slot per
  * tile holding its status descriptor (section 4.1, "partition descriptor":
  * status flag X/A/P plus a value).  Tiles are 8192 elements (32-bit types)
- * or 4096 (int64), so about n/256 bytes (n/128 for int64).  The same size
+ * or 4096 (int64), so about n/128 bytes (n/64 for int64).  The same size
  * serves every algorithm below.
  */
 size_t ps_scan_workspace_size(ps_dtype dtype, size_t n);
@@ -174,7 +174,7 @@ size_t ps_tile_elements(ps_dtype dtype);
  *     through the regular entry points (there is no caller workspace here).
  */
 #define PS_NOALLOC_MAX_ELEMENTS 536870912u /* 2^29 elements */
-#define PS_NOALLOC_SCRATCH_BYTES (256u + 32u * (PS_NOALLOC_MAX_ELEMENTS / 8192u)) /* 2 MiB + 256 */
+#define PS_NOALLOC_SCRATCH_BYTES (256u + 64u * (PS_NOALLOC_MAX_ELEMENTS / 8192u)) /* 4 MiB + 256 */
 ps_status ps_scan_inclusive_i32_noalloc(const int32_t *in, int32_t *out, size_t n,
                                         ps_stream_t stream);
 

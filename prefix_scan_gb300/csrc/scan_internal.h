@@ -67,10 +67,11 @@ static_assert(sizeof(Header) <= kHeaderBytes, "header too large");
 #endif
 // Bytes between consecutive tile descriptors.  Packed 8-byte descriptors
 // put 16 neighbouring tiles on one 128-byte L2 line, which every publish
-// and every look-back of those tiles then contends for; one descriptor per
-// 32-byte sector measured fastest on GB300.  64-bit types use at least 16.
+// and every look-back of those tiles then contends for; spreading them to
+// one per 64 bytes measured fastest over int32 and int64 on GB300.  64-bit
+// types use at least 16.
 #ifndef PS_DESC_STRIDE
-#define PS_DESC_STRIDE 32
+#define PS_DESC_STRIDE 64
 #endif
 constexpr int kDescStride32 = PS_DESC_STRIDE;
 constexpr int kDescStride64 = PS_DESC_STRIDE < 16 ? 16 : PS_DESC_STRIDE;

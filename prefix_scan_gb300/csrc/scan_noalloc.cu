@@ -12,7 +12,7 @@
 //
 // Consequences of a file-scope device array:
 //   - every GPU that loads this library holds the array
-//     (PS_NOALLOC_SCRATCH_BYTES, 2 MiB + 256 bytes) until the process exits;
+//     (PS_NOALLOC_SCRATCH_BYTES, 4 MiB + 256 bytes) until the process exits;
 //   - all calls on a device share it: two calls whose work overlaps on the
 //     GPU (different streams, or different host threads without ordering)
 //     race on it and give wrong results; calls on one stream are ordered and

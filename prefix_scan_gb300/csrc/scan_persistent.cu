@@ -11,20 +11,24 @@
 //     (cp.async.bulk, completion counted in bytes on an mbarrier);
 //   - one aggregator warp, which reduces each tile as soon as its copy has
 //     landed and publishes the aggregate (A; P for tile 0) at once (step 3
-//     of section 4.1).
+//     of section 4.1), whatever the rest of the CTA is doing;
+//   - one look-back warp, which then runs the warp-parallel look-back,
+//     publishes P and hands the tile's exclusive prefix to the compute
+//     warps (steps 4-5).
 // The producer runs up to STAGES-1 tiles ahead, so the HBM reads of later
-// tiles stay in flight while the compute warps wait on the look-back of the
-// current one, and the tile-id atomic leaves the critical path.  Because a
-// tile id is taken before its CTA is ready to scan it, publishing A only
-// when the compute warps reach the tile would make every successor wait for
-// the slowest CTA; the aggregator publishes it when the data arrives.
+// tiles stay in flight, and the tile-id atomic leaves the critical path.
+// Because a tile id is taken before its CTA is ready to scan it, publishing
+// A only when some warp of the CTA gets round to it (after the scan, or
+// after the previous tile's look-back) would make every successor wait for
+// the slowest CTA; the aggregator publishes it when the data arrives.  The
+// look-back usually finishes before the compute warps need the prefix, so
+// its latency hides behind the scans of earlier tiles.
 //
-// Per tile the compute warps do steps a2-a9 exactly as the one-tile-per-CTA
-// kernel (scan_single_pass.cu): read the tile from shared memory in rows of
-// 16-byte vectors (conflict-free), release the buffer, scan in registers,
-// combine warp totals, let compute warp 0 publish A (P for tile 0), run the
-// look-back and publish P, then add the prefix and store with 16-byte
-// streaming stores.
+// Per tile the compute warps do steps a2-a5 and a9 as the one-tile-per-CTA
+// kernel (scan_single_pass.cu) does: read the tile from shared memory in
+// rows of 16-byte vectors (conflict-free), scan in registers, combine warp
+// totals, wait for the prefix, add it and store with 16-byte streaming
+// stores, then release the buffer.
 //
 // A tile that is cut by the end of the array is not copied; the compute
 // warps read it from global memory with bounds checks.  Every wait on an
@@ -35,7 +39,8 @@
 namespace ps {
 
 constexpr int kPCW = kThreads / 32;   // compute warps per CTA
-constexpr uint32_t kMbarSpinCap = 1u << 24;
+constexpr uint32_t kMbarSpinCap = 1u << 22;   // try_wait rounds before giving up
+constexpr size_t kStageTailBytes = ((size_t)kPStages * (4 * 8 + 8 + 8 + 8) + 127) / 128 * 128;
 
 // ---- mbarrier and bulk-copy helpers (inline PTX) ----------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -86,13 +91,15 @@ constexpr long long persistent_tile_elems() {
 
 template <typename T>
 constexpr size_t persistent_smem_bytes() {
-    return (size_t)kPStages * persistent_tile_elems<T>() * sizeof(T) + 256;
+    // + per stage: 4 mbarriers, a tile id, an aggregate and a prefix
+    return (size_t)kPStages * persistent_tile_elems<T>() * sizeof(T) + kStageTailBytes;
 }
 
 static_assert(kThreads % 32 == 0 && kThreads <= 960, "compute threads per CTA");
 
+
 template <typename T, bool EXCL>
-__global__ void __launch_bounds__((kPCW + 2) * 32, kPCtasPerSm)
+__global__ void __launch_bounds__((kPCW + 3) * 32, kPCtasPerSm)
 persistent_kernel(PassArgs a, long long num_tiles) {
     using Tr = Traits<T>;
     using U = typename Tr::U;
@@ -110,9 +117,11 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kPStages * TILE_BYTES);
     uint64_t *empty = full + kPStages;
     uint64_t *agg_done = empty + kPStages;
-    long long *tile_of = reinterpret_cast<long long *>(agg_done + kPStages);
-    __shared__ U s_warp[kPCW];
-    __shared__ U s_excl;
+    uint64_t *prefix_ready = agg_done + kPStages;
+    long long *tile_of = reinterpret_cast<long long *>(prefix_ready + kPStages);
+    U *agg_of = reinterpret_cast<U *>(tile_of + kPStages);
+    U *excl_of = agg_of + kPStages;
+    __shared__ U s_warp[2][kPCW];
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -128,6 +137,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kPCW + 1);     // compute warps + aggregator
             mbar_init(&agg_done[s], 1);
+            mbar_init(&prefix_ready[s], 1);
             tile_of[s] = num_tiles;   // end marker until the producer fills the stage
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -162,6 +172,9 @@ persistent_kernel(PassArgs a, long long num_tiles) {
 
     if (warp == kPCW + 1) {
         // ---------------- aggregator warp ----------------
+        // Reduces each tile as soon as its copy lands and publishes A (P for
+        // tile 0) at once, independently of any look-back (step 3 of
+        // section 4.1).
         for (long long k = 0;; ++k) {
             const int s = (int)(k % kPStages);
             if (!mbar_wait(&full[s], (uint32_t)((k / kPStages) & 1))) {   // never in a correct run
@@ -169,7 +182,10 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 break;
             }
             const long long tile = tile_of[s];
-            if (tile < 0 || tile >= num_tiles) break;
+            if (tile < 0 || tile >= num_tiles) {   // end marker: pass it on to the look-back warp
+                if (lane == 0) mbar_arrive(&agg_done[s]);
+                break;
+            }
             const unsigned long long tile_base = (unsigned long long)tile * TILE;
             U acc = U(0);
             if (tile_base + TILE <= n) {
@@ -193,7 +209,38 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 } else {
                     Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg);
                 }
+                agg_of[s] = agg;
                 mbar_arrive(&agg_done[s]);
+            }
+        }
+        return;
+    }
+
+    if (warp == kPCW + 2) {
+        // ---------------- look-back warp ----------------
+        // Runs ahead of the compute warps: once a tile's A is out it looks
+        // back, publishes P and leaves the exclusive prefix in excl_of[s]
+        // (steps 4-5 of section 4.1), so the compute warps rarely wait.
+        for (long long k = 0;; ++k) {
+            const int s = (int)(k % kPStages);
+            if (!mbar_wait(&agg_done[s], (uint32_t)((k / kPStages) & 1))) {   // never in a correct run
+                atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+                break;
+            }
+            const long long tile = tile_of[s];
+            if (tile < 0 || tile >= num_tiles) break;
+            const U agg = agg_of[s];
+            U excl;
+            if (tile == 0) {
+                excl = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
+            } else {
+                excl = look_back<U, Tr::DW, kLookbackK>(desc, tile, a.max_polls, &hdr->status);
+                if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg);
+            }
+            if (lane == 0) {
+                if (a.carry_out && tile == num_tiles - 1) *reinterpret_cast<U *>(a.carry_out) = excl + agg;
+                excl_of[s] = excl;
+                mbar_arrive(&prefix_ready[s]);
             }
         }
         return;
@@ -260,38 +307,22 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             running = running + row_total;
         }
 
-        // a5
-        if (lane == 0) s_warp[warp] = running;
+        // a5 (double-buffered by iteration, so that no second barrier is needed)
+        U *sw = s_warp[k & 1];
+        if (lane == 0) sw[warp] = running;
         named_barrier(1, CT);
-        U warp_excl = U(0), agg = U(0);
+        U warp_excl = U(0);
 #pragma unroll
-        for (int w = 0; w < kPCW; ++w) {
-            const U t = s_warp[w];
-            if (w < warp) warp_excl = warp_excl + t;
-            agg = agg + t;
-        }
+        for (int w = 0; w < kPCW; ++w)
+            if (w < warp) warp_excl = warp_excl + sw[w];
 
-        // a6..a8 (A, and P of tile 0, come from the aggregator warp)
-        if (warp == 0) {
-            U excl;
-            if (tile == 0) {
-                excl = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
-            } else {
-                excl = look_back<U, Tr::DW, kLookbackK>(desc, tile, a.max_polls, &hdr->status);
-                // P must land after the aggregator's A, never before it
-                if (!mbar_wait(&agg_done[s], (uint32_t)((k / kPStages) & 1)))
-                    atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
-                if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg);
-            }
-            if (lane == 0) {
-                s_excl = excl;
-                if (a.carry_out && tile == num_tiles - 1) *reinterpret_cast<U *>(a.carry_out) = excl + agg;
-            }
-        }
-        named_barrier(1, CT);
+        // the look-back warp provides the tile's exclusive prefix
+        if (!mbar_wait(&prefix_ready[s], (uint32_t)((k / kPStages) & 1)))   // never in a correct run
+            atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+        const U tile_excl = excl_of[s];
 
         // a9
-        const U base = s_excl + warp_excl;
+        const U base = tile_excl + warp_excl;
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
             const U o = base + off[r];
@@ -316,9 +347,9 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                     if (i < n) out[i] = (T)v[r][j];
                 }
         }
-        // Release the stage only now: the aggregator cannot then run a whole
-        // ring ahead on it, so agg_done[s] completes exactly one phase per
-        // use and the parity wait above cannot alias.
+        // Release the stage only now: the look-back warp cannot then run a
+        // whole ring ahead on it, so prefix_ready[s] completes exactly one
+        // phase per use and the parity wait above cannot alias.
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -343,7 +374,7 @@ cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     long long grid = (long long)sms * kPCtasPerSm;
     if (grid > tiles) grid = tiles;
-    persistent_kernel<T, EXCL><<<(unsigned int)grid, (kPCW + 2) * 32, smem, s>>>(a, tiles);
+    persistent_kernel<T, EXCL><<<(unsigned int)grid, (kPCW + 3) * 32, smem, s>>>(a, tiles);
     return cudaGetLastError();
 }
 
