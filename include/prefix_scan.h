@@ -131,6 +131,46 @@ ps_status ps_scan(ps_algo algo, ps_dtype dtype, int exclusive, const void *in, v
                   size_t n, void *ws, size_t ws_bytes, ps_stream_t stream);
 
 /*
+ * Seeded scan: the decoupled look-back scan of `in` with a carry added to
+ * every output, and the running total written back.  It is what a scan of
+ * an array cut into pieces needs (a stream of chunks, shards on several
+ * GPUs): piece i is scanned with the total of pieces 0..i-1 as its carry.
+ *   carry_in  : device pointer to one element of `dtype` added to every
+ *               output (exclusive: y[0] = *carry_in); NULL means 0.
+ *   carry_out : device pointer receiving *carry_in + x[0] + ... + x[n-1];
+ *               NULL means not written.  May equal carry_in.
+ * Same conventions and errors as ps_scan; PS_ERR_OVERLAP if a carry lies
+ * inside in, out or ws.  n == 0 copies *carry_in (or 0) to *carry_out.
+ */
+ps_status ps_scan_seeded(ps_dtype dtype, int exclusive, const void *in, void *out, size_t n,
+                         const void *carry_in, void *carry_out, void *ws, size_t ws_bytes,
+                         ps_stream_t stream);
+
+/*
+ * Scan of arrays in HOST memory (the end-to-end path).  The array is
+ * streamed through the GPU in 64 MiB chunks: the host-to-device copy of
+ * chunk i+1, the seeded scan of chunk i and the device-to-host copy of
+ * chunk i-1 run at the same time on three streams, and the running total
+ * is carried on the device from chunk to chunk.
+ *   h_in, h_out : host arrays of n elements (h_out == h_in scans in place);
+ *                 page-locked memory lets the copies overlap, pageable
+ *                 memory works but the copies then serialise.
+ *   d_staging   : device buffer of at least ps_scan_host_staging_size(dtype,
+ *                 n) bytes, 256-byte aligned (two chunk buffers + a carry).
+ *   ws          : device workspace of at least ps_scan_workspace_size(dtype,
+ *                 min(n, chunk)) bytes; ps_scan_workspace_size(dtype, n)
+ *                 always suffices.
+ * Work is enqueued on `stream`; the call returns before it completes and
+ * h_out is complete once `stream` has reached this point (e.g. after
+ * cudaStreamSynchronize).  Internal streams and events are created and
+ * released by the call.  h_in and h_out must not change until then.
+ */
+size_t ps_scan_host_staging_size(ps_dtype dtype, size_t n);
+ps_status ps_scan_host(ps_dtype dtype, int exclusive, const void *h_in, void *h_out, size_t n,
+                       void *d_staging, size_t staging_bytes, void *ws, size_t ws_bytes,
+                       ps_stream_t stream);
+
+/*
  * Waits for `stream`, then reads the device-side status the last scan
  * that used `ws` left there (PS_OK or PS_ERR_LOOKBACK_TIMEOUT) into *out.
  * Returns PS_ERR_CUDA if the wait or the copy fails.

@@ -38,6 +38,9 @@ SIGNATURES = {
     "ps_testing_lookback": (_int, [_int, _vp, _i64, _u32, _vp, _vp, _vp]),
 }
 SIGNATURES["ps_scan_inclusive_i32_noalloc"] = (_int, [_vp, _vp, _sz, _vp])
+SIGNATURES["ps_scan_seeded"] = (_int, [_int, _int, _vp, _vp, _sz, _vp, _vp, _vp, _sz, _vp])
+SIGNATURES["ps_scan_host_staging_size"] = (_sz, [_int, _sz])
+SIGNATURES["ps_scan_host"] = (_int, [_int, _int, _vp, _vp, _sz, _vp, _sz, _vp, _sz, _vp])
 PS_NOALLOC_MAX_ELEMENTS = 1 << 29
 
 for _kind in ("inclusive", "exclusive"):

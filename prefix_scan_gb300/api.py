@@ -102,6 +102,82 @@ def scan_exclusive(x: torch.Tensor, out: torch.Tensor | None = None, **kw) -> to
     return scan(x, exclusive=True, out=out, **kw)
 
 
+def scan_seeded(x: torch.Tensor, carry_in: torch.Tensor | None = None,
+                carry_out: torch.Tensor | None = None, *, exclusive: bool = False,
+                out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """Scan with a device carry: y = carry_in + scan(x); carry_out = carry_in + sum(x).
+
+    ``carry_in``/``carry_out`` are one-element CUDA tensors of x's dtype (or
+    None); they may be the same tensor.
+    """
+    if not x.is_cuda or x.dim() != 1 or not x.is_contiguous():
+        raise ValueError("prefix scan: input must be a contiguous 1-D CUDA tensor")
+    code = dtype_code(x.dtype)
+    n = x.numel()
+    out = torch.empty_like(x) if out is None else out
+    for c in (carry_in, carry_out):
+        if c is not None and (c.dtype != x.dtype or c.numel() != 1 or c.device != x.device):
+            raise ValueError("prefix scan: carries are one-element tensors of the input's dtype")
+    lib = _lib.load()
+    need = int(lib.ps_scan_workspace_size(code, n))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    st = lib.ps_scan_seeded(code, int(exclusive), x.data_ptr() if n else None,
+                            out.data_ptr() if n else None, n,
+                            carry_in.data_ptr() if carry_in is not None else None,
+                            carry_out.data_ptr() if carry_out is not None else None,
+                            workspace.data_ptr(), workspace.numel(), _stream_handle(stream, x.device))
+    _lib.check("ps_scan_seeded", st)
+    return out
+
+
+def host_staging_size(dtype: torch.dtype, n: int) -> int:
+    return int(_lib.load().ps_scan_host_staging_size(dtype_code(dtype), n))
+
+
+class HostScanBuffers:
+    """Device staging buffer + workspace for :func:`scan_host`, reusable across calls."""
+
+    def __init__(self, dtype: torch.dtype, n: int, device=None):
+        dev = torch.device(device or "cuda")
+        self.dtype, self.n = dtype, n
+        self.staging = torch.empty(max(host_staging_size(dtype, n), 256), dtype=torch.uint8, device=dev)
+        self.workspace = torch.empty(max(workspace_size(dtype, n), 1), dtype=torch.uint8, device=dev)
+
+
+def scan_host(x: torch.Tensor, *, exclusive: bool = False, out: torch.Tensor | None = None,
+              buffers: HostScanBuffers | None = None, stream=None, synchronize: bool = True,
+              device=None) -> torch.Tensor:
+    """Scan of a contiguous 1-D HOST tensor, streamed through the GPU.
+
+    ``out`` (host) may be ``x`` for an in-place scan.  Pinned (page-locked)
+    tensors let the two copy directions overlap.  With ``synchronize`` the
+    call waits for the stream, so ``out`` is ready on return.
+    """
+    if x.is_cuda or x.dim() != 1 or not x.is_contiguous():
+        raise ValueError("scan_host: input must be a contiguous 1-D host tensor")
+    code = dtype_code(x.dtype)
+    n = x.numel()
+    out = torch.empty_like(x) if out is None else out
+    if out.is_cuda or out.dtype != x.dtype or out.numel() != n or not out.is_contiguous():
+        raise ValueError("scan_host: `out` must be a host tensor matching the input")
+    if n == 0:
+        return out
+    dev = torch.device(device or "cuda")
+    if buffers is None or buffers.n < n or buffers.dtype != x.dtype:
+        buffers = HostScanBuffers(x.dtype, n, dev)
+    s = stream if stream is not None else torch.cuda.current_stream(buffers.staging.device)
+    st = _lib.load().ps_scan_host(code, int(exclusive), x.data_ptr(), out.data_ptr(), n,
+                                  buffers.staging.data_ptr(), buffers.staging.numel(),
+                                  buffers.workspace.data_ptr(), buffers.workspace.numel(),
+                                  ctypes.c_void_p(s.cuda_stream))
+    _lib.check("ps_scan_host", st)
+    if synchronize:
+        s.synchronize()
+    return out
+
+
 def device_status(workspace: torch.Tensor, stream=None) -> int:
     """Waits for the stream, returns the status the last scan left in ``workspace``."""
     lib = _lib.load()

@@ -47,13 +47,13 @@ ps_status check_args(ps_dtype dt, const void *in, const void *out, size_t n, con
 
 template <typename T>
 ps_status run(ps_algo algo, bool exclusive, const void *in, void *out, size_t n, void *ws,
-              cudaStream_t s) {
+              cudaStream_t s, const void *carry_in = nullptr, void *carry_out = nullptr) {
     cudaError_t e;
     unsigned char *w = static_cast<unsigned char *>(ws);
     switch (algo) {
     case PS_ALGO_DECOUPLED_LOOKBACK:
     case PS_ALGO_CHAINED: {
-        ps::PassArgs a{in, out, (unsigned long long)n, w, nullptr, nullptr, ps::kDefaultMaxPolls};
+        ps::PassArgs a{in, out, (unsigned long long)n, w, carry_in, carry_out, ps::kDefaultMaxPolls};
         e = ps::launch_single_pass<T>(a, exclusive,
                                       algo == PS_ALGO_CHAINED ? ps::Lookback::Chained
                                                               : ps::Lookback::Decoupled, s);
@@ -88,6 +88,35 @@ ps_status dispatch(ps_algo algo, ps_dtype dt, int exclusive, const void *in, voi
 
 void ps::note_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
+ps_status ps::scan_seeded(ps_dtype dt, int exclusive, const void *in, void *out, size_t n,
+                          const void *carry_in, void *carry_out, void *ws, size_t ws_bytes,
+                          cudaStream_t s) {
+    if (!valid_dtype(dt)) return PS_ERR_INVALID_ARG;
+    const size_t es = ps::elem_bytes(dt);
+    if ((reinterpret_cast<uintptr_t>(carry_in) | reinterpret_cast<uintptr_t>(carry_out)) % es != 0)
+        return PS_ERR_INVALID_ARG;
+    if (n == 0) {
+        // the running total of nothing added to carry_in is carry_in
+        if (carry_out == nullptr || carry_out == carry_in) return PS_OK;
+        cudaError_t e = carry_in ? cudaMemcpyAsync(carry_out, carry_in, es, cudaMemcpyDeviceToDevice, s)
+                                 : cudaMemsetAsync(carry_out, 0, es, s);
+        return e == cudaSuccess ? PS_OK : cuda_fail(e);
+    }
+    const ps_status st = check_args(dt, in, out, n, ws, ws_bytes);
+    if (st != PS_OK) return st;
+    const size_t bytes = n * es, wsb = ps::workspace_bytes(dt, n);
+    for (const void *c : {static_cast<const void *>(carry_in), static_cast<const void *>(carry_out)})
+        if (c && (ranges_overlap(c, es, in, bytes) || ranges_overlap(c, es, out, bytes) ||
+                  ranges_overlap(c, es, ws, wsb)))
+            return PS_ERR_OVERLAP;
+    switch (dt) {
+    case PS_INT32: return run<int32_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, s, carry_in, carry_out);
+    case PS_INT64: return run<int64_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, s, carry_in, carry_out);
+    case PS_FLOAT32: return run<float>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, s, carry_in, carry_out);
+    }
+    return PS_ERR_INVALID_ARG;
+}
+
 extern "C" {
 
 size_t ps_scan_workspace_size(ps_dtype dtype, size_t n) {
@@ -118,6 +147,13 @@ PS_DEFINE_ENTRY(ps_scan_exclusive_i64, int64_t, PS_INT64, 1)
 PS_DEFINE_ENTRY(ps_scan_inclusive_f32, float, PS_FLOAT32, 0)
 PS_DEFINE_ENTRY(ps_scan_exclusive_f32, float, PS_FLOAT32, 1)
 #undef PS_DEFINE_ENTRY
+
+ps_status ps_scan_seeded(ps_dtype dtype, int exclusive, const void *in, void *out, size_t n,
+                         const void *carry_in, void *carry_out, void *ws, size_t ws_bytes,
+                         ps_stream_t stream) {
+    return ps::scan_seeded(dtype, exclusive, in, out, n, carry_in, carry_out, ws, ws_bytes,
+                           (cudaStream_t)stream);
+}
 
 ps_status ps_get_device_status(const void *ws, ps_stream_t stream, ps_status *out) {
     if (ws == nullptr || out == nullptr) return PS_ERR_INVALID_ARG;

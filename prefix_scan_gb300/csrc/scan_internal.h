@@ -145,4 +145,9 @@ cudaError_t launch_lookback_probe(const void *desc, long long tile, uint32_t max
 // Records `e` as the calling thread's last CUDA error (ps_last_cuda_error).
 void note_cuda_error(cudaError_t e);
 
+// The checked body of ps_scan_seeded (decoupled look-back with carries).
+ps_status scan_seeded(ps_dtype dt, int exclusive, const void *in, void *out, size_t n,
+                      const void *carry_in, void *carry_out, void *ws, size_t ws_bytes,
+                      cudaStream_t s);
+
 }  // namespace ps

@@ -204,8 +204,12 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             const U agg = warp_sum<U>(acc);
             if (lane == 0) {
                 if (tile == 0) {
+                    // the only read of carry_in: it precedes tile 0's P, hence
+                    // every other tile's P and the write of carry_out, so
+                    // carry_in may alias carry_out
                     const U c = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
                     Desc<U, Tr::DW>::store(desc, 0, kFlagP, c + agg);
+                    excl_of[s] = c;   // for the look-back warp
                 } else {
                     Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg);
                 }
@@ -230,9 +234,10 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             const long long tile = tile_of[s];
             if (tile < 0 || tile >= num_tiles) break;
             const U agg = agg_of[s];
+            __syncwarp();
             U excl;
             if (tile == 0) {
-                excl = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
+                excl = excl_of[s];   // the carry the aggregator read
             } else {
                 excl = look_back<U, Tr::DW, kLookbackK>(desc, tile, a.max_polls, &hdr->status);
                 if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg);

@@ -138,7 +138,12 @@ single_pass_kernel(PassArgs a) {
     } else if (warp == 0) {
         U excl;
         if (tile == 0) {
-            excl = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
+            // one read of carry_in, by the lane that then publishes tile 0's
+            // P: every other tile's P and the write of carry_out follow it,
+            // so carry_in may alias carry_out
+            U c = U(0);
+            if (lane == 0 && a.carry_in) c = *reinterpret_cast<const U *>(a.carry_in);
+            excl = __shfl_sync(kFull, c, 0);
             if (lane == 0) Desc<U, Tr::DW>::store(desc, 0, kFlagP, excl + agg);
         } else {
             if (LB == Lookback::Decoupled && lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg);

@@ -60,7 +60,15 @@ def test_workspace_size(lib):
 FAKE = 1 << 40  # never dereferenced: every call below fails validation first
 
 
-def test_argument_errors(lib):
+@pytest.fixture
+def no_device():
+    """The calls with made-up addresses run only where no GPU could receive them."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("made-up device addresses are only passed on hosts without a GPU")
+
+
+def test_argument_errors(lib, no_device):
     ws_need = lib.ps_scan_workspace_size(0, 1000)
     f = lib.ps_scan_inclusive_i32
     assert f(None, None, 0, None, 0, None) == _lib.PS_OK                       # n == 0: no-op
@@ -82,6 +90,34 @@ def test_argument_errors(lib):
     # int64 misalignment is checked against 8 bytes
     ws64 = lib.ps_scan_workspace_size(1, 1000)
     assert lib.ps_scan_inclusive_i64(FAKE + 4, FAKE + 16384, 1000, FAKE + (1 << 20), ws64, None) == \
+        _lib.PS_ERR_INVALID_ARG
+
+
+def test_host_scan_argument_errors(lib, no_device):
+    n = 1000
+    need = lib.ps_scan_host_staging_size(0, n)
+    ws = lib.ps_scan_workspace_size(0, n)
+    assert lib.ps_scan_host_staging_size(0, 0) == 0 and need >= 2 * 4000
+    f = lib.ps_scan_host
+    H, D = 1 << 41, 1 << 40   # never dereferenced: each call fails validation first
+    assert f(0, 0, None, None, 0, None, 0, None, 0, None) == _lib.PS_OK
+    assert f(0, 0, None, H, n, D, need, D + (1 << 30), ws, None) == _lib.PS_ERR_INVALID_ARG
+    assert f(0, 0, H + 2, H + 8192, n, D, need, D + (1 << 30), ws, None) == _lib.PS_ERR_INVALID_ARG
+    assert f(0, 0, H, H + 8192, n, D + 16, need, D + (1 << 30), ws, None) == _lib.PS_ERR_INVALID_ARG
+    assert f(0, 0, H, H + 400, n, D, need, D + (1 << 30), ws, None) == _lib.PS_ERR_OVERLAP
+    assert f(0, 0, H, H + 8192, n, D, need - 1, D + (1 << 30), ws, None) == _lib.PS_ERR_WORKSPACE_TOO_SMALL
+    assert f(0, 0, H, H + 8192, n, D, need, D + (1 << 30), ws - 1, None) == _lib.PS_ERR_WORKSPACE_TOO_SMALL
+    assert f(9, 0, H, H + 8192, n, D, need, D + (1 << 30), ws, None) == _lib.PS_ERR_INVALID_ARG
+
+
+def test_seeded_argument_errors(lib, no_device):
+    ws = lib.ps_scan_workspace_size(0, 1000)
+    g = lib.ps_scan_seeded
+    # a carry inside the input or the workspace, a misaligned carry
+    assert g(0, 0, FAKE, FAKE + 8192, 1000, FAKE + 40, None, FAKE + (1 << 20), ws, None) == _lib.PS_ERR_OVERLAP
+    assert g(0, 0, FAKE, FAKE + 8192, 1000, None, FAKE + (1 << 20) + 64, FAKE + (1 << 20), ws, None) == \
+        _lib.PS_ERR_OVERLAP
+    assert g(0, 0, FAKE, FAKE + 8192, 1000, FAKE + (1 << 22) + 2, None, FAKE + (1 << 20), ws, None) == \
         _lib.PS_ERR_INVALID_ARG
 
 
