@@ -171,24 +171,64 @@ def barrier(world):
         dist.barrier()
 
 
+def _reduce(v: float, world: int, op) -> float:
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
+    return float(t.item())
+
+
 def max_over_ranks(v: float, world: int) -> float:
     if world == 1:
         return v
-    import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return _reduce(v, world, dist.ReduceOp.MAX)
 
 
 def sum_over_ranks(v: float, world: int) -> float:
     if world == 1:
         return v
-    import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(v, world, dist.ReduceOp.SUM)
+
+
+def replica_stats(local_seconds: float, local_units: float, world: int) -> tuple[float, float]:
+    """Whole-job numbers of N independent replicas: (max time over ranks,
+    units processed by all ranks).  Throughput = units / time."""
+    return max_over_ranks(local_seconds, world), sum_over_ranks(local_units, world)
+
+
+KERNEL_TRAFFIC_FILE = ROOT / "profiles" / "persistent_kernel_i32_excl_2p28_traffic.md"
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = ROOT / "prefix_scan_gb300" / "csrc"
+    for p in sorted(list(csrc.glob("*.cu")) + list(csrc.glob("*.cuh")) + list(csrc.glob("*.h"))):
+        h.update(p.name.encode())
+        h.update(p.read_bytes())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str, n: int):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is for another workload or the kernel sources changed since."""
+    try:
+        kv = {}
+        for line in KERNEL_TRAFFIC_FILE.read_text().splitlines():
+            if line.startswith("- ") and ":" in line:
+                k, _, v = line[2:].partition(":")
+                kv[k.strip()] = v.strip().strip("`")
+        if kv.get("workload") != workload or int(kv.get("n", -1)) != n:
+            return None
+        if kv.get("kernel_sources_sha256") != kernel_sources_sha256():
+            return None
+        return int(kv["dram_bytes_read_per_launch"]) + int(kv["dram_bytes_write_per_launch"])
+    except Exception:
+        return None
 
 
 def cpu_baseline(w: workloads.Workload, target_s: float = 10.0, sample_n: int = 1 << 26) -> dict:
@@ -394,7 +434,7 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
     sampler = ClockSampler(local)
     with sampler:
         t_scan, per = h.timed(args.steps, h.step, world)
-    t_scan = max_over_ranks(t_scan, world)
+    t_scan, units_total = replica_stats(t_scan, float(n * args.steps), world)
     # same-run device-to-device copy of the same bytes, same protocol
     for _ in range(max(3, args.warmup)):
         h.memcpy()
@@ -412,7 +452,6 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
     t_e2e = max_over_ranks(t_e2e, world)
     ok = h.property_check()
 
-    units_total = sum_over_ranks(float(n * args.steps), world)
     gbs = 2.0 * w.itemsize * units_total / t_scan / 1e9
     per_launch = statistics.median(per)
     achieved = bytes_step / per_launch / 1e9
@@ -443,7 +482,8 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
         "gelem_per_s": round(units_total / t_scan / 1e9, 3),
         "memcpy_gbs": round(copy_gbs, 2), "vs_memcpy": round(gbs / copy_gbs, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": args.traffic if args.traffic is not None else recorded_traffic(w.name, n),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "per_launch_ms": round(per_launch * 1000, 4),
