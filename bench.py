@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Benchmark of the single-pass decoupled look-back prefix sum on GB300.
 
-One "step" is one scan call (workspace reset + the single-pass kernel) over
+One "step" is one scan call (one launch of the single-pass kernel) over
 the whole input of the chosen workload, inputs resident in HBM.  Prints ONE
 JSON line (rank 0).  Metric: achieved bandwidth in GB/s with the algorithmic
 traffic 2 * n * sizeof(T) (read every input once, write every output once),
@@ -487,7 +487,7 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "per_launch_ms": round(per_launch * 1000, 4),
-                     "note": "per-launch time spans the workspace reset + the single-pass kernel"},
+                     "note": "one kernel launch per step (no workspace reset); median CUDA-event step time"},
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": n * w.itemsize, "d2h_bytes_per_step": n * w.itemsize,
                 "steps": e2e_steps,

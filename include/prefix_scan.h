@@ -33,9 +33,14 @@
  *     the two arrays, or of either with the workspace, is rejected with
  *     PS_ERR_OVERLAP before anything is enqueued.
  *   - `ws` is a scratch workspace of at least ps_scan_workspace_size(dtype,
- *     n) bytes, 256-byte aligned.  It is reset by every call (an
- *     asynchronous memset enqueued on `stream` before the kernel); two
- *     calls that may run at the same time must not share one.
+ *     n) bytes, 16-byte aligned.  It must be ZERO-FILLED ONCE before its
+ *     first use (ps_workspace_init, cudaMemset, or a zeroed allocation) and
+ *     then left alone between calls: no call resets it, each call leaves it
+ *     ready for the next (any dtype, algorithm or n it is large enough for).
+ *     A workspace that was never zero-filled makes the kernels do nothing
+ *     and ps_get_device_status report PS_ERR_WORKSPACE_NOT_INITIALIZED.
+ *     After an error from a call or from ps_get_device_status, zero it
+ *     again.  Two calls that may run at the same time must not share one.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without waiting for it.
  *   - n == 0 returns PS_OK, touches nothing and accepts NULL pointers.
@@ -46,6 +51,9 @@
  *     launch never does) gives up instead of hanging: the kernel records
  *     PS_ERR_LOOKBACK_TIMEOUT in the workspace, writes unspecified output
  *     and finishes.  Read it with ps_get_device_status().
+ *   - One kernel launch per scan (three for reduce-then-scan): there is no
+ *     per-call workspace reset, because each tile descriptor carries the
+ *     number of the call that wrote it (see ps_workspace_init).
  */
 #ifndef PREFIX_SCAN_H
 #define PREFIX_SCAN_H
@@ -68,20 +76,29 @@ typedef enum ps_status {
     PS_ERR_WORKSPACE_TOO_SMALL = 2, /* ws_bytes < ps_scan_workspace_size(dtype, n) */
     PS_ERR_OVERLAP = 3,             /* partial overlap of in/out, or ws overlapping either */
     PS_ERR_CUDA = 4,                /* a CUDA runtime call failed: see ps_last_cuda_error() */
-    PS_ERR_LOOKBACK_TIMEOUT = 5     /* device side: a look-back gave up waiting */
+    PS_ERR_LOOKBACK_TIMEOUT = 5,    /* device side: a look-back gave up waiting */
+    PS_ERR_WORKSPACE_NOT_INITIALIZED = 6 /* device side: workspace never zero-filled */
 } ps_status;
 
 typedef enum ps_dtype { PS_INT32 = 0, PS_INT64 = 1, PS_FLOAT32 = 2 } ps_dtype;
 
 /*
  * Bytes of workspace a scan of n elements of `dtype` needs (0 for n == 0):
- * a 256-byte header (tile counter, status word) plus one 64-byte slot per
- * tile holding its status descriptor (section 4.1, "partition descriptor":
- * status flag X/A/P plus a value).  Tiles are 8192 elements (32-bit types)
- * or 4096 (int64), so about n/128 bytes (n/64 for int64).  The same size
- * serves every algorithm below.
+ * a 256-byte header (tile counter, call number, status word) plus one
+ * 64-byte slot per tile holding its status descriptor (section 4.1,
+ * "partition descriptor": status flag X/A/P plus a value) and 8 bytes per
+ * tile for the reduce-then-scan comparison path.  Tiles are 8192 elements
+ * (32-bit types) or 4096 (int64), so about n/114 bytes (n/57 for int64).
+ * The same size serves every algorithm below.
  */
 size_t ps_scan_workspace_size(ps_dtype dtype, size_t n);
+
+/*
+ * Zero-fills `ws_bytes` bytes of workspace on `stream` (asynchronous): the
+ * one preparation a workspace needs before its first scan, and after an
+ * error.  Equivalent to cudaMemsetAsync(ws, 0, ws_bytes, stream).
+ */
+ps_status ps_workspace_init(void *ws, size_t ws_bytes, ps_stream_t stream);
 
 /*
  * Single-pass decoupled look-back scans (the product path).
@@ -171,8 +188,9 @@ ps_status ps_scan_host(ps_dtype dtype, int exclusive, const void *h_in, void *h_
                        ps_stream_t stream);
 
 /*
- * Waits for `stream`, then reads the device-side status the last scan
- * that used `ws` left there (PS_OK or PS_ERR_LOOKBACK_TIMEOUT) into *out.
+ * Waits for `stream`, then reads into *out the device-side status of the
+ * last scan that used `ws`: PS_OK, PS_ERR_LOOKBACK_TIMEOUT, or
+ * PS_ERR_WORKSPACE_NOT_INITIALIZED (the workspace was never zero-filled).
  * Returns PS_ERR_CUDA if the wait or the copy fails.
  */
 ps_status ps_get_device_status(const void *ws, ps_stream_t stream, ps_status *out);
@@ -203,18 +221,19 @@ size_t ps_tile_elements(ps_dtype dtype);
  *     anything is enqueued (the fixed scratch holds descriptors for at most
  *     that many elements).
  *   - The first call on a device looks up the scratch array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first
- *     call before any stream capture.  A failed look-up returns PS_ERR_CUDA
- *     (see ps_last_cuda_error).
- *   - All calls on a device share the one array and every call clears it on
- *     `stream` before use.  Calls whose GPU work can overlap (other streams,
- *     unordered host threads) race on it and produce wrong results; calls
- *     ordered on one stream are safe.
+ *     (cudaGetSymbolAddress, with that device current) and zero-fills the
+ *     array on `stream`; make that first call before any stream capture.  A
+ *     failed look-up returns PS_ERR_CUDA (see ps_last_cuda_error).
+ *   - All calls on a device share the one array, and each call leaves it
+ *     ready for the next (as any workspace, see ps_workspace_init).  Calls
+ *     whose GPU work can overlap (other streams, unordered host threads)
+ *     race on it and produce wrong results; calls ordered on one stream are
+ *     safe.
  *   - Device-side timeouts can be read with ps_get_device_status only
  *     through the regular entry points (there is no caller workspace here).
  */
 #define PS_NOALLOC_MAX_ELEMENTS 536870912u /* 2^29 elements */
-#define PS_NOALLOC_SCRATCH_BYTES (256u + 64u * (PS_NOALLOC_MAX_ELEMENTS / 8192u)) /* 4 MiB + 256 */
+#define PS_NOALLOC_SCRATCH_BYTES (256u + 72u * (PS_NOALLOC_MAX_ELEMENTS / 8192u)) /* 4.5 MiB + 256 */
 ps_status ps_scan_inclusive_i32_noalloc(const int32_t *in, int32_t *out, size_t n,
                                         ps_stream_t stream);
 

@@ -27,23 +27,36 @@ enum { PS_FLAG_X = 0, PS_FLAG_A = 1, PS_FLAG_P = 2 };
 size_t ps_testing_descriptor_bytes(ps_dtype dtype);
 
 /*
- * Host-side encoding of one descriptor: writes ps_testing_descriptor_bytes
- * bytes to `out` (host memory) holding `flag` and the value at `value`
- * (host pointer to one element of `dtype`).  PS_ERR_INVALID_ARG on a bad
- * dtype, flag or NULL pointer.
+ * Host-side encoding of one descriptor of call `epoch` (< 2^30): writes
+ * the first 8 bytes (16 for int64) of a ps_testing_descriptor_bytes-byte
+ * slot to `out` (host memory), holding `flag`, `epoch` and the value at
+ * `value` (host pointer to one element of `dtype`).  PS_ERR_INVALID_ARG on
+ * a bad dtype, flag, epoch or NULL pointer.
  */
-ps_status ps_testing_encode_descriptor(ps_dtype dtype, int flag, const void *value, void *out);
+ps_status ps_testing_encode_descriptor(ps_dtype dtype, int flag, uint32_t epoch, const void *value,
+                                       void *out);
 
 /*
- * Runs the look-back of tile `tile` (>= 1) with one warp over the device
- * array `desc` of at least `tile` descriptors, polling at most `max_polls`
- * times.  Writes the exclusive prefix (one element of `dtype`) to device
- * `result`; `status` (device, one uint32, caller-zeroed) receives
- * PS_ERR_LOOKBACK_TIMEOUT if the wait ran out.  Only descriptors
- * 0 .. tile-1 are read.  Asynchronous on `stream`.
+ * Runs the look-back of tile `tile` (>= 1) of call `epoch` with one warp
+ * over the device array `desc` of at least `tile` descriptor slots, polling
+ * at most `max_polls` times.  Writes the exclusive prefix (one element of
+ * `dtype`) to device `result`; `status` (device, one uint64, caller-zeroed)
+ * receives epoch << 8 | PS_ERR_LOOKBACK_TIMEOUT if the wait ran out.  Only
+ * descriptors 0 .. tile-1 are read; descriptors of another epoch count as
+ * not published.  Asynchronous on `stream`.
  */
-ps_status ps_testing_lookback(ps_dtype dtype, const void *desc, int64_t tile, uint32_t max_polls,
-                              void *result, uint32_t *status, ps_stream_t stream);
+ps_status ps_testing_lookback(ps_dtype dtype, const void *desc, int64_t tile, uint32_t epoch,
+                              uint32_t max_polls, void *result, uint64_t *status,
+                              ps_stream_t stream);
+
+/*
+ * The call number (epoch, modulo 2^30) the next scan on `ws` will run as:
+ * read after waiting for `stream`, or set (marking the workspace as in
+ * use), so that a test can bring a workspace to the epoch wrap-around
+ * without 2^30 calls.
+ */
+ps_status ps_testing_workspace_epoch(const void *ws, ps_stream_t stream, uint32_t *epoch);
+ps_status ps_testing_set_workspace_epoch(void *ws, uint32_t epoch, ps_stream_t stream);
 
 #ifdef __cplusplus
 }

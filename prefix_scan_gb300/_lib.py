@@ -18,6 +18,7 @@ PS_ERR_WORKSPACE_TOO_SMALL = 2
 PS_ERR_OVERLAP = 3
 PS_ERR_CUDA = 4
 PS_ERR_LOOKBACK_TIMEOUT = 5
+PS_ERR_WORKSPACE_NOT_INITIALIZED = 6
 
 PS_INT32, PS_INT64, PS_FLOAT32 = 0, 1, 2
 PS_ALGO_DECOUPLED_LOOKBACK, PS_ALGO_REDUCE_THEN_SCAN, PS_ALGO_CHAINED = 0, 1, 2
@@ -34,8 +35,11 @@ SIGNATURES = {
     "ps_status_string": (ctypes.c_char_p, [_int]),
     "ps_last_cuda_error": (_int, []),
     "ps_testing_descriptor_bytes": (_sz, [_int]),
-    "ps_testing_encode_descriptor": (_int, [_int, _int, _vp, _vp]),
-    "ps_testing_lookback": (_int, [_int, _vp, _i64, _u32, _vp, _vp, _vp]),
+    "ps_testing_encode_descriptor": (_int, [_int, _int, _u32, _vp, _vp]),
+    "ps_testing_lookback": (_int, [_int, _vp, _i64, _u32, _u32, _vp, _vp, _vp]),
+    "ps_testing_workspace_epoch": (_int, [_vp, _vp, ctypes.POINTER(_u32)]),
+    "ps_testing_set_workspace_epoch": (_int, [_vp, _u32, _vp]),
+    "ps_workspace_init": (_int, [_vp, _sz, _vp]),
 }
 SIGNATURES["ps_scan_inclusive_i32_noalloc"] = (_int, [_vp, _vp, _sz, _vp])
 SIGNATURES["ps_scan_seeded"] = (_int, [_int, _int, _vp, _vp, _sz, _vp, _vp, _vp, _sz, _vp])

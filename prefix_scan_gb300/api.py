@@ -38,8 +38,10 @@ def tile_elements(dtype: torch.dtype) -> int:
 
 
 def alloc_workspace(dtype: torch.dtype, n: int, device=None) -> torch.Tensor:
-    """A uint8 device tensor large enough for a scan of ``n`` elements."""
-    return torch.empty(max(workspace_size(dtype, n), 1), dtype=torch.uint8, device=device or "cuda")
+    """A zero-filled uint8 device tensor large enough for a scan of ``n``
+    elements, ready for any number of calls (it must not be reused for
+    anything else in between)."""
+    return torch.zeros(max(workspace_size(dtype, n), 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def _stream_handle(stream, device) -> ctypes.c_void_p:
@@ -75,7 +77,7 @@ def scan(x: torch.Tensor, *, exclusive: bool = False, out: torch.Tensor | None =
     lib = _lib.load()
     need = int(lib.ps_scan_workspace_size(code, n))
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
     elif workspace.numel() * workspace.element_size() < need or workspace.device != x.device:
         raise ValueError(f"prefix scan: workspace needs {need} bytes on {x.device}")
     ws_bytes = workspace.numel() * workspace.element_size()
@@ -122,7 +124,7 @@ def scan_seeded(x: torch.Tensor, carry_in: torch.Tensor | None = None,
     lib = _lib.load()
     need = int(lib.ps_scan_workspace_size(code, n))
     if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=x.device)
     st = lib.ps_scan_seeded(code, int(exclusive), x.data_ptr() if n else None,
                             out.data_ptr() if n else None, n,
                             carry_in.data_ptr() if carry_in is not None else None,
@@ -143,7 +145,7 @@ class HostScanBuffers:
         dev = torch.device(device or "cuda")
         self.dtype, self.n = dtype, n
         self.staging = torch.empty(max(host_staging_size(dtype, n), 256), dtype=torch.uint8, device=dev)
-        self.workspace = torch.empty(max(workspace_size(dtype, n), 1), dtype=torch.uint8, device=dev)
+        self.workspace = torch.zeros(max(workspace_size(dtype, n), 16), dtype=torch.uint8, device=dev)
 
 
 def scan_host(x: torch.Tensor, *, exclusive: bool = False, out: torch.Tensor | None = None,

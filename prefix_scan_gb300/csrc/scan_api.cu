@@ -47,13 +47,15 @@ ps_status check_args(ps_dtype dt, const void *in, const void *out, size_t n, con
 
 template <typename T>
 ps_status run(ps_algo algo, bool exclusive, const void *in, void *out, size_t n, void *ws,
-              cudaStream_t s, const void *carry_in = nullptr, void *carry_out = nullptr) {
+              size_t ws_bytes, cudaStream_t s, const void *carry_in = nullptr,
+              void *carry_out = nullptr) {
     cudaError_t e;
     unsigned char *w = static_cast<unsigned char *>(ws);
     switch (algo) {
     case PS_ALGO_DECOUPLED_LOOKBACK:
     case PS_ALGO_CHAINED: {
-        ps::PassArgs a{in, out, (unsigned long long)n, w, carry_in, carry_out, ps::kDefaultMaxPolls};
+        ps::PassArgs a{in, out, (unsigned long long)n, w, carry_in, carry_out,
+                       (unsigned long long)(ws_bytes & ~(size_t)7), ps::kDefaultMaxPolls};
         e = ps::launch_single_pass<T>(a, exclusive,
                                       algo == PS_ALGO_CHAINED ? ps::Lookback::Chained
                                                               : ps::Lookback::Decoupled, s);
@@ -77,9 +79,9 @@ ps_status dispatch(ps_algo algo, ps_dtype dt, int exclusive, const void *in, voi
     const ps_status st = check_args(dt, in, out, n, ws, ws_bytes);
     if (st != PS_OK) return st;
     switch (dt) {
-    case PS_INT32: return run<int32_t>(algo, exclusive != 0, in, out, n, ws, s);
-    case PS_INT64: return run<int64_t>(algo, exclusive != 0, in, out, n, ws, s);
-    case PS_FLOAT32: return run<float>(algo, exclusive != 0, in, out, n, ws, s);
+    case PS_INT32: return run<int32_t>(algo, exclusive != 0, in, out, n, ws, ws_bytes, s);
+    case PS_INT64: return run<int64_t>(algo, exclusive != 0, in, out, n, ws, ws_bytes, s);
+    case PS_FLOAT32: return run<float>(algo, exclusive != 0, in, out, n, ws, ws_bytes, s);
     }
     return PS_ERR_INVALID_ARG;
 }
@@ -110,9 +112,9 @@ ps_status ps::scan_seeded(ps_dtype dt, int exclusive, const void *in, void *out,
                   ranges_overlap(c, es, ws, wsb)))
             return PS_ERR_OVERLAP;
     switch (dt) {
-    case PS_INT32: return run<int32_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, s, carry_in, carry_out);
-    case PS_INT64: return run<int64_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, s, carry_in, carry_out);
-    case PS_FLOAT32: return run<float>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, s, carry_in, carry_out);
+    case PS_INT32: return run<int32_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes, s, carry_in, carry_out);
+    case PS_INT64: return run<int64_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes, s, carry_in, carry_out);
+    case PS_FLOAT32: return run<float>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes, s, carry_in, carry_out);
     }
     return PS_ERR_INVALID_ARG;
 }
@@ -155,15 +157,28 @@ ps_status ps_scan_seeded(ps_dtype dtype, int exclusive, const void *in, void *ou
                            (cudaStream_t)stream);
 }
 
+ps_status ps_workspace_init(void *ws, size_t ws_bytes, ps_stream_t stream) {
+    if (ws_bytes == 0) return PS_OK;
+    if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 16 != 0) return PS_ERR_INVALID_ARG;
+    const cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream);
+    return e == cudaSuccess ? PS_OK : cuda_fail(e);
+}
+
 ps_status ps_get_device_status(const void *ws, ps_stream_t stream, ps_status *out) {
     if (ws == nullptr || out == nullptr) return PS_ERR_INVALID_ARG;
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    unsigned int st = 0;
-    e = cudaMemcpy(&st, static_cast<const unsigned char *>(ws) + offsetof(ps::Header, status),
-                   sizeof(st), cudaMemcpyDeviceToHost);
+    ps::Header h;
+    e = cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e);
-    *out = (ps_status)st;
+    if (!((h.magic == ps::kWorkspaceMagic && h.epoch <= ps::kEpochMask) || (h.magic == 0 && h.epoch == 0))) {
+        *out = PS_ERR_WORKSPACE_NOT_INITIALIZED;
+        return PS_OK;
+    }
+    // the last call that completed ran as epoch - 1; older errors are history
+    const uint32_t last = (h.epoch - 1u) & ps::kEpochMask;
+    const bool current = h.magic == ps::kWorkspaceMagic && (uint32_t)(h.status >> 8) == last;
+    *out = current ? (ps_status)(h.status & 0xffu) : PS_OK;
     return PS_OK;
 }
 
@@ -175,6 +190,7 @@ const char *ps_status_string(ps_status status) {
     case PS_ERR_OVERLAP: return "PS_ERR_OVERLAP";
     case PS_ERR_CUDA: return "PS_ERR_CUDA";
     case PS_ERR_LOOKBACK_TIMEOUT: return "PS_ERR_LOOKBACK_TIMEOUT";
+    case PS_ERR_WORKSPACE_NOT_INITIALIZED: return "PS_ERR_WORKSPACE_NOT_INITIALIZED";
     }
     return "PS_ERR_UNKNOWN";
 }
@@ -188,35 +204,62 @@ size_t ps_testing_descriptor_bytes(ps_dtype dtype) {
     return ps::desc_bytes(dtype);
 }
 
-ps_status ps_testing_encode_descriptor(ps_dtype dtype, int flag, const void *value, void *out) {
-    if (!valid_dtype(dtype) || value == nullptr || out == nullptr) return PS_ERR_INVALID_ARG;
+ps_status ps_testing_encode_descriptor(ps_dtype dtype, int flag, uint32_t epoch, const void *value,
+                                       void *out) {
+    if (!valid_dtype(dtype) || value == nullptr || out == nullptr || epoch > ps::kEpochMask)
+        return PS_ERR_INVALID_ARG;
     if (flag != PS_FLAG_X && flag != PS_FLAG_A && flag != PS_FLAG_P) return PS_ERR_INVALID_ARG;
-    const uint64_t f = (uint64_t)flag << 32;
+    const uint64_t t = ((uint64_t)epoch << 34) | ((uint64_t)flag << 32);
     if (dtype == PS_INT64) {
         uint64_t v;
         std::memcpy(&v, value, 8);
-        const uint64_t w[2] = {f | (v & 0xffffffffull), f | (v >> 32)};
+        const uint64_t w[2] = {t | (v & 0xffffffffull), t | (v >> 32)};
         std::memcpy(out, w, 16);
     } else {
         uint32_t v;
         std::memcpy(&v, value, 4);
-        const uint64_t w = f | v;
+        const uint64_t w = t | v;
         std::memcpy(out, &w, 8);
     }
     return PS_OK;
 }
 
-ps_status ps_testing_lookback(ps_dtype dtype, const void *desc, int64_t tile, uint32_t max_polls,
-                              void *result, uint32_t *status, ps_stream_t stream) {
-    if (!valid_dtype(dtype) || desc == nullptr || result == nullptr || status == nullptr || tile < 1)
+ps_status ps_testing_lookback(ps_dtype dtype, const void *desc, int64_t tile, uint32_t epoch,
+                              uint32_t max_polls, void *result, uint64_t *status,
+                              ps_stream_t stream) {
+    if (!valid_dtype(dtype) || desc == nullptr || result == nullptr || status == nullptr || tile < 1 ||
+        epoch > ps::kEpochMask)
         return PS_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
+    unsigned long long *st = reinterpret_cast<unsigned long long *>(status);
     cudaError_t e;
     switch (dtype) {
-    case PS_INT32: e = ps::launch_lookback_probe<int32_t>(desc, tile, max_polls, result, status, s); break;
-    case PS_INT64: e = ps::launch_lookback_probe<int64_t>(desc, tile, max_polls, result, status, s); break;
-    default: e = ps::launch_lookback_probe<float>(desc, tile, max_polls, result, status, s); break;
+    case PS_INT32: e = ps::launch_lookback_probe<int32_t>(desc, tile, epoch, max_polls, result, st, s); break;
+    case PS_INT64: e = ps::launch_lookback_probe<int64_t>(desc, tile, epoch, max_polls, result, st, s); break;
+    default: e = ps::launch_lookback_probe<float>(desc, tile, epoch, max_polls, result, st, s); break;
     }
+    return e == cudaSuccess ? PS_OK : cuda_fail(e);
+}
+
+ps_status ps_testing_workspace_epoch(const void *ws, ps_stream_t stream, uint32_t *epoch) {
+    if (ws == nullptr || epoch == nullptr) return PS_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(epoch, static_cast<const unsigned char *>(ws) + offsetof(ps::Header, epoch),
+                       sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? PS_OK : cuda_fail(e);
+}
+
+ps_status ps_testing_set_workspace_epoch(void *ws, uint32_t epoch, ps_stream_t stream) {
+    if (ws == nullptr || epoch > ps::kEpochMask) return PS_ERR_INVALID_ARG;
+    const uint32_t magic = ps::kWorkspaceMagic;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(static_cast<unsigned char *>(ws) + offsetof(ps::Header, epoch), &epoch,
+                       sizeof(uint32_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(static_cast<unsigned char *>(ws) + offsetof(ps::Header, magic), &magic,
+                       sizeof(uint32_t), cudaMemcpyHostToDevice);
     return e == cudaSuccess ? PS_OK : cuda_fail(e);
 }
 

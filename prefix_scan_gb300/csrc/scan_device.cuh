@@ -105,52 +105,71 @@ __device__ __forceinline__ void st_stream(ulonglong2 *p, const ulonglong2 &v) {
 // ---- tile status descriptors ----------------------------------------------
 // Flag and value share one single-copy-atomic 64-bit word, so a reader that
 // sees the flag also sees the value and no memory fence is needed
-// ("fence-free descriptor updates", section 4.4).  For 32-bit values:
-//     word = flag << 32 | bits(value)
-// For 64-bit values two such words are written with one 16-byte store:
-//     word0 = flag << 32 | low half,  word1 = flag << 32 | high half
-// and a reader accepts the pair only when both flags agree (each word is
-// atomic on its own; a torn pair shows differing flags and is re-polled).
+// ("fence-free descriptor updates", section 4.4).  The word also carries the
+// epoch (call number) of the call that wrote it; a word from another call
+// reads as X, so no call has to reset the descriptors.  For 32-bit values:
+//     word = epoch << 34 | flag << 32 | bits(value)
+// For 64-bit values two such words are written with one 16-byte store, one
+// with the low half and one with the high half of the value, and a reader
+// accepts the pair only when both carry the same flag and the current epoch
+// (each word is atomic on its own; a torn pair is re-polled).
+__device__ __forceinline__ unsigned long long desc_tag(uint32_t flag, uint32_t epoch) {
+    return ((unsigned long long)epoch << 34) | ((unsigned long long)flag << 32);
+}
+__device__ __forceinline__ uint32_t desc_flag(unsigned long long w, uint32_t epoch) {
+    return (uint32_t)(w >> 34) == epoch ? (uint32_t)(w >> 32) & 3u : kFlagX;
+}
+
 template <typename U, int DW> struct Desc;
 
 template <typename U> struct Desc<U, 1> {
-    static __device__ __forceinline__ void store(void *base, long long i, uint32_t flag, U v) {
-        unsigned long long w = ((unsigned long long)flag << 32) | to_bits(v);
+    static __device__ __forceinline__ void store(void *base, long long i, uint32_t flag, U v,
+                                                 uint32_t epoch) {
+        unsigned long long w = desc_tag(flag, epoch) | to_bits(v);
         unsigned long long *p = reinterpret_cast<unsigned long long *>(
             reinterpret_cast<unsigned char *>(base) + i * kDescStride32);
         asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(w) : "memory");
     }
-    static __device__ __forceinline__ void load(const void *base, long long i, uint32_t &flag, U &v) {
+    static __device__ __forceinline__ void load(const void *base, long long i, uint32_t epoch,
+                                                uint32_t &flag, U &v) {
         const unsigned long long *p = reinterpret_cast<const unsigned long long *>(
             reinterpret_cast<const unsigned char *>(base) + i * kDescStride32);
         unsigned long long w;
         asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
-        flag = (uint32_t)(w >> 32);
+        flag = desc_flag(w, epoch);
         v = from_bits<U>((uint32_t)w);
     }
 };
 
 template <> struct Desc<unsigned long long, 2> {
     using U = unsigned long long;
-    static __device__ __forceinline__ void store(void *base, long long i, uint32_t flag, U v) {
-        unsigned long long f = (unsigned long long)flag << 32;
-        unsigned long long w0 = f | (v & 0xffffffffull), w1 = f | (v >> 32);
+    static __device__ __forceinline__ void store(void *base, long long i, uint32_t flag, U v,
+                                                 uint32_t epoch) {
+        const unsigned long long t = desc_tag(flag, epoch);
+        unsigned long long w0 = t | (v & 0xffffffffull), w1 = t | (v >> 32);
         unsigned long long *p = reinterpret_cast<unsigned long long *>(
             reinterpret_cast<unsigned char *>(base) + i * kDescStride64);
         asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1,%2};" :: "l"(p), "l"(w0), "l"(w1)
                      : "memory");
     }
-    static __device__ __forceinline__ void load(const void *base, long long i, uint32_t &flag, U &v) {
+    static __device__ __forceinline__ void load(const void *base, long long i, uint32_t epoch,
+                                                uint32_t &flag, U &v) {
         const unsigned long long *p = reinterpret_cast<const unsigned long long *>(
             reinterpret_cast<const unsigned char *>(base) + i * kDescStride64);
         unsigned long long w0, w1;
         asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p)
                      : "memory");
-        uint32_t f0 = (uint32_t)(w0 >> 32), f1 = (uint32_t)(w1 >> 32);
+        const uint32_t f0 = desc_flag(w0, epoch), f1 = desc_flag(w1, epoch);
         flag = (f0 == f1) ? f0 : kFlagX;
         v = (w0 & 0xffffffffull) | (w1 << 32);
     }
 };
+
+// A device-side error of call `epoch` (ps_get_device_status reads it).
+__device__ __forceinline__ void report_error(unsigned long long *status, uint32_t epoch,
+                                             ps_status code) {
+    atomicExch(status, ((unsigned long long)epoch << 8) | (unsigned long long)code);
+}
 
 // ---- warp primitives -------------------------------------------------------
 // Inclusive Kogge-Stone scan over the 32 lanes with shuffles (the warp scan
@@ -200,8 +219,8 @@ __device__ __forceinline__ void poll_backoff(uint32_t polls) {
 // PS_ERR_LOOKBACK_TIMEOUT and the missing tiles count as P with the
 // identity, so the warp finishes (with a wrong value) instead of hanging.
 template <typename U, int DW, int K>
-__device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_t max_polls,
-                                       unsigned int *status) {
+__device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_t epoch,
+                                       uint32_t max_polls, unsigned long long *status) {
     const int lane = threadIdx.x & 31;
     U excl = U(0);
     long long base = tile - 1;
@@ -215,7 +234,7 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
             const long long idx = base - (long long)(lane * K + j);
             f[j] = kFlagP;
             v[j] = U(0);
-            if (idx >= 0) Desc<U, DW>::load(desc, idx, f[j], v[j]);
+            if (idx >= 0) Desc<U, DW>::load(desc, idx, epoch, f[j], v[j]);
         }
         bool done;
         while (true) {
@@ -249,7 +268,7 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
                 for (int j = 0; j < K; ++j) {
                     const int pos = lane * K + j;
                     if (f[j] == kFlagX && pos < pos_p)
-                        Desc<U, DW>::load(desc, base - (long long)pos, f[j], v[j]);
+                        Desc<U, DW>::load(desc, base - (long long)pos, epoch, f[j], v[j]);
                 }
                 continue;
             }
@@ -266,7 +285,7 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
         if (done) break;
         base -= 32 * K;
     }
-    if (gave_up && lane == 0) atomicMax(status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+    if (gave_up && lane == 0) report_error(status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
     return excl;
 }
 
@@ -275,25 +294,73 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
 // predecessor's inclusive prefix.  Comparison path only; bounded like the
 // look-back.
 template <typename U, int DW>
-__device__ __forceinline__ U chained_wait(const void *desc, long long tile, uint32_t max_polls,
-                                          unsigned int *status) {
+__device__ __forceinline__ U chained_wait(const void *desc, long long tile, uint32_t epoch,
+                                          uint32_t max_polls, unsigned long long *status) {
     const int lane = threadIdx.x & 31;
     uint32_t flag = kFlagX;
     U val = U(0);
     uint32_t polls = 0;
     if (lane == 0) {
-        Desc<U, DW>::load(desc, tile - 1, flag, val);
+        Desc<U, DW>::load(desc, tile - 1, epoch, flag, val);
         while (flag != kFlagP) {
             if (++polls > max_polls) {
-                atomicMax(status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+                report_error(status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 val = U(0);
                 break;
             }
             poll_backoff(polls);
-            Desc<U, DW>::load(desc, tile - 1, flag, val);
+            Desc<U, DW>::load(desc, tile - 1, epoch, flag, val);
         }
     }
     return __shfl_sync(kFull, val, 0);
+}
+
+// ---- call protocol ----------------------------------------------------------
+// Start of a call, by every CTA: the epoch of this call, or false if the
+// header is neither fresh (all zero) nor one this library left behind -- a
+// workspace that was never zero-filled -- in which case the CTA does nothing
+// (ps_get_device_status then reports PS_ERR_WORKSPACE_NOT_INITIALIZED).
+__device__ __forceinline__ bool begin_call(const Header *hdr, uint32_t *epoch) {
+    const uint32_t magic = *reinterpret_cast<const volatile uint32_t *>(&hdr->magic);
+    const uint32_t e = *reinterpret_cast<const volatile uint32_t *>(&hdr->epoch);
+    *epoch = e;
+    return (magic == kWorkspaceMagic && e <= kEpochMask) || (magic == 0u && e == 0u);
+}
+
+// End of a call, by every thread of every CTA once the CTA's work is done.
+// The last CTA to finish (counted with a fenced atomic, so all other CTAs'
+// writes precede it) puts the header back for the next call: tile counter
+// and done count to 0, epoch + 1.  When the epoch wraps it first clears
+// every descriptor slot the workspace has ever been declared to hold, so no
+// descriptor written 2^30 calls ago can pass for a current one.  No CTA
+// waits for another here.
+__device__ __forceinline__ void finish_call(Header *hdr, unsigned char *ws, unsigned long long ws_bytes,
+                                            uint32_t epoch) {
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned int prev = atomicAdd(&hdr->done, 1u);
+        s_last = (prev == gridDim.x * gridDim.y * gridDim.z - 1);
+        if (s_last) __threadfence();
+    }
+    __syncthreads();
+    if (!s_last) return;
+    const unsigned long long cap = hdr->capacity > ws_bytes ? hdr->capacity : ws_bytes;
+    if (epoch == kEpochMask) {
+        unsigned long long *p = reinterpret_cast<unsigned long long *>(ws + kHeaderBytes);
+        const unsigned long long words = (cap - kHeaderBytes) / 8;
+        for (unsigned long long i = threadIdx.x; i < words; i += blockDim.x) p[i] = 0ull;
+        __threadfence();
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        hdr->capacity = cap;
+        hdr->tile_counter = 0ull;
+        hdr->done = 0u;
+        hdr->epoch = (epoch + 1u) & kEpochMask;
+        hdr->magic = kWorkspaceMagic;
+    }
 }
 
 }  // namespace ps

@@ -12,18 +12,29 @@
 namespace ps {
 
 // ---- workspace layout ------------------------------------------------------
-// [0, 256)        header: tile counter, status word, carry slots
-// [256, ...)      one status descriptor per tile (8 B for 32-bit types,
-//                 16 B for 64-bit types), or the tile aggregates of the
-//                 reduce-then-scan comparison path (same footprint).
+// [0, 256)                 header
+// [256, 256 + D)           descriptor slots, one per tile of a single-pass scan
+// [256 + D, 256 + D + P)   tile aggregates of the reduce-then-scan comparison
+//                          path (its own region: it never disturbs descriptors)
+//
+// No call resets the workspace before it starts.  A workspace is zero-filled
+// once, before its first use; from then on every call leaves it ready for the
+// next: descriptors carry the number ("epoch") of the call that wrote them,
+// so those of earlier calls read as "nothing published", and the last CTA of
+// a call puts the tile counter back to 0 and advances the epoch.
 struct Header {
-    unsigned long long tile_counter;  // dynamic tile ids (atomicAdd)
-    unsigned int status;              // ps_status written by the device
-    unsigned int pad0;
-    unsigned long long carry[4];      // device-side carries (host streaming)
+    unsigned long long tile_counter;  // dynamic tile ids; 0 between calls
+    unsigned long long status;        // epoch << 8 | ps_status of a device-side error
+    unsigned long long capacity;      // largest ws_bytes any call declared (cleared on wrap)
+    unsigned int done;                // CTAs finished in the running call; 0 between calls
+    unsigned int epoch;               // number of this call, modulo 2^30
+    unsigned int magic;               // 0 in a fresh workspace, kWorkspaceMagic once used
 };
 constexpr size_t kHeaderBytes = 256;
 static_assert(sizeof(Header) <= kHeaderBytes, "header too large");
+constexpr uint32_t kEpochBits = 30;
+constexpr uint32_t kEpochMask = (1u << kEpochBits) - 1;
+constexpr uint32_t kWorkspaceMagic = 0x50534742u;
 
 // Tile geometry: THREADS scanning threads per tile, ITEMS elements per
 // thread (in rows of 16-byte vectors): 8192-element tiles for 32-bit types,
@@ -90,9 +101,13 @@ constexpr size_t elem_bytes(ps_dtype dt) { return dt == PS_INT64 ? 8 : 4; }
 constexpr size_t desc_bytes(ps_dtype dt) { return dt == PS_INT64 ? kDescStride64 : kDescStride32; }
 constexpr size_t num_tiles(ps_dtype dt, size_t n) { return (n + tile_elems(dt) - 1) / tile_elems(dt); }
 constexpr size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+constexpr size_t desc_region_bytes(ps_dtype dt, size_t n) {
+    return round_up(num_tiles(dt, n) * desc_bytes(dt), 256);
+}
+constexpr size_t partials_offset(ps_dtype dt, size_t n) { return kHeaderBytes + desc_region_bytes(dt, n); }
 constexpr size_t workspace_bytes(ps_dtype dt, size_t n) {
     if (n == 0) return 0;
-    return kHeaderBytes + round_up(num_tiles(dt, n) * desc_bytes(dt), 256);
+    return partials_offset(dt, n) + round_up(num_tiles(dt, n) * 8, 256);
 }
 
 // Default cap on look-back polls before a CTA gives up (each poll is at
@@ -114,6 +129,7 @@ struct PassArgs {
     unsigned char *ws;             // workspace base (header + descriptors)
     const void *carry_in;          // optional device scalar added to every output
     void *carry_out;               // optional device scalar: inclusive total
+    unsigned long long ws_bytes;   // workspace capacity (cleared when the epoch wraps)
     uint32_t max_polls;
 };
 
@@ -121,9 +137,9 @@ struct PassArgs {
 template <typename T>
 cudaError_t launch_persistent(const PassArgs &a, bool exclusive, cudaStream_t s);
 
-// Enqueue one single-pass scan (workspace reset + kernel).  T is int32_t,
-// int64_t or float.  Decoupled look-back on 16-byte aligned arrays runs the
-// persistent kernel; otherwise one CTA per tile.
+// Enqueue one single-pass scan (one kernel; the workspace needs no reset).
+// T is int32_t, int64_t or float.  Decoupled look-back on 16-byte aligned
+// arrays runs the persistent kernel; otherwise one CTA per tile.
 template <typename T>
 cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s);
 
@@ -137,10 +153,12 @@ cudaError_t launch_reduce_then_scan(const void *in, void *out, unsigned long lon
                                     unsigned char *ws, bool exclusive, cudaStream_t s);
 
 // Test hook: run the look-back alone for `tile` over a prepared descriptor
-// array (one warp), writing the exclusive prefix and a status word.
+// array (one warp) as call `epoch`, writing the exclusive prefix and a
+// status word.
 template <typename T>
-cudaError_t launch_lookback_probe(const void *desc, long long tile, uint32_t max_polls,
-                                  void *result, unsigned int *status, cudaStream_t s);
+cudaError_t launch_lookback_probe(const void *desc, long long tile, uint32_t epoch,
+                                  uint32_t max_polls, void *result, unsigned long long *status,
+                                  cudaStream_t s);
 
 // Records `e` as the calling thread's last CUDA error (ps_last_cuda_error).
 void note_cuda_error(cudaError_t e);

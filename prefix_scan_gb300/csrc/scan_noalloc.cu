@@ -12,14 +12,14 @@
 //
 // Consequences of a file-scope device array:
 //   - every GPU that loads this library holds the array
-//     (PS_NOALLOC_SCRATCH_BYTES, 4 MiB + 256 bytes) until the process exits;
+//     (PS_NOALLOC_SCRATCH_BYTES, 4.5 MiB + 256 bytes) until the process exits;
 //   - all calls on a device share it: two calls whose work overlaps on the
 //     GPU (different streams, or different host threads without ordering)
 //     race on it and give wrong results; calls on one stream are ordered and
 //     safe;
-//   - it keeps whatever the last call left there, so every call clears the
-//     part it uses (header and descriptors) with cudaMemsetAsync on the
-//     caller's stream before the kernel, as the regular entry point does.
+//   - it keeps what the last call left there, which is exactly the state the
+//     next call needs (a workspace is zero-filled once and every call leaves
+//     it ready for the next); the first call on a device zero-fills it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -45,10 +45,11 @@ std::mutex g_setup_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
 
 // Once per device, with that device current: look up the device address of
-// the scratch array.  Looking up the symbol may load the library's device
-// code onto the device, which is why the first call on a device should not
-// be made while a stream is being captured.
-cudaError_t scratch_for_current_device(void **out) {
+// the scratch array and zero-fill it on the caller's stream.  Looking up the
+// symbol may load the library's device code onto the device, which is why
+// the first call on a device should not be made while a stream is being
+// captured.
+cudaError_t scratch_for_current_device(cudaStream_t stream, void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -57,6 +58,9 @@ cudaError_t scratch_for_current_device(void **out) {
     if (g_scratch_ptr[dev] == nullptr) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        // a workspace starts zero-filled; device globals are, but make sure
+        e = cudaMemsetAsync(p, 0, PS_NOALLOC_SCRATCH_BYTES, stream);
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = p;
     }
@@ -71,7 +75,7 @@ extern "C" ps_status ps_scan_inclusive_i32_noalloc(const int32_t *in, int32_t *o
     if (n == 0) return PS_OK;
     if (n > (size_t)PS_NOALLOC_MAX_ELEMENTS) return PS_ERR_WORKSPACE_TOO_SMALL;
     void *scratch = nullptr;
-    const cudaError_t e = scratch_for_current_device(&scratch);
+    const cudaError_t e = scratch_for_current_device((cudaStream_t)stream, &scratch);
     if (e != cudaSuccess) {
         ps::note_cuda_error(e);  // readable with ps_last_cuda_error()
         return PS_ERR_CUDA;

@@ -132,6 +132,9 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     const T *in = reinterpret_cast<const T *>(a.in);
     T *out = reinterpret_cast<T *>(a.out);
 
+    uint32_t epoch;
+    if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA: nothing runs
+
     if (tid == 0) {
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(&full[s], 1);
@@ -152,7 +155,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 if (k >= kPStages) {
                     const uint32_t parity = (uint32_t)((k / kPStages - 1) & 1);
                     if (!mbar_wait(&empty[s], parity)) {   // never in a correct run
-                        atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+                        report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                         break;
                     }
                 }
@@ -167,10 +170,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 if (t >= num_tiles) break;
             }
         }
-        return;
-    }
-
-    if (warp == kPCW + 1) {
+    } else if (warp == kPCW + 1) {
         // ---------------- aggregator warp ----------------
         // Reduces each tile as soon as its copy lands and publishes A (P for
         // tile 0) at once, independently of any look-back (step 3 of
@@ -178,7 +178,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         for (long long k = 0;; ++k) {
             const int s = (int)(k % kPStages);
             if (!mbar_wait(&full[s], (uint32_t)((k / kPStages) & 1))) {   // never in a correct run
-                atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
             const long long tile = tile_of[s];
@@ -208,19 +208,16 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                     // every other tile's P and the write of carry_out, so
                     // carry_in may alias carry_out
                     const U c = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
-                    Desc<U, Tr::DW>::store(desc, 0, kFlagP, c + agg);
+                    Desc<U, Tr::DW>::store(desc, 0, kFlagP, c + agg, epoch);
                     excl_of[s] = c;   // for the look-back warp
                 } else {
-                    Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg);
+                    Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg, epoch);
                 }
                 agg_of[s] = agg;
                 mbar_arrive(&agg_done[s]);
             }
         }
-        return;
-    }
-
-    if (warp == kPCW + 2) {
+    } else if (warp == kPCW + 2) {
         // ---------------- look-back warp ----------------
         // Runs ahead of the compute warps: once a tile's A is out it looks
         // back, publishes P and leaves the exclusive prefix in excl_of[s]
@@ -228,7 +225,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         for (long long k = 0;; ++k) {
             const int s = (int)(k % kPStages);
             if (!mbar_wait(&agg_done[s], (uint32_t)((k / kPStages) & 1))) {   // never in a correct run
-                atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
             const long long tile = tile_of[s];
@@ -239,8 +236,8 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             if (tile == 0) {
                 excl = excl_of[s];   // the carry the aggregator read
             } else {
-                excl = look_back<U, Tr::DW, kLookbackK>(desc, tile, a.max_polls, &hdr->status);
-                if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg);
+                excl = look_back<U, Tr::DW, kLookbackK>(desc, tile, epoch, a.max_polls, &hdr->status);
+                if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg, epoch);
             }
             if (lane == 0) {
                 if (a.carry_out && tile == num_tiles - 1) *reinterpret_cast<U *>(a.carry_out) = excl + agg;
@@ -248,14 +245,12 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 mbar_arrive(&prefix_ready[s]);
             }
         }
-        return;
-    }
-
+    } else {
     // ---------------- compute warps ----------------
     for (long long k = 0;; ++k) {
         const int s = (int)(k % kPStages);
         if (!mbar_wait(&full[s], (uint32_t)((k / kPStages) & 1))) {   // never in a correct run
-            atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+            report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
             break;
         }
         const long long tile = tile_of[s];
@@ -323,7 +318,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
 
         // the look-back warp provides the tile's exclusive prefix
         if (!mbar_wait(&prefix_ready[s], (uint32_t)((k / kPStages) & 1)))   // never in a correct run
-            atomicMax(&hdr->status, (unsigned int)PS_ERR_LOOKBACK_TIMEOUT);
+            report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
         const U tile_excl = excl_of[s];
 
         // a9
@@ -358,6 +353,10 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
+    }
+
+    // every warp of the CTA is done: the last CTA readies the workspace
+    finish_call(hdr, a.ws, a.ws_bytes, epoch);
 }
 
 template <typename T, bool EXCL>

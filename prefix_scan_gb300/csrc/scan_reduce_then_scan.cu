@@ -99,11 +99,12 @@ cudaError_t launch_reduce_then_scan(const void *in, void *out, unsigned long lon
     using U = typename Traits<T>::U;
     constexpr int ITEMS = rts_dtype<T>() == PS_INT64 ? kItems64 : kItems32;
     const size_t tiles = num_tiles(rts_dtype<T>(), n);
-    U *partials = reinterpret_cast<U *>(ws + kHeaderBytes);
+    // the partials have a region of their own: the header and the
+    // descriptors of the single-pass scans are left as they are
+    U *partials = reinterpret_cast<U *>(ws + partials_offset(rts_dtype<T>(), n));
     const T *tin = reinterpret_cast<const T *>(in);
     const bool vec_io = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
-    cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderBytes, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     if (vec_io)
         tile_reduce_kernel<T, kThreads, ITEMS, true><<<(unsigned int)tiles, kThreads, 0, s>>>(tin, n, partials);
     else
@@ -111,7 +112,7 @@ cudaError_t launch_reduce_then_scan(const void *in, void *out, unsigned long lon
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     partials_scan_kernel<U><<<1, 1024, 0, s>>>(partials, tiles);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    PassArgs a{in, out, n, ws, nullptr, nullptr, 0};
+    PassArgs a{in, out, n, reinterpret_cast<unsigned char *>(partials), nullptr, nullptr, 0, 0};
     return launch_seeded_tile_scan<T>(a, exclusive, s);
 }
 

@@ -24,8 +24,9 @@
 //   a8  warp 0 publishes the inclusive prefix (P);
 //   a9  every thread adds tile prefix + warp offset + row/lane offset and
 //       stores its elements with 16-byte streaming stores.
-// Steps 1-6 of section 4.1 of the paper summary map to a0 (host memset of
-// the descriptors), a1..a5, a6, a7, a8 and a9.
+// Steps 1-6 of section 4.1 of the paper summary map to a0 (descriptors of
+// earlier calls carry another epoch and read as X; see begin_call and
+// finish_call), a1..a5, a6, a7, a8 and a9.
 #include "scan_device.cuh"
 
 namespace ps {
@@ -58,9 +59,11 @@ single_pass_kernel(PassArgs a) {
 
     // a1: dynamic tile id
     long long tile;
+    uint32_t epoch = 0;
     if (LB == Lookback::Precomputed) {
         tile = blockIdx.x;
     } else {
+        if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA
         if (tid == 0) s_tile = (long long)atomicAdd(&hdr->tile_counter, 1ull);
         __syncthreads();
         tile = s_tile;
@@ -134,7 +137,8 @@ single_pass_kernel(PassArgs a) {
 
     // a6..a8: publish, look back, publish
     if (LB == Lookback::Precomputed) {
-        if (tid == 0) s_excl = reinterpret_cast<const U *>(desc)[tile];
+        // a.ws points at the reduce-then-scan partials for this kernel
+        if (tid == 0) s_excl = reinterpret_cast<const U *>(a.ws)[tile];
     } else if (warp == 0) {
         U excl;
         if (tile == 0) {
@@ -144,13 +148,13 @@ single_pass_kernel(PassArgs a) {
             U c = U(0);
             if (lane == 0 && a.carry_in) c = *reinterpret_cast<const U *>(a.carry_in);
             excl = __shfl_sync(kFull, c, 0);
-            if (lane == 0) Desc<U, Tr::DW>::store(desc, 0, kFlagP, excl + agg);
+            if (lane == 0) Desc<U, Tr::DW>::store(desc, 0, kFlagP, excl + agg, epoch);
         } else {
-            if (LB == Lookback::Decoupled && lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg);
+            if (LB == Lookback::Decoupled && lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg, epoch);
             excl = (LB == Lookback::Chained)
-                       ? chained_wait<U, Tr::DW>(desc, tile, a.max_polls, &hdr->status)
-                       : look_back<U, Tr::DW, kLookbackK>(desc, tile, a.max_polls, &hdr->status);
-            if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg);
+                       ? chained_wait<U, Tr::DW>(desc, tile, epoch, a.max_polls, &hdr->status)
+                       : look_back<U, Tr::DW, kLookbackK>(desc, tile, epoch, a.max_polls, &hdr->status);
+            if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg, epoch);
         }
         if (lane == 0) {
             s_excl = excl;
@@ -186,6 +190,7 @@ single_pass_kernel(PassArgs a) {
                 if (i < n) out[i] = (T)v[r][k];
             }
     }
+    if (LB != Lookback::Precomputed) finish_call(hdr, a.ws, a.ws_bytes, epoch);
 }
 
 template <typename T> struct ItemsOf { static constexpr int value = kItems32; };
@@ -214,9 +219,8 @@ template <typename T>
 cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s) {
     constexpr ps_dtype dt = dtype_of<T>();
     const size_t tiles = num_tiles(dt, a.n);
-    // a0: every descriptor to X, tile counter and status to zero
-    cudaError_t e = cudaMemsetAsync(a.ws, 0, kHeaderBytes + tiles * desc_bytes(dt), s);
-    if (e != cudaSuccess) return e;
+    // a0 needs no work here: descriptors of earlier calls carry another
+    // epoch and read as X, and the previous call left the counter at 0
     const bool vec_io = ((reinterpret_cast<uintptr_t>(a.in) | reinterpret_cast<uintptr_t>(a.out)) & 15u) == 0;
     if (lb == Lookback::Decoupled) {
         if (vec_io) return launch_persistent<T>(a, exclusive, s);
@@ -246,25 +250,27 @@ template cudaError_t launch_single_pass<float>(const PassArgs &, bool, Lookback,
 
 // ---- test hook: the look-back alone -----------------------------------------
 template <typename T>
-__global__ void lookback_probe_kernel(const void *desc, long long tile, uint32_t max_polls,
-                                      void *result, unsigned int *status) {
+__global__ void lookback_probe_kernel(const void *desc, long long tile, uint32_t epoch,
+                                      uint32_t max_polls, void *result,
+                                      unsigned long long *status) {
     using U = typename Traits<T>::U;
-    const U excl = look_back<U, Traits<T>::DW, kLookbackK>(desc, tile, max_polls, status);
+    const U excl = look_back<U, Traits<T>::DW, kLookbackK>(desc, tile, epoch, max_polls, status);
     if (threadIdx.x == 0) *reinterpret_cast<U *>(result) = excl;
 }
 
 template <typename T>
-cudaError_t launch_lookback_probe(const void *desc, long long tile, uint32_t max_polls,
-                                  void *result, unsigned int *status, cudaStream_t s) {
-    lookback_probe_kernel<T><<<1, 32, 0, s>>>(desc, tile, max_polls, result, status);
+cudaError_t launch_lookback_probe(const void *desc, long long tile, uint32_t epoch,
+                                  uint32_t max_polls, void *result, unsigned long long *status,
+                                  cudaStream_t s) {
+    lookback_probe_kernel<T><<<1, 32, 0, s>>>(desc, tile, epoch, max_polls, result, status);
     return cudaGetLastError();
 }
 
-template cudaError_t launch_lookback_probe<int32_t>(const void *, long long, uint32_t, void *,
-                                                    unsigned int *, cudaStream_t);
-template cudaError_t launch_lookback_probe<int64_t>(const void *, long long, uint32_t, void *,
-                                                    unsigned int *, cudaStream_t);
-template cudaError_t launch_lookback_probe<float>(const void *, long long, uint32_t, void *,
-                                                  unsigned int *, cudaStream_t);
+template cudaError_t launch_lookback_probe<int32_t>(const void *, long long, uint32_t, uint32_t,
+                                                    void *, unsigned long long *, cudaStream_t);
+template cudaError_t launch_lookback_probe<int64_t>(const void *, long long, uint32_t, uint32_t,
+                                                    void *, unsigned long long *, cudaStream_t);
+template cudaError_t launch_lookback_probe<float>(const void *, long long, uint32_t, uint32_t,
+                                                  void *, unsigned long long *, cudaStream_t);
 
 }  // namespace ps

@@ -53,7 +53,7 @@ def test_workspace_size(lib):
         for n in (1, T, T + 1, 1 << 30):
             tiles = -(-n // T)
             need = lib.ps_scan_workspace_size(code, n)
-            assert need >= 256 + tiles * db and need % 256 == 0
+            assert need >= 256 + tiles * db + tiles * 8 and need % 256 == 0
     assert lib.ps_scan_workspace_size(7, 100) == 0
 
 
@@ -123,25 +123,27 @@ def test_seeded_argument_errors(lib, no_device):
 
 def test_status_strings(lib):
     for code, name in [(0, b"PS_OK"), (1, b"PS_ERR_INVALID_ARG"), (2, b"PS_ERR_WORKSPACE_TOO_SMALL"),
-                       (3, b"PS_ERR_OVERLAP"), (4, b"PS_ERR_CUDA"), (5, b"PS_ERR_LOOKBACK_TIMEOUT")]:
+                       (3, b"PS_ERR_OVERLAP"), (4, b"PS_ERR_CUDA"), (5, b"PS_ERR_LOOKBACK_TIMEOUT"),
+                       (6, b"PS_ERR_WORKSPACE_NOT_INITIALIZED")]:
         assert lib.ps_status_string(code) == name
 
 
 def test_descriptor_encoding(lib):
-    # flag in the high half of each 64-bit word, value bits in the low half
+    # each 64-bit word: epoch in bits 34..63, flag in bits 32..33, value bits below
     import numpy as np
     buf = (ctypes.c_char * 16)()
     v32 = np.array([-7], dtype=np.int32)
-    assert lib.ps_testing_encode_descriptor(0, 2, v32.ctypes.data, buf) == 0
-    w = np.frombuffer(bytes(buf)[:8], dtype=np.uint64)[0]
-    assert int(w) >> 32 == 2 and int(w) & 0xFFFFFFFF == (-7) & 0xFFFFFFFF
+    assert lib.ps_testing_encode_descriptor(0, 2, 12345, v32.ctypes.data, buf) == 0
+    w = int(np.frombuffer(bytes(buf)[:8], dtype=np.uint64)[0])
+    assert w >> 34 == 12345 and (w >> 32) & 3 == 2 and w & 0xFFFFFFFF == (-7) & 0xFFFFFFFF
     v64 = np.array([-(1 << 40) - 3], dtype=np.int64)
-    assert lib.ps_testing_encode_descriptor(1, 1, v64.ctypes.data, buf) == 0
-    w0, w1 = np.frombuffer(bytes(buf), dtype=np.uint64)
+    assert lib.ps_testing_encode_descriptor(1, 1, (1 << 30) - 1, v64.ctypes.data, buf) == 0
+    w0, w1 = (int(x) for x in np.frombuffer(bytes(buf), dtype=np.uint64))
     u = int(v64.view(np.uint64)[0])
-    assert int(w0) >> 32 == 1 and int(w1) >> 32 == 1
-    assert (int(w0) & 0xFFFFFFFF) | ((int(w1) & 0xFFFFFFFF) << 32) == u
-    assert lib.ps_testing_encode_descriptor(0, 3, v32.ctypes.data, buf) == _lib.PS_ERR_INVALID_ARG
+    assert w0 >> 34 == w1 >> 34 == (1 << 30) - 1 and (w0 >> 32) & 3 == (w1 >> 32) & 3 == 1
+    assert (w0 & 0xFFFFFFFF) | ((w1 & 0xFFFFFFFF) << 32) == u
+    assert lib.ps_testing_encode_descriptor(0, 3, 0, v32.ctypes.data, buf) == _lib.PS_ERR_INVALID_ARG
+    assert lib.ps_testing_encode_descriptor(0, 1, 1 << 30, v32.ctypes.data, buf) == _lib.PS_ERR_INVALID_ARG
 
 
 def test_python_layer_refuses_cpu_tensors():

@@ -166,7 +166,7 @@ def test_repeated_runs_are_identical_for_integers():
 
 # ---- the look-back alone, on hand-made descriptors ---------------------------
 
-def _desc_array(dtype: str, entries):
+def _desc_array(dtype: str, entries, epoch: int = 0):
     import ctypes
     from prefix_scan_gb300 import _lib
     lib = _lib.load()
@@ -176,20 +176,21 @@ def _desc_array(dtype: str, entries):
     for k, (flag, val) in enumerate(entries):
         v = np.array([val], dtype=DTYPES[dtype][0])
         buf = (ctypes.c_char * db)()
-        assert lib.ps_testing_encode_descriptor(code, flag, v.ctypes.data, buf) == 0
+        assert lib.ps_testing_encode_descriptor(code, flag, epoch, v.ctypes.data, buf) == 0
         raw[k * db:(k + 1) * db] = bytes(buf)
     return torch.frombuffer(raw, dtype=torch.uint8).to(DEV), code
 
 
-def _lookback(dtype: str, entries, tile: int, max_polls: int = 1 << 20):
+def _lookback(dtype: str, entries, tile: int, max_polls: int = 1 << 20, epoch: int = 0,
+              written_epoch: int | None = None):
     from prefix_scan_gb300 import _lib
     lib = _lib.load()
-    desc, code = _desc_array(dtype, entries)
+    desc, code = _desc_array(dtype, entries, epoch if written_epoch is None else written_epoch)
     res = torch.zeros(1, dtype=DTYPES[dtype][1], device=DEV)
-    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int64, device=DEV)
     s = torch.cuda.current_stream().cuda_stream
     _lib.check("ps_testing_lookback",
-               lib.ps_testing_lookback(code, desc.data_ptr(), tile, max_polls, res.data_ptr(),
+               lib.ps_testing_lookback(code, desc.data_ptr(), tile, epoch, max_polls, res.data_ptr(),
                                        status.data_ptr(), s))
     torch.cuda.synchronize()
     return res.item(), status.item()
@@ -227,9 +228,20 @@ def test_lookback_slides_over_many_windows(dtype):
 
 def test_lookback_wait_runs_out_without_hanging():
     # a predecessor that never publishes: the bounded wait gives up, reports
-    # PS_ERR_LOOKBACK_TIMEOUT, and the kernel returns normally
+    # PS_ERR_LOOKBACK_TIMEOUT tagged with the call's epoch, and the kernel
+    # returns normally
     entries = [(2, 5), (1, 5), (0, 0), (1, 5)]
-    val, st = _lookback("int32", entries, 4, max_polls=200)
-    assert st == 5
+    val, st = _lookback("int32", entries, 4, max_polls=200, epoch=77)
+    assert st & 0xFF == 5 and st >> 8 == 77
     x = torch.arange(10, dtype=torch.int32, device=DEV)   # context still usable
     assert api.scan_inclusive(x)[-1].item() == 45
+
+
+def test_lookback_ignores_descriptors_of_other_calls():
+    # descriptors written by an earlier call (another epoch) read as "not
+    # published": the look-back waits on them like on X and gives up
+    entries = [(2, 5), (1, 5), (1, 5)]
+    val, st = _lookback("int32", entries, 3, max_polls=200, epoch=9, written_epoch=8)
+    assert st & 0xFF == 5 and st >> 8 == 9
+    val, st = _lookback("int64", entries, 3, epoch=9, written_epoch=9)
+    assert st == 0 and val == 15

@@ -1,0 +1,141 @@
+"""The workspace across calls: zero-filled once, never reset by a call.
+
+Descriptors carry the number (epoch) of the call that wrote them, and the
+last CTA of each call puts the tile counter back and advances the epoch.
+These tests drive one workspace through many calls of mixed lengths,
+dtypes and algorithms, a workspace that was never zero-filled, and the
+epoch wrap-around, always checking the results against the oracle.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import fp32_ok
+from prefix_scan_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from prefix_scan_gb300 import _lib, api  # noqa: E402
+
+DEV = torch.device("cuda:0")
+EPOCH_MASK = (1 << 30) - 1
+
+
+def epoch_of(ws) -> int:
+    e = ctypes.c_uint32(0)
+    _lib.check("ps_testing_workspace_epoch",
+               _lib.load().ps_testing_workspace_epoch(ws.data_ptr(), None, ctypes.byref(e)))
+    return e.value
+
+
+def set_epoch(ws, epoch: int) -> None:
+    _lib.check("ps_testing_set_workspace_epoch",
+               _lib.load().ps_testing_set_workspace_epoch(ws.data_ptr(), epoch, None))
+
+
+def check(y, x, exclusive):
+    if x.dtype == np.float32:
+        assert fp32_ok(y, x, exclusive).all()
+    else:
+        ref = oracle.exclusive(x) if exclusive else oracle.inclusive(x)
+        assert np.array_equal(y, ref)
+
+
+def test_one_workspace_many_calls_mixed():
+    big = 1 << 22
+    ws = api.alloc_workspace(torch.int32, big, DEV)   # largest need: int32, n = 2^22
+    assert epoch_of(ws) == 0
+    plan = [  # (dtype, n, exclusive, algo, inplace)
+        ("int32", big, False, "decoupled", False),
+        ("int32", 5000, True, "decoupled", False),       # shorter: stale descriptors beyond
+        ("int64", big // 2, False, "decoupled", True),   # another descriptor format
+        ("float32", 123_457, False, "decoupled", False),
+        ("int32", big, True, "reduce_then_scan", False),  # does not touch the descriptors
+        ("int32", big, False, "decoupled", False),        # long again, over stale slots
+        ("int64", 77_777, True, "chained", False),
+        ("int32", 3, False, "decoupled", True),
+        ("int32", big - 1, True, "decoupled", False),
+    ]
+    expected_epoch = 0
+    for k, (dt, n, excl, algo, inplace) in enumerate(plan):
+        x = (inputs.full_range_i32(n, 70 + k) if dt == "int32"
+             else inputs.hashes(n, 70 + k).view(np.int64) if dt == "int64"
+             else inputs.uniform_f32(n, 70 + k))
+        t = torch.from_numpy(x.copy()).to(DEV)
+        y = api.scan(t, exclusive=excl, algo=algo, inplace=inplace, workspace=ws)
+        check(y.cpu().numpy(), x, excl)
+        if algo != "reduce_then_scan":
+            expected_epoch += 1
+        assert epoch_of(ws) == expected_epoch, (k, dt, algo)
+        assert api.device_status(ws) == _lib.PS_OK
+
+
+def test_workspace_never_zero_filled_refuses_to_run():
+    n = 50_000
+    ws = torch.full((api.workspace_size(torch.int32, n),), 0xAB, dtype=torch.uint8, device=DEV)
+    x = torch.ones(n, dtype=torch.int32, device=DEV)
+    out = torch.full_like(x, -7)
+    api.scan_inclusive(x, out=out, workspace=ws)        # enqueued, does nothing on the device
+    assert api.device_status(ws) == _lib.PS_ERR_WORKSPACE_NOT_INITIALIZED
+    assert torch.all(out == -7)
+    _lib.check("ps_workspace_init", _lib.load().ps_workspace_init(ws.data_ptr(), ws.numel(), None))
+    api.scan_inclusive(x, out=out, workspace=ws)
+    assert api.device_status(ws) == _lib.PS_OK
+    assert torch.equal(out, torch.arange(1, n + 1, dtype=torch.int32, device=DEV))
+
+
+def _plant_stale_descriptors(ws, code: int, epoch: int, count: int) -> None:
+    """Write descriptors that claim P with a wrong value, tagged `epoch`, into
+    the first `count` slots (what a call 2^30 calls earlier could have left)."""
+    lib = _lib.load()
+    db = lib.ps_testing_descriptor_bytes(code)
+    raw = bytearray(db * count)
+    v = np.array([123456789], dtype=np.int64 if code == 1 else np.int32)
+    buf = (ctypes.c_char * db)()
+    assert lib.ps_testing_encode_descriptor(code, 2, epoch, v.ctypes.data, buf) == 0
+    for k in range(count):
+        raw[k * db:(k + 1) * db] = bytes(buf)
+    ws[256:256 + len(raw)].copy_(torch.frombuffer(raw, dtype=torch.uint8))
+
+
+@pytest.mark.parametrize("dtype", ["int32", "int64"])
+def test_epoch_wraparound_clears_stale_descriptors(dtype):
+    tdt = torch.int32 if dtype == "int32" else torch.int64
+    code = 0 if dtype == "int32" else 1
+    n = 200 * api.tile_elements(tdt) + 17
+    ws = api.alloc_workspace(tdt, n, DEV)
+    x0 = torch.ones(n, dtype=tdt, device=DEV)
+    api.scan_inclusive(x0, workspace=ws)                # the workspace is in use now
+    torch.cuda.synchronize()
+    # descriptors of epoch 0 that a look-back at epoch 0 would trust
+    _plant_stale_descriptors(ws, code, 0, 200)
+    set_epoch(ws, EPOCH_MASK)                           # the next call is the last before the wrap
+    small = torch.ones(10, dtype=tdt, device=DEV)
+    assert torch.equal(api.scan_inclusive(small, workspace=ws).cpu(), torch.arange(1, 11, dtype=tdt))
+    assert epoch_of(ws) == 0
+    # epoch 0 again: a wrong value planted above would now be read unless cleared
+    xs = (inputs.full_range_i32(n, 5) if dtype == "int32" else inputs.hashes(n, 5).view(np.int64))
+    y = api.scan_inclusive(torch.from_numpy(xs).to(DEV), workspace=ws).cpu().numpy()
+    assert np.array_equal(y, oracle.inclusive(xs))
+    assert epoch_of(ws) == 1 and api.device_status(ws) == _lib.PS_OK
+
+
+def test_stale_descriptors_of_other_epochs_are_ignored():
+    n = 64 * api.tile_elements(torch.int32)
+    ws = api.alloc_workspace(torch.int32, n, DEV)
+    for e in (1, 2, 3):
+        api.scan_inclusive(torch.ones(100, dtype=torch.int32, device=DEV), workspace=ws)
+    torch.cuda.synchronize()
+    assert epoch_of(ws) == 3
+    _plant_stale_descriptors(ws, 0, 2, 64)             # written "two calls ago"
+    x = inputs.full_range_i32(n, 6)
+    y = api.scan_inclusive(torch.from_numpy(x).to(DEV), workspace=ws).cpu().numpy()
+    assert np.array_equal(y, oracle.inclusive(x))
