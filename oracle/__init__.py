@@ -7,8 +7,10 @@ it never touches the CUDA library: the two share no code.
 The arithmetic lives in ``scan_oracle.c`` (a plain sequential running sum,
 written from the definition y[i] = x[0] + ... + x[i] on the cumsum page
 "CUDA-Operators-6-Cumsum", section 1, and the inclusive/exclusive conversion
-section of the RTX 4090 scan tutorial).  This module only compiles that file
-with gcc and marshals numpy arrays into it.
+section of the RTX 4090 scan tutorial; and a plain sequential stream
+compaction, the definition behind section 4.4 of the decoupled look-back
+paper summary).  This module only compiles that file with gcc and marshals
+numpy arrays into it.
 
 Every function here is pinned by ``tests/test_oracle_pins.py``; none is
 "parity unpinned".
@@ -63,6 +65,16 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         fn.restype = None
     lib.oracle_abs_prefix_f32.argtypes = [vp, sz, ctypes.c_int, vp]
     lib.oracle_abs_prefix_f32.restype = None
+    for name in ("oracle_select_b32", "oracle_select_b64", "oracle_partition_b32",
+                 "oracle_partition_b64"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, vp, sz, vp]
+        fn.restype = sz
+    lib.oracle_flags_i32.argtypes = [vp, sz, ctypes.c_int, ctypes.c_int32, vp]
+    lib.oracle_flags_i64.argtypes = [vp, sz, ctypes.c_int, ctypes.c_int64, vp]
+    lib.oracle_flags_f32.argtypes = [vp, sz, ctypes.c_int, ctypes.c_float, vp]
+    for fn in (lib.oracle_flags_i32, lib.oracle_flags_i64, lib.oracle_flags_f32):
+        fn.restype = None
     return lib
 
 
@@ -114,3 +126,43 @@ def abs_prefix(x: np.ndarray, exclusive_: bool, lib: ctypes.CDLL | None = None) 
     a = np.empty(x.shape[0], dtype=np.float64)
     lib.oracle_abs_prefix_f32(_ptr(x), x.shape[0], int(bool(exclusive_)), _ptr(a))
     return a
+
+
+# ---- stream compaction -------------------------------------------------------
+
+PREDICATES = {"nonzero": 0, "greater": 1, "less": 2}
+
+
+def flags(x: np.ndarray, op: str, threshold=0, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """uint8 flags of a value predicate: nonzero, greater (x > t), less (x < t)."""
+    lib = lib if lib is not None else load()
+    x = np.ascontiguousarray(x)
+    f = np.empty(x.shape[0], dtype=np.uint8)
+    fn = {np.dtype(np.int32): lib.oracle_flags_i32, np.dtype(np.int64): lib.oracle_flags_i64,
+          np.dtype(np.float32): lib.oracle_flags_f32}[x.dtype]
+    fn(_ptr(x), x.shape[0], PREDICATES[op], threshold, _ptr(f))
+    return f
+
+
+def _compact(x: np.ndarray, f: np.ndarray, partition: bool, lib) -> tuple[np.ndarray, int]:
+    lib = lib if lib is not None else load()
+    x = np.ascontiguousarray(x)
+    f = np.ascontiguousarray(f, dtype=np.uint8)
+    if f.shape != x.shape:
+        raise ValueError("oracle: flags and values differ in length")
+    out = np.zeros_like(x)
+    bits = x.dtype.itemsize * 8
+    name = f"oracle_{'partition' if partition else 'select'}_b{bits}"
+    k = int(getattr(lib, name)(_ptr(x), _ptr(f), x.shape[0], _ptr(out)))
+    return out, k
+
+
+def select(x: np.ndarray, f: np.ndarray, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """The elements of x whose flag is nonzero, in order."""
+    out, k = _compact(x, f, False, lib)
+    return out[:k]
+
+
+def partition(x: np.ndarray, f: np.ndarray, lib: ctypes.CDLL | None = None) -> tuple[np.ndarray, int]:
+    """Flagged elements first in order, the others from the back in reverse; (out, count)."""
+    return _compact(x, f, True, lib)

@@ -6,7 +6,8 @@
  * CPU-baseline leg do.  It shares no code, header, table or constant with
  * the CUDA library.
  *
- * What it computes is the plain definition of the scan and nothing else:
+ * What it computes is the plain definition of the scan (and, at the end of
+ * the file, of stream compaction) and nothing else:
  *
  *   inclusive  y[i] = x[0] + x[1] + ... + x[i]
  *       ("Prefix Sum" definition, page "CUDA-Operators-6-Cumsum", section 1;
@@ -130,4 +131,83 @@ void oracle_abs_prefix_f32(const float *x, size_t n, int exclusive, double *a)
             a[i] = sum;
         }
     }
+}
+
+/* ---- stream compaction ("select") and partition -------------------------
+ *
+ * Decoupled look-back paper summary, section 4.4 ("in-place compaction
+ * behaviour"): the output position of a kept element is the exclusive prefix
+ * sum of a 0/1 flag array.  The plain definition that this reaches is written
+ * out here directly: walk the input once and append every flagged element.
+ *
+ * select:    out = the elements whose flag is nonzero, in input order;
+ *            returns how many.
+ * partition: the flagged elements first, in input order, then the others
+ *            from the END of `out` backwards (the j-th unflagged element goes
+ *            to out[n-1-j]); returns how many were flagged.  Placing the
+ *            others from the back is the reading that a single pass can
+ *            realise: it needs no total count before writing.
+ * Elements are moved as raw 4- or 8-byte words, so int32/fp32 share the
+ * 32-bit functions and int64 uses the 64-bit ones.
+ */
+size_t oracle_select_b32(const uint32_t *x, const uint8_t *flags, size_t n, uint32_t *out)
+{
+    size_t k = 0;
+    for (size_t i = 0; i < n; ++i)
+        if (flags[i])
+            out[k++] = x[i];
+    return k;
+}
+
+size_t oracle_select_b64(const uint64_t *x, const uint8_t *flags, size_t n, uint64_t *out)
+{
+    size_t k = 0;
+    for (size_t i = 0; i < n; ++i)
+        if (flags[i])
+            out[k++] = x[i];
+    return k;
+}
+
+size_t oracle_partition_b32(const uint32_t *x, const uint8_t *flags, size_t n, uint32_t *out)
+{
+    size_t k = 0, r = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (flags[i])
+            out[k++] = x[i];
+        else
+            out[n - 1 - r++] = x[i];
+    }
+    return k;
+}
+
+size_t oracle_partition_b64(const uint64_t *x, const uint8_t *flags, size_t n, uint64_t *out)
+{
+    size_t k = 0, r = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (flags[i])
+            out[k++] = x[i];
+        else
+            out[n - 1 - r++] = x[i];
+    }
+    return k;
+}
+
+/* Flags from value predicates: op 0 = nonzero, 1 = greater than t,
+ * 2 = less than t (IEEE comparisons for fp32: NaN never passes). */
+void oracle_flags_i32(const int32_t *x, size_t n, int op, int32_t t, uint8_t *flags)
+{
+    for (size_t i = 0; i < n; ++i)
+        flags[i] = (uint8_t)(op == 0 ? x[i] != 0 : op == 1 ? x[i] > t : x[i] < t);
+}
+
+void oracle_flags_i64(const int64_t *x, size_t n, int op, int64_t t, uint8_t *flags)
+{
+    for (size_t i = 0; i < n; ++i)
+        flags[i] = (uint8_t)(op == 0 ? x[i] != 0 : op == 1 ? x[i] > t : x[i] < t);
+}
+
+void oracle_flags_f32(const float *x, size_t n, int op, float t, uint8_t *flags)
+{
+    for (size_t i = 0; i < n; ++i)
+        flags[i] = (uint8_t)(op == 0 ? x[i] != 0.0f : op == 1 ? x[i] > t : x[i] < t);
 }

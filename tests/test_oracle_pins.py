@@ -232,9 +232,76 @@ def pin_degenerate(lib):
     assert list(oracle.inclusive(x, lib)) == [1.0, np.inf, np.inf]
 
 
+# ---- stream compaction pins ---------------------------------------------------
+
+def _rand_flags(rng, n, p=0.5):
+    # nonzero flags of assorted values: only "nonzero" may matter
+    f = (rng.random(n) < p).astype(np.uint8)
+    return f * rng.integers(1, 256, n, dtype=np.uint8) if n else f
+
+
+def pin_select_brute_force(lib):
+    rng = np.random.default_rng(77)
+    for dt in (np.int32, np.int64, np.float32):
+        for n in range(0, 65):
+            x = rng.integers(-1000, 1000, n).astype(dt)
+            f = _rand_flags(rng, n)
+            want = [x[i] for i in range(n) if f[i] != 0]
+            assert list(oracle.select(x, f, lib)) == want, (dt, n)
+            out, k = oracle.partition(x, f, lib)
+            rejected = [x[i] for i in range(n) if f[i] == 0]
+            assert k == len(want) and list(out[:k]) == want
+            assert list(out[k:]) == rejected[::-1], (dt, n)
+
+
+def pin_select_library_crosscheck(lib):
+    rng = np.random.default_rng(78)
+    n = 500_003
+    for dt in (np.int32, np.int64, np.float32):
+        x = inputs.uniform_int(n, -10**6, 10**6, 79).astype(dt)
+        f = _rand_flags(rng, n, 0.3)
+        m = f != 0
+        assert np.array_equal(oracle.select(x, f, lib), x[m])
+        out, k = oracle.partition(x, f, lib)
+        assert k == int(m.sum())
+        assert np.array_equal(out, np.concatenate([x[m], x[~m][::-1]]))
+
+
+def pin_select_closed_forms(lib):
+    n = 100_001
+    x = np.arange(n, dtype=np.int64) * 3 - 7
+    assert np.array_equal(oracle.select(x, np.ones(n, np.uint8), lib), x)
+    assert oracle.select(x, np.zeros(n, np.uint8), lib).shape == (0,)
+    every3 = (np.arange(n) % 3 == 0).astype(np.uint8)
+    assert np.array_equal(oracle.select(x, every3, lib), x[::3])
+    out, k = oracle.partition(x, np.zeros(n, np.uint8), lib)
+    assert k == 0 and np.array_equal(out, x[::-1])
+    # the partition is a permutation of the input
+    f = (x % 7 == 1).astype(np.uint8)
+    out, k = oracle.partition(x, f, lib)
+    assert np.array_equal(np.sort(out), np.sort(x))
+    assert np.array_equal(oracle.select(x, f, lib), out[:k])
+
+
+def pin_flags_predicates(lib):
+    x = inputs.uniform_int(200_001, -50, 50, 80)
+    for dt in (np.int32, np.int64, np.float32):
+        xd = x.astype(dt)
+        assert np.array_equal(oracle.flags(xd, "nonzero", 0, lib), (xd != 0).astype(np.uint8))
+        assert np.array_equal(oracle.flags(xd, "greater", 7, lib), (xd > 7).astype(np.uint8))
+        assert np.array_equal(oracle.flags(xd, "less", -3, lib), (xd < -3).astype(np.uint8))
+    xf = np.array([np.nan, -0.0, 0.0, 1.5, -np.inf], dtype=np.float32)
+    assert list(oracle.flags(xf, "nonzero", 0, lib)) == [1, 0, 0, 1, 1]
+    assert list(oracle.flags(xf, "greater", 0.0, lib)) == [0, 0, 0, 1, 0]
+    assert list(oracle.flags(xf, "less", 0.0, lib)) == [0, 0, 0, 0, 1]
+    big = np.array([np.iinfo(np.int64).max, np.iinfo(np.int64).min], dtype=np.int64)
+    assert list(oracle.flags(big, "greater", 0, lib)) == [1, 0]
+
+
 PINS = [pin_worked_examples, pin_fig6_snapshot, pin_brute_force_int, pin_brute_force_f32,
         pin_abs_prefix, pin_closed_forms, pin_wraparound, pin_library_crosscheck,
-        pin_invariants, pin_degenerate]
+        pin_invariants, pin_degenerate, pin_select_brute_force, pin_select_library_crosscheck,
+        pin_select_closed_forms, pin_flags_predicates]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -260,11 +327,15 @@ MUTANTS = [
      "sum += xi;\n        y[i] = sum - xi;"),                                    # derived by subtraction
     ("oracle_abs_prefix_f32", "xi = -xi;", "xi = xi;"),                          # dropped abs
     ("oracle_abs_prefix_f32", "if (exclusive) {", "if (!exclusive) {"),          # swapped modes
+    ("oracle_select_b32", "if (flags[i])", "if (flags[i] & 1)"),                # low bit only
+    ("oracle_partition_b64", "out[n - 1 - r++] = x[i];", "out[k + r++] = x[i];"),  # rejected not from the back
+    ("oracle_flags_i32", "x[i] > t", "x[i] >= t"),                              # off-by-one predicate
+    ("oracle_flags_f32", "x[i] != 0.0f", "x[i] == x[i]"),                       # NaN test instead of nonzero
 ]
 
 
 def _function_span(src: str, name: str) -> tuple[int, int]:
-    m = re.search(r"\n(void " + re.escape(name) + r"\([^)]*\)\s*\{)", src)
+    m = re.search(r"\n((?:void|size_t) " + re.escape(name) + r"\([^)]*\)\s*\{)", src)
     assert m, name
     start = m.start(1)
     depth, k = 0, src.index("{", start)
