@@ -188,6 +188,46 @@ ps_status ps_scan_host(ps_dtype dtype, int exclusive, const void *h_in, void *h_
                        ps_stream_t stream);
 
 /*
+ * Stream compaction in one pass (decoupled look-back paper summary,
+ * section 4.4, "in-place compaction behaviour"): the output position of a
+ * kept element is the exclusive prefix sum of the 0/1 keep flags, computed
+ * by the same single-pass look-back and fused with the scatter.
+ *   op         PS_SELECT_FLAGGED  keep x[i] where flags[i] != 0
+ *              PS_SELECT_NONZERO  keep x[i] != 0
+ *              PS_SELECT_GREATER  keep x[i] >  *threshold
+ *              PS_SELECT_LESS     keep x[i] <  *threshold
+ *              (fp32 compares per IEEE: NaN is never kept by GREATER/LESS,
+ *              and is kept by NONZERO; -0.0 counts as zero)
+ *   in         device array of n elements of `dtype`
+ *   flags      device array of n bytes (PS_SELECT_FLAGGED only, else NULL)
+ *   threshold  HOST pointer to one element of `dtype` (GREATER / LESS only)
+ *   out        device array of n elements
+ *   num_selected  device uint64 receiving the number kept (may be NULL)
+ *   ws         workspace as for the scans: ps_scan_workspace_size(dtype, n)
+ * ps_select writes the kept elements, in order, to out[0 .. count); the rest
+ * of `out` is left untouched.  out == in compacts in place: safe in a single
+ * pass because a tile learns its output offset only after every earlier
+ * tile has loaded its input (needs in and flags 16-byte aligned, else
+ * PS_ERR_OVERLAP).  ps_partition writes the kept elements to the front in
+ * order and the others from the back in reverse order (the j-th rejected
+ * element goes to out[n-1-j]), so `out` holds a permutation of `in`; out
+ * must not overlap in.  n must be below 2^32.  Other conventions as for the
+ * scans.
+ */
+typedef enum ps_select_op {
+    PS_SELECT_FLAGGED = 0,
+    PS_SELECT_NONZERO = 1,
+    PS_SELECT_GREATER = 2,
+    PS_SELECT_LESS = 3
+} ps_select_op;
+ps_status ps_select(ps_dtype dtype, ps_select_op op, const void *in, const uint8_t *flags,
+                    const void *threshold, void *out, uint64_t *num_selected, size_t n, void *ws,
+                    size_t ws_bytes, ps_stream_t stream);
+ps_status ps_partition(ps_dtype dtype, ps_select_op op, const void *in, const uint8_t *flags,
+                       const void *threshold, void *out, uint64_t *num_selected, size_t n,
+                       void *ws, size_t ws_bytes, ps_stream_t stream);
+
+/*
  * Waits for `stream`, then reads into *out the device-side status of the
  * last scan that used `ws`: PS_OK, PS_ERR_LOOKBACK_TIMEOUT, or
  * PS_ERR_WORKSPACE_NOT_INITIALIZED (the workspace was never zero-filled).

@@ -134,6 +134,59 @@ def scan_seeded(x: torch.Tensor, carry_in: torch.Tensor | None = None,
     return out
 
 
+SELECT_OPS = {"flagged": 0, "nonzero": 1, "greater": 2, "less": 3}
+
+
+def _compact(partition: bool, x: torch.Tensor, flags, op, threshold, out, inplace, workspace, stream):
+    if not x.is_cuda or x.dim() != 1 or not x.is_contiguous():
+        raise ValueError("select: input must be a contiguous 1-D CUDA tensor")
+    code = dtype_code(x.dtype)
+    n = x.numel()
+    op = op or ("flagged" if flags is not None else "nonzero")
+    if op == "flagged":
+        if flags is None or flags.dtype != torch.uint8 or flags.numel() != n or not flags.is_cuda:
+            raise ValueError("select: `flags` must be a uint8 CUDA tensor of the input's length")
+    if inplace:
+        out = x
+    elif out is None:
+        out = torch.empty_like(x)
+    count = torch.zeros(1, dtype=torch.int64, device=x.device)
+    lib = _lib.load()
+    need = int(lib.ps_scan_workspace_size(code, n))
+    if workspace is None:
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=x.device)
+    thr = None
+    if threshold is not None:
+        import numpy as np
+        thr = np.array([threshold], dtype={torch.int32: np.int32, torch.int64: np.int64,
+                                           torch.float32: np.float32}[x.dtype])
+    fn = lib.ps_partition if partition else lib.ps_select
+    st = fn(code, SELECT_OPS[op], x.data_ptr() if n else None,
+            flags.data_ptr() if (flags is not None and n) else None,
+            thr.ctypes.data if thr is not None else None, out.data_ptr() if n else None,
+            count.data_ptr(), n, workspace.data_ptr(), workspace.numel(), _stream_handle(stream, x.device))
+    _lib.check("ps_partition" if partition else "ps_select", st)
+    return out, count
+
+
+def select(x: torch.Tensor, flags: torch.Tensor | None = None, *, op: str | None = None,
+           threshold=None, out: torch.Tensor | None = None, inplace: bool = False,
+           workspace: torch.Tensor | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Single-pass stream compaction: (out, count) with the kept elements in
+    out[:count] in input order.  ``op``: "flagged" (flags != 0), "nonzero",
+    "greater"/"less" (than ``threshold``).  ``count`` is a one-element int64
+    CUDA tensor (no host synchronisation here)."""
+    return _compact(False, x, flags, op, threshold, out, inplace, workspace, stream)
+
+
+def partition(x: torch.Tensor, flags: torch.Tensor | None = None, *, op: str | None = None,
+              threshold=None, out: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Kept elements to out[:count] in order, the others to the back in
+    reverse order (out[n-1-j] = j-th rejected)."""
+    return _compact(True, x, flags, op, threshold, out, False, workspace, stream)
+
+
 def host_staging_size(dtype: torch.dtype, n: int) -> int:
     return int(_lib.load().ps_scan_host_staging_size(dtype_code(dtype), n))
 

@@ -90,6 +90,50 @@ ps_status dispatch(ps_algo algo, ps_dtype dt, int exclusive, const void *in, voi
 
 void ps::note_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
+namespace {
+
+ps_status compact(bool partition, ps_dtype dt, int op, const void *in, const uint8_t *flags,
+                  const void *threshold, void *out, uint64_t *num_selected, size_t n, void *ws,
+                  size_t ws_bytes, cudaStream_t s) {
+    if (!valid_dtype(dt) || op < PS_SELECT_FLAGGED || op > PS_SELECT_LESS) return PS_ERR_INVALID_ARG;
+    const size_t es = ps::elem_bytes(dt);
+    if (reinterpret_cast<uintptr_t>(num_selected) % 8 != 0) return PS_ERR_INVALID_ARG;
+    if (n == 0) {
+        if (num_selected == nullptr) return PS_OK;
+        const cudaError_t e = cudaMemsetAsync(num_selected, 0, sizeof(uint64_t), s);
+        return e == cudaSuccess ? PS_OK : cuda_fail(e);
+    }
+    if (n > 0xffffffffull) return PS_ERR_INVALID_ARG;   // 32-bit counts
+    if (op == PS_SELECT_FLAGGED && flags == nullptr) return PS_ERR_INVALID_ARG;
+    if ((op == PS_SELECT_GREATER || op == PS_SELECT_LESS) && threshold == nullptr) return PS_ERR_INVALID_ARG;
+    const ps_status st = check_args(dt, in, out, n, ws, ws_bytes);
+    if (st != PS_OK) return st;
+    const size_t bytes = n * es;
+    const bool bulk = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(flags)) & 15u) == 0;
+    if (in == out && (partition || !bulk)) return PS_ERR_OVERLAP;   // see ps_select / ps_partition
+    if (op == PS_SELECT_FLAGGED && (ranges_overlap(flags, n, out, bytes) ||
+                                    ranges_overlap(flags, n, ws, ps::workspace_bytes(dt, n))))
+        return PS_ERR_OVERLAP;
+    if (num_selected && (ranges_overlap(num_selected, 8, out, bytes) || ranges_overlap(num_selected, 8, in, bytes) ||
+                         ranges_overlap(num_selected, 8, ws, ps::workspace_bytes(dt, n))))
+        return PS_ERR_OVERLAP;
+    unsigned long long tb = 0;
+    if (threshold) std::memcpy(&tb, threshold, es);
+    ps::SelectArgs a{in, op == PS_SELECT_FLAGGED ? flags : nullptr, out, (unsigned long long)n,
+                     static_cast<unsigned char *>(ws), (unsigned long long)(ws_bytes & ~(size_t)7),
+                     reinterpret_cast<unsigned long long *>(num_selected), tb, ps::kDefaultMaxPolls,
+                     bulk ? 1 : 0};
+    cudaError_t e;
+    switch (dt) {
+    case PS_INT32: e = ps::launch_select<int32_t>(a, op, partition, s); break;
+    case PS_INT64: e = ps::launch_select<int64_t>(a, op, partition, s); break;
+    default: e = ps::launch_select<float>(a, op, partition, s); break;
+    }
+    return e == cudaSuccess ? PS_OK : cuda_fail(e);
+}
+
+}  // namespace
+
 ps_status ps::scan_seeded(ps_dtype dt, int exclusive, const void *in, void *out, size_t n,
                           const void *carry_in, void *carry_out, void *ws, size_t ws_bytes,
                           cudaStream_t s) {
@@ -155,6 +199,20 @@ ps_status ps_scan_seeded(ps_dtype dtype, int exclusive, const void *in, void *ou
                          ps_stream_t stream) {
     return ps::scan_seeded(dtype, exclusive, in, out, n, carry_in, carry_out, ws, ws_bytes,
                            (cudaStream_t)stream);
+}
+
+ps_status ps_select(ps_dtype dtype, ps_select_op op, const void *in, const uint8_t *flags,
+                    const void *threshold, void *out, uint64_t *num_selected, size_t n, void *ws,
+                    size_t ws_bytes, ps_stream_t stream) {
+    return compact(false, dtype, (int)op, in, flags, threshold, out, num_selected, n, ws, ws_bytes,
+                   (cudaStream_t)stream);
+}
+
+ps_status ps_partition(ps_dtype dtype, ps_select_op op, const void *in, const uint8_t *flags,
+                       const void *threshold, void *out, uint64_t *num_selected, size_t n, void *ws,
+                       size_t ws_bytes, ps_stream_t stream) {
+    return compact(true, dtype, (int)op, in, flags, threshold, out, num_selected, n, ws, ws_bytes,
+                   (cudaStream_t)stream);
 }
 
 ps_status ps_workspace_init(void *ws, size_t ws_bytes, ps_stream_t stream) {

@@ -160,6 +160,25 @@ cudaError_t launch_lookback_probe(const void *desc, long long tile, uint32_t epo
                                   uint32_t max_polls, void *result, unsigned long long *status,
                                   cudaStream_t s);
 
+// Launch arguments of the compaction kernels (select / partition).
+struct SelectArgs {
+    const void *in;
+    const uint8_t *flags;
+    void *out;
+    unsigned long long n;
+    unsigned char *ws;
+    unsigned long long ws_bytes;
+    unsigned long long *num_selected;   // device, may be null
+    unsigned long long threshold_bits;  // the threshold's bits (greater / less)
+    uint32_t max_polls;
+    int use_bulk;                       // values (and flags) 16-byte aligned
+};
+
+// Enqueue a single-pass select or partition; op: 0 flag array, 1 nonzero,
+// 2 greater than the threshold, 3 less than the threshold.
+template <typename T>
+cudaError_t launch_select(const SelectArgs &a, int op, bool partition, cudaStream_t s);
+
 // Records `e` as the calling thread's last CUDA error (ps_last_cuda_error).
 void note_cuda_error(cudaError_t e);
 

@@ -1,0 +1,349 @@
+// scan_select.cu -- single-pass stream compaction: select and partition.
+//
+// The output position of a kept element is the exclusive prefix sum of the
+// 0/1 selection flags (decoupled look-back paper summary, section 4.4,
+// "in-place compaction behaviour"), so compaction is the single-pass scan of
+// the flags with a scatter fused into its last step:
+//   select     out[count of selected before i] = x[i] for every selected i;
+//   partition  the same for selected elements, and every other element i
+//              goes to out[n - 1 - (i - count of selected before i)], i.e.
+//              the rejected ones fill the array from the back in reverse
+//              order -- a position known without the final count.
+// Selection is a flag array (nonzero = keep) or a predicate on the value
+// (nonzero, greater than a threshold, less than a threshold).
+//
+// Same structure as the persistent scan kernel (scan_persistent.cu): a
+// producer warp takes tile ids and bulk-copies values (and flags) into a
+// shared-memory ring, an aggregator warp counts each tile's selected
+// elements and publishes the count at once, a look-back warp resolves the
+// tile's offset, and the compute warps scan the flags in registers and
+// scatter.  Counts are 32-bit (n < 2^32).
+//
+// In place (out == in, select only) is safe because a tile learns its
+// offset only after every predecessor has published its count, which each
+// does after its data sits in shared memory: nothing is overwritten that a
+// predecessor still has to read, and a tile never writes past its own end.
+// That argument needs the bulk copies, so in place requires 16-byte
+// aligned values and flags.
+#include "scan_device.cuh"
+#include "scan_pipeline.cuh"
+
+namespace ps {
+
+namespace {
+
+constexpr int kSCW = kThreads / 32;   // compute warps per CTA
+
+template <typename T> struct SelItems { static constexpr int value = kItems32; };
+template <> struct SelItems<int64_t> { static constexpr int value = kItems64; };
+
+template <typename T> constexpr long long sel_tile() { return (long long)kThreads * SelItems<T>::value; }
+template <int OP> constexpr int sel_stages() { return OP == 0 ? 2 : kPStages; }
+template <typename T, int OP> constexpr size_t sel_stage_bytes() {
+    return (size_t)sel_tile<T>() * sizeof(T) + (OP == 0 ? (size_t)sel_tile<T>() : 0);
+}
+template <typename T, int OP> constexpr size_t sel_smem_bytes() {
+    return (size_t)sel_stages<OP>() * sel_stage_bytes<T, OP>() +
+           ((size_t)sel_stages<OP>() * (4 * 8 + 8 + 4 + 4) + 127) / 128 * 128;
+}
+
+// Raw bits of the element type, for comparisons in the element's own type.
+template <typename T> __device__ __forceinline__ T from_raw(unsigned long long b);
+template <> __device__ __forceinline__ int32_t from_raw<int32_t>(unsigned long long b) { return (int32_t)(uint32_t)b; }
+template <> __device__ __forceinline__ int64_t from_raw<int64_t>(unsigned long long b) { return (int64_t)b; }
+template <> __device__ __forceinline__ float from_raw<float>(unsigned long long b) { return __uint_as_float((uint32_t)b); }
+
+// OP: 0 flag array, 1 nonzero, 2 greater than t, 3 less than t
+template <typename T, int OP>
+__device__ __forceinline__ bool keep(T x, uint8_t f, T t) {
+    if (OP == 0) return f != 0;
+    if (OP == 1) return x != T(0);
+    if (OP == 2) return x > t;
+    return x < t;
+}
+
+template <typename T> __device__ __forceinline__ T vget_t(const typename Traits<T>::V &v, int j);
+template <> __device__ __forceinline__ int32_t vget_t<int32_t>(const uint4 &v, int j) { return (int32_t)vget(v, j); }
+template <> __device__ __forceinline__ float vget_t<float>(const float4 &v, int j) { return vget(v, j); }
+template <> __device__ __forceinline__ int64_t vget_t<int64_t>(const ulonglong2 &v, int j) { return (int64_t)vget(v, j); }
+
+}  // namespace
+
+
+template <typename T, int OP, bool PARTITION>
+__global__ void __launch_bounds__((kSCW + 3) * 32, kPCtasPerSm)
+select_kernel(SelectArgs a, long long num_tiles) {
+    using V = typename Traits<T>::V;
+    using U = uint32_t;                     // counts
+    constexpr int VEC = Traits<T>::VEC;
+    constexpr int ITEMS = SelItems<T>::value;
+    constexpr int ROWS = ITEMS / VEC;
+    constexpr long long TILE = sel_tile<T>();
+    constexpr int S = sel_stages<OP>();
+    constexpr uint32_t VAL_BYTES = (uint32_t)(TILE * sizeof(T));
+    constexpr uint32_t FLAG_BYTES = OP == 0 ? (uint32_t)TILE : 0u;
+    constexpr int CT = kSCW * 32;
+    static_assert(ITEMS % VEC == 0, "ITEMS must be a multiple of the vector width");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    T *vals = reinterpret_cast<T *>(smem);
+    uint8_t *flg = smem + (size_t)S * VAL_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * (VAL_BYTES + FLAG_BYTES));
+    uint64_t *empty = full + S;
+    uint64_t *agg_done = empty + S;
+    uint64_t *prefix_ready = agg_done + S;
+    long long *tile_of = reinterpret_cast<long long *>(prefix_ready + S);
+    U *agg_of = reinterpret_cast<U *>(tile_of + S);
+    U *excl_of = agg_of + S;
+    __shared__ U s_warp[2][kSCW];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    Header *hdr = reinterpret_cast<Header *>(a.ws);
+    void *desc = a.ws + kHeaderBytes;
+    const unsigned long long n = a.n;
+    const T *in = reinterpret_cast<const T *>(a.in);
+    T *out = reinterpret_cast<T *>(a.out);
+    const T thr = from_raw<T>(a.threshold_bits);
+
+    uint32_t epoch;
+    if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kSCW + 1);
+            mbar_init(&agg_done[s], 1);
+            mbar_init(&prefix_ready[s], 1);
+            tile_of[s] = num_tiles;
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kSCW) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            for (long long k = 0;; ++k) {
+                const int s = (int)(k % S);
+                if (k >= S && !mbar_wait(&empty[s], (uint32_t)((k / S - 1) & 1))) {
+                    report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                    break;
+                }
+                const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
+                tile_of[s] = t;
+                if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
+                    mbar_arrive_expect_tx(&full[s], VAL_BYTES + FLAG_BYTES);
+                    bulk_load(vals + (size_t)s * TILE, in + t * TILE, VAL_BYTES, &full[s]);
+                    if (OP == 0) bulk_load(flg + (size_t)s * TILE, a.flags + t * TILE, FLAG_BYTES, &full[s]);
+                } else {
+                    mbar_arrive(&full[s]);   // end marker, or a tile read from global
+                }
+                if (t >= num_tiles) break;
+            }
+        }
+    } else if (warp == kSCW + 1) {
+        // ---------------- aggregator: count and publish ----------------
+        for (long long k = 0;; ++k) {
+            const int s = (int)(k % S);
+            if (!mbar_wait(&full[s], (uint32_t)((k / S) & 1))) {
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                break;
+            }
+            const long long tile = tile_of[s];
+            if (tile < 0 || tile >= num_tiles) {
+                if (lane == 0) mbar_arrive(&agg_done[s]);
+                break;
+            }
+            const unsigned long long base = (unsigned long long)tile * TILE;
+            U cnt = 0;
+            if (a.use_bulk && base + TILE <= n) {
+                if (OP == 0) {
+                    const uint4 *f4 = reinterpret_cast<const uint4 *>(flg + (size_t)s * TILE);
+                    for (int i = lane; i < (int)(TILE / 16); i += 32) {
+                        const uint4 w = f4[i];
+                        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) cnt += ((ws4[q] >> (8 * b)) & 0xffu) != 0u;
+                    }
+                } else {
+                    const V *src = reinterpret_cast<const V *>(vals + (size_t)s * TILE);
+                    for (int i = lane; i < (int)(TILE / VEC); i += 32) {
+                        const V x = src[i];
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) cnt += keep<T, OP>(vget_t<T>(x, j), 0, thr);
+                    }
+                }
+            } else {
+                const unsigned long long end = base + TILE < n ? base + TILE : n;
+                for (unsigned long long i = base + lane; i < end; i += 32)
+                    cnt += keep<T, OP>(OP == 0 ? T(0) : in[i], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            const U agg = __reduce_add_sync(kFull, cnt);
+            if (lane == 0) {
+                Desc<U, 1>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
+                agg_of[s] = agg;
+                mbar_arrive(&agg_done[s]);
+            }
+        }
+    } else if (warp == kSCW + 2) {
+        // ---------------- look-back: the tile's output offset ----------------
+        for (long long k = 0;; ++k) {
+            const int s = (int)(k % S);
+            if (!mbar_wait(&agg_done[s], (uint32_t)((k / S) & 1))) {
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                break;
+            }
+            const long long tile = tile_of[s];
+            if (tile < 0 || tile >= num_tiles) break;
+            const U agg = agg_of[s];
+            __syncwarp();
+            U excl = 0;
+            if (tile != 0) {
+                excl = look_back<U, 1, kLookbackK>(desc, tile, epoch, a.max_polls, &hdr->status);
+                if (lane == 0) Desc<U, 1>::store(desc, tile, kFlagP, excl + agg, epoch);
+            }
+            if (lane == 0) {
+                if (a.num_selected && tile == num_tiles - 1) *a.num_selected = (unsigned long long)(excl + agg);
+                excl_of[s] = excl;
+                mbar_arrive(&prefix_ready[s]);
+            }
+        }
+    } else {
+        // ---------------- compute warps: scan the flags, scatter ----------------
+        for (long long k = 0;; ++k) {
+            const int s = (int)(k % S);
+            if (!mbar_wait(&full[s], (uint32_t)((k / S) & 1))) {
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                break;
+            }
+            const long long tile = tile_of[s];
+            if (tile < 0 || tile >= num_tiles) break;
+            const unsigned long long base = (unsigned long long)tile * TILE;
+            const bool staged = a.use_bulk && base + TILE <= n;
+            const int seg = warp * 32 * ITEMS;
+
+            T v[ROWS][VEC];
+            uint32_t sel[ROWS];   // bit j: element j of this lane's row chunk is kept
+            if (staged) {
+                const V *src = reinterpret_cast<const V *>(vals + (size_t)s * TILE + seg) + lane;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const V x = src[r * 32];
+                    uint32_t fb = 0;
+                    if (OP == 0) {
+                        const uint8_t *fp = flg + (size_t)s * TILE + seg + (r * 32 + lane) * VEC;
+                        fb = VEC == 4 ? *reinterpret_cast<const uint32_t *>(fp)
+                                      : (uint32_t)*reinterpret_cast<const uint16_t *>(fp);
+                    }
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        v[r][j] = vget_t<T>(x, j);
+                        m |= (uint32_t)keep<T, OP>(v[r][j], (uint8_t)(fb >> (8 * j)), thr) << j;
+                    }
+                    sel[r] = m;
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const unsigned long long i = base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
+                        v[r][j] = i < n ? in[i] : T(0);
+                        const bool kp = i < n && keep<T, OP>(v[r][j], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
+                        m |= (uint32_t)kp << j;
+                    }
+                    sel[r] = m;
+                }
+            }
+
+            // exclusive count of kept elements before each lane's row chunk
+            U off[ROWS];
+            U running = 0;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const U t = (U)__popc(sel[r]);
+                const U sc = warp_inclusive<U>(t, lane);
+                off[r] = running + (sc - t);
+                running += __shfl_sync(kFull, sc, 31);
+            }
+            U *sw = s_warp[k & 1];
+            if (lane == 0) sw[warp] = running;
+            named_barrier(1, CT);
+            U warp_excl = 0;
+#pragma unroll
+            for (int w = 0; w < kSCW; ++w)
+                if (w < warp) warp_excl += sw[w];
+            if (!mbar_wait(&prefix_ready[s], (uint32_t)((k / S) & 1)))
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+            const U tile_excl = excl_of[s];
+
+            // scatter
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const U before = tile_excl + warp_excl + off[r];
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const unsigned long long i = base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
+                    const U sel_before = before + (U)__popc(sel[r] & ((1u << j) - 1u));
+                    if ((sel[r] >> j) & 1u) {
+                        out[sel_before] = v[r][j];
+                    } else if (PARTITION && i < n) {
+                        out[n - 1 - (i - sel_before)] = v[r][j];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+    }
+
+    finish_call(hdr, a.ws, a.ws_bytes, epoch);
+}
+
+template <typename T, int OP, bool PARTITION>
+static cudaError_t launch_select_variant(const SelectArgs &a, cudaStream_t s) {
+    constexpr size_t smem = sel_smem_bytes<T, OP>();
+    const long long tiles = (long long)((a.n + sel_tile<T>() - 1) / sel_tile<T>());
+    static volatile int configured[64] = {};
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(select_kernel<T, OP, PARTITION>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = 1;
+    }
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    long long grid = (long long)sms * kPCtasPerSm;
+    if (grid > tiles) grid = tiles;
+    select_kernel<T, OP, PARTITION><<<(unsigned int)grid, (kSCW + 3) * 32, smem, s>>>(a, tiles);
+    return cudaGetLastError();
+}
+
+template <typename T, bool PARTITION>
+static cudaError_t launch_select_part(const SelectArgs &a, int op, cudaStream_t s) {
+    switch (op) {
+    case 0: return launch_select_variant<T, 0, PARTITION>(a, s);
+    case 1: return launch_select_variant<T, 1, PARTITION>(a, s);
+    case 2: return launch_select_variant<T, 2, PARTITION>(a, s);
+    default: return launch_select_variant<T, 3, PARTITION>(a, s);
+    }
+}
+
+template <typename T>
+cudaError_t launch_select(const SelectArgs &a, int op, bool partition, cudaStream_t s) {
+    return partition ? launch_select_part<T, true>(a, op, s) : launch_select_part<T, false>(a, op, s);
+}
+
+template cudaError_t launch_select<int32_t>(const SelectArgs &, int, bool, cudaStream_t);
+template cudaError_t launch_select<int64_t>(const SelectArgs &, int, bool, cudaStream_t);
+template cudaError_t launch_select<float>(const SelectArgs &, int, bool, cudaStream_t);
+
+}  // namespace ps
