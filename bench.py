@@ -470,6 +470,7 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
     sweep = []
     if args.sweep and world == 1:
         sweep = run_sweep(args)
+    compaction = run_compaction(args) if args.compaction and world == 1 else None
 
     if rank != 0:
         return
@@ -500,6 +501,8 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
         line["comparison_paths"] = extra
     if sweep:
         line["sweep"] = sweep
+    if compaction:
+        line["compaction"] = compaction
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -532,6 +535,41 @@ def run_sweep(args) -> list[dict]:
     return out
 
 
+def run_compaction(args, n: int = 1 << 28) -> dict:
+    """Single-pass select / partition of int32 values by a Bernoulli(1/2)
+    flag array (the 0/1 pattern of the exclusive-scan workload), GB/s with
+    the algorithmic bytes: values read + flags read + elements written."""
+    import torch
+    from prefix_scan_gb300 import api, inputs
+    dev = torch.device("cuda", 0)
+    x = torch.from_numpy(inputs.full_range_i32(n, 8)).to(dev)
+    f = torch.from_numpy(inputs.bernoulli_half(n, 3).astype(np.uint8)).to(dev)
+    ws = api.alloc_workspace(torch.int32, n, dev)
+    out = torch.empty_like(x)
+    res = {"n": n, "values": "int32 uniform", "flags": "Bernoulli(0.5) uint8"}
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, fn in (("select", lambda: api.select(x, f, out=out, workspace=ws)),
+                     ("partition", lambda: api.partition(x, f, out=out, workspace=ws))):
+        for _ in range(3):
+            _, cnt = fn()
+        torch.cuda.synchronize()
+        k = int(cnt.item())
+        reps = max(3, min(args.steps, 20))
+        ev0.record(stream)
+        for _ in range(reps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t = ev0.elapsed_time(ev1) / 1e3 / reps
+        written = k if name == "select" else n
+        b = n * 4 + n + written * 4
+        res[name] = {"ms": round(t * 1000, 4), "gbs": round(b / t / 1e9, 2),
+                     "gelem_per_s": round(n / t / 1e9, 3), "kept": k,
+                     "algorithmic_bytes": b}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -543,6 +581,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--compare", action="store_true", help="also time the comparison paths")
     ap.add_argument("--sweep", action="store_true", help="also time every workload (extra key)")
+    ap.add_argument("--compaction", action="store_true", help="also time select / partition at 2^28")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

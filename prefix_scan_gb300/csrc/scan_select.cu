@@ -158,15 +158,17 @@ select_kernel(SelectArgs a, long long num_tiles) {
             U cnt = 0;
             if (a.use_bulk && base + TILE <= n) {
                 if (OP == 0) {
+                    // __vcmpne4 sets a byte to 0xff where the flag byte is
+                    // nonzero: eight set bits per kept element
                     const uint4 *f4 = reinterpret_cast<const uint4 *>(flg + (size_t)s * TILE);
+                    U bits = 0;
+#pragma unroll 4
                     for (int i = lane; i < (int)(TILE / 16); i += 32) {
                         const uint4 w = f4[i];
-                        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-#pragma unroll
-                            for (int b = 0; b < 4; ++b) cnt += ((ws4[q] >> (8 * b)) & 0xffu) != 0u;
+                        bits += __popc(__vcmpne4(w.x, 0u)) + __popc(__vcmpne4(w.y, 0u)) +
+                                __popc(__vcmpne4(w.z, 0u)) + __popc(__vcmpne4(w.w, 0u));
                     }
+                    cnt = bits >> 3;
                 } else {
                     const V *src = reinterpret_cast<const V *>(vals + (size_t)s * TILE);
                     for (int i = lane; i < (int)(TILE / VEC); i += 32) {
@@ -283,20 +285,46 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
             const U tile_excl = excl_of[s];
 
-            // scatter
+            if (!PARTITION) {
+                // select: kept elements straight to their places; within a
+                // warp row they form one contiguous run
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                const U before = tile_excl + warp_excl + off[r];
+                for (int r = 0; r < ROWS; ++r) {
+                    const U before = tile_excl + warp_excl + off[r];
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const unsigned long long i = base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
-                    const U sel_before = before + (U)__popc(sel[r] & ((1u << j) - 1u));
-                    if ((sel[r] >> j) & 1u) {
-                        out[sel_before] = v[r][j];
-                    } else if (PARTITION && i < n) {
-                        out[n - 1 - (i - sel_before)] = v[r][j];
+                    for (int j = 0; j < VEC; ++j)
+                        if ((sel[r] >> j) & 1u) out[before + (U)__popc(sel[r] & ((1u << j) - 1u))] = v[r][j];
+                }
+            } else {
+                // partition: each warp packs its kept elements, then its
+                // rejected ones, into its own slice of the stage buffer --
+                // free now: this warp has read its slice and the aggregator
+                // finished with the stage before the prefix was handed over
+                // -- and writes them as two contiguous runs, consecutive
+                // lanes to consecutive addresses (the rejected run downwards
+                // from the end of `out`).
+                T *wbuf = vals + (size_t)s * TILE + seg;
+                const U w_sel = running;   // kept elements of this warp
+                const unsigned long long w_first = base + seg;
+                const U w_valid = w_first >= n ? 0u
+                                  : (n - w_first >= (unsigned long long)(32 * ITEMS) ? (U)(32 * ITEMS)
+                                                                                    : (U)(n - w_first));
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const U e = (U)((r * 32 + lane) * VEC + j);   // index within the warp's slice
+                        const U sel_before = off[r] + (U)__popc(sel[r] & ((1u << j) - 1u));
+                        if ((sel[r] >> j) & 1u) wbuf[sel_before] = v[r][j];
+                        else if (e < w_valid) wbuf[w_sel + (e - sel_before)] = v[r][j];
                     }
                 }
+                __syncwarp();
+                const U dst = tile_excl + warp_excl;   // kept elements before this warp
+                for (U q = lane; q < w_sel; q += 32) out[dst + q] = wbuf[q];
+                const unsigned long long rej_before = w_first - dst;   // rejected before this warp
+                const U w_rej = w_valid - w_sel;
+                for (U q = lane; q < w_rej; q += 32) out[n - 1 - (rej_before + q)] = wbuf[w_sel + q];
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
