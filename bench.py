@@ -471,6 +471,7 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
     if args.sweep and world == 1:
         sweep = run_sweep(args)
     compaction = run_compaction(args) if args.compaction and world == 1 else None
+    ops = run_ops(args) if args.ops and world == 1 else None
 
     if rank != 0:
         return
@@ -503,6 +504,8 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
         line["sweep"] = sweep
     if compaction:
         line["compaction"] = compaction
+    if ops:
+        line["other_ops"] = ops
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -570,6 +573,38 @@ def run_compaction(args, n: int = 1 << 28) -> dict:
     return res
 
 
+def run_ops(args, n: int = 1 << 28) -> dict:
+    """Running max / min of int32 (uniform full range) and the fp32 sum of the
+    deterministic mode at 2^28, GB/s with 2n*4 bytes."""
+    import torch
+    from prefix_scan_gb300 import api, inputs
+    dev = torch.device("cuda", 0)
+    x = torch.from_numpy(inputs.full_range_i32(n, 9)).to(dev)
+    xf = torch.from_numpy(inputs.uniform_f32(n, 10)).to(dev)
+    out = torch.empty_like(x)
+    ws = api.alloc_workspace(torch.int32, n, dev)
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    res = {"n": n}
+    cases = (("max_int32", lambda: api.scan(x, op="max", out=out, workspace=ws)),
+             ("min_int32", lambda: api.scan(x, op="min", out=out, workspace=ws)),
+             ("sum_fp32_deterministic", lambda: api.scan(xf, out=out.view(torch.float32), workspace=ws,
+                                                         algo="deterministic")))
+    for name, fn in cases:
+        for _ in range(3):
+            fn()
+        reps = max(3, min(args.steps, 20))
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(reps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t = ev0.elapsed_time(ev1) / 1e3 / reps
+        res[name] = {"ms": round(t * 1000, 4), "gbs": round(8 * n / t / 1e9, 2)}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -582,6 +617,7 @@ def main():
     ap.add_argument("--compare", action="store_true", help="also time the comparison paths")
     ap.add_argument("--sweep", action="store_true", help="also time every workload (extra key)")
     ap.add_argument("--compaction", action="store_true", help="also time select / partition at 2^28")
+    ap.add_argument("--ops", action="store_true", help="also time max / min and the deterministic mode at 2^28")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -122,6 +122,23 @@ ps_status ps_scan_exclusive_f32(const float *in, float *out, size_t n,
                                 void *ws, size_t ws_bytes, ps_stream_t stream);
 
 /*
+ * Scans with other associative operators (section 4.2 of the paper
+ * summary: the method combines only contiguous parts, in order):
+ *   PS_OP_SUM  y[i] = x[0] + ... + x[i]        (the scans above)
+ *   PS_OP_MAX  y[i] = max(x[0], ..., x[i])     exclusive y[0] = the lowest
+ *   PS_OP_MIN  y[i] = min(x[0], ..., x[i])     value (INT_MIN, -inf) / the
+ *                                              highest (INT_MAX, +inf)
+ * Integers compare as signed.  fp32 max/min follow fmaxf/fminf: NaN
+ * elements are skipped, so y[i] is the max/min of the non-NaN elements so
+ * far (the identity if there is none); results are exact and identical
+ * from run to run.  Decoupled look-back, same conventions, workspace and
+ * errors as the scans above.
+ */
+typedef enum ps_op { PS_OP_SUM = 0, PS_OP_MAX = 1, PS_OP_MIN = 2 } ps_op;
+ps_status ps_scan_op(ps_op op, ps_dtype dtype, int exclusive, const void *in, void *out, size_t n,
+                     void *ws, size_t ws_bytes, ps_stream_t stream);
+
+/*
  * Global scan strategies.  PS_ALGO_DECOUPLED_LOOKBACK is the product path
  * (the six named entry points above).  The other two exist for comparison
  * only (paper summary, section 3.2 "global scan strategies"):
@@ -132,6 +149,12 @@ ps_status ps_scan_exclusive_f32(const float *in, float *out, size_t n,
  *                             immediate predecessor's inclusive prefix only
  *                             (the "domino" scan with adjacent
  *                             synchronisation of the PMPP single-pass page).
+ * PS_ALGO_REDUCE_THEN_SCAN is also the DETERMINISTIC mode: its additions
+ * are associated in a fixed order (tile reductions, one CTA scanning the
+ * tile aggregates, seeded tile scans), so fp32 results are bitwise
+ * reproducible from run to run, which the single pass's look-back -- whose
+ * order depends on scheduling -- does not give.  It costs about 3n words
+ * of traffic instead of 2n.
  */
 typedef enum ps_algo {
     PS_ALGO_DECOUPLED_LOOKBACK = 0,

@@ -49,7 +49,7 @@ def build(force: bool = False, source: Path | None = None, target: Path | None =
         return out
     tmp = out.with_name(out.name + f".{os.getpid()}.tmp")
     cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-fPIC", "-shared",
-           "-o", str(tmp), str(src)]
+           "-o", str(tmp), str(src), "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -74,6 +74,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_flags_i64.argtypes = [vp, sz, ctypes.c_int, ctypes.c_int64, vp]
     lib.oracle_flags_f32.argtypes = [vp, sz, ctypes.c_int, ctypes.c_float, vp]
     for fn in (lib.oracle_flags_i32, lib.oracle_flags_i64, lib.oracle_flags_f32):
+        fn.restype = None
+    for name in ("oracle_scan_op_i32", "oracle_scan_op_i64", "oracle_scan_op_f32"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, sz, ctypes.c_int, ctypes.c_int, vp]
         fn.restype = None
     return lib
 
@@ -166,3 +170,20 @@ def select(x: np.ndarray, f: np.ndarray, lib: ctypes.CDLL | None = None) -> np.n
 def partition(x: np.ndarray, f: np.ndarray, lib: ctypes.CDLL | None = None) -> tuple[np.ndarray, int]:
     """Flagged elements first in order, the others from the back in reverse; (out, count)."""
     return _compact(x, f, True, lib)
+
+
+# ---- running maximum / minimum -------------------------------------------------
+
+OPS = {"max": 1, "min": 2}
+
+
+def scan_op(x: np.ndarray, op: str, exclusive_: bool = False,
+            lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Running max / min (inclusive, or exclusive with the identity first)."""
+    lib = lib if lib is not None else load()
+    x = np.ascontiguousarray(x)
+    y = np.empty_like(x)
+    fn = {np.dtype(np.int32): lib.oracle_scan_op_i32, np.dtype(np.int64): lib.oracle_scan_op_i64,
+          np.dtype(np.float32): lib.oracle_scan_op_f32}[x.dtype]
+    fn(_ptr(x), x.shape[0], OPS[op], int(bool(exclusive_)), _ptr(y))
+    return y

@@ -6,8 +6,8 @@
  * CPU-baseline leg do.  It shares no code, header, table or constant with
  * the CUDA library.
  *
- * What it computes is the plain definition of the scan (and, at the end of
- * the file, of stream compaction) and nothing else:
+ * What it computes is the plain definition of the scan (and, further down,
+ * of stream compaction and of running maximum / minimum) and nothing else:
  *
  *   inclusive  y[i] = x[0] + x[1] + ... + x[i]
  *       ("Prefix Sum" definition, page "CUDA-Operators-6-Cumsum", section 1;
@@ -36,6 +36,7 @@
  * Parity is pinned by the CPU tests (worked examples printed on the pages,
  * O(n^2) brute force, closed forms, invariants, library cross-checks).
  */
+#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -210,4 +211,61 @@ void oracle_flags_f32(const float *x, size_t n, int op, float t, uint8_t *flags)
 {
     for (size_t i = 0; i < n; ++i)
         flags[i] = (uint8_t)(op == 0 ? x[i] != 0.0f : op == 1 ? x[i] > t : x[i] < t);
+}
+
+/* ---- other associative operators: running maximum / minimum -------------
+ *
+ * Section 4.2 of the decoupled look-back paper summary: the method applies
+ * any associative operator to contiguous parts in order.  The definitions
+ * reached, written out directly (op 1 = maximum, 2 = minimum):
+ *   inclusive  y[i] = op(x[0], ..., x[i])
+ *   exclusive  y[0] = identity, y[i] = op(x[0], ..., x[i-1])
+ * with the identity the lowest value of the type for the maximum and the
+ * highest for the minimum (INT_MIN / INT_MAX, -inf / +inf).  Integers
+ * compare as signed.  fp32 uses fmaxf / fminf, which skip a NaN operand,
+ * so a NaN element never becomes the running value.
+ */
+void oracle_scan_op_i32(const int32_t *x, size_t n, int op, int exclusive, int32_t *y)
+{
+    int32_t acc = op == 1 ? INT32_MIN : INT32_MAX;
+    for (size_t i = 0; i < n; ++i) {
+        int32_t xi = x[i];
+        if (exclusive)
+            y[i] = acc;
+        if (op == 1)
+            acc = xi > acc ? xi : acc;
+        else
+            acc = xi < acc ? xi : acc;
+        if (!exclusive)
+            y[i] = acc;
+    }
+}
+
+void oracle_scan_op_i64(const int64_t *x, size_t n, int op, int exclusive, int64_t *y)
+{
+    int64_t acc = op == 1 ? INT64_MIN : INT64_MAX;
+    for (size_t i = 0; i < n; ++i) {
+        int64_t xi = x[i];
+        if (exclusive)
+            y[i] = acc;
+        if (op == 1)
+            acc = xi > acc ? xi : acc;
+        else
+            acc = xi < acc ? xi : acc;
+        if (!exclusive)
+            y[i] = acc;
+    }
+}
+
+void oracle_scan_op_f32(const float *x, size_t n, int op, int exclusive, float *y)
+{
+    float acc = op == 1 ? -INFINITY : INFINITY;
+    for (size_t i = 0; i < n; ++i) {
+        float xi = x[i];
+        if (exclusive)
+            y[i] = acc;
+        acc = op == 1 ? fmaxf(acc, xi) : fminf(acc, xi);
+        if (!exclusive)
+            y[i] = acc;
+    }
 }

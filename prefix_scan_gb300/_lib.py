@@ -45,6 +45,8 @@ SIGNATURES["ps_scan_inclusive_i32_noalloc"] = (_int, [_vp, _vp, _sz, _vp])
 SIGNATURES["ps_scan_seeded"] = (_int, [_int, _int, _vp, _vp, _sz, _vp, _vp, _vp, _sz, _vp])
 SIGNATURES["ps_scan_host_staging_size"] = (_sz, [_int, _sz])
 SIGNATURES["ps_scan_host"] = (_int, [_int, _int, _vp, _vp, _sz, _vp, _sz, _vp, _sz, _vp])
+SIGNATURES["ps_scan_op"] = (_int, [_int, _int, _int, _vp, _vp, _sz, _vp, _sz, _vp])
+PS_OP_SUM, PS_OP_MAX, PS_OP_MIN = 0, 1, 2
 SIGNATURES["ps_select"] = (_int, [_int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp])
 SIGNATURES["ps_partition"] = (_int, [_int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp])
 PS_SELECT_FLAGGED, PS_SELECT_NONZERO, PS_SELECT_GREATER, PS_SELECT_LESS = 0, 1, 2, 3

@@ -18,6 +18,8 @@ DTYPE_CODES = {torch.int32: PS_INT32, torch.int64: PS_INT64, torch.float32: PS_F
 _SUFFIX = {PS_INT32: "i32", PS_INT64: "i64", PS_FLOAT32: "f32"}
 ALGOS = {"decoupled": PS_ALGO_DECOUPLED_LOOKBACK,
          "reduce_then_scan": PS_ALGO_REDUCE_THEN_SCAN,
+         # fixed association: bitwise-reproducible fp32 results
+         "deterministic": PS_ALGO_REDUCE_THEN_SCAN,
          "chained": PS_ALGO_CHAINED}
 
 
@@ -49,9 +51,12 @@ def _stream_handle(stream, device) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
+OPS = {"sum": 0, "max": 1, "min": 2}
+
+
 def scan(x: torch.Tensor, *, exclusive: bool = False, out: torch.Tensor | None = None,
          inplace: bool = False, workspace: torch.Tensor | None = None, stream=None,
-         algo: str = "decoupled") -> torch.Tensor:
+         algo: str = "decoupled", op: str = "sum") -> torch.Tensor:
     """Inclusive/exclusive sum scan of a contiguous 1-D CUDA tensor.
 
     ``inplace=True`` writes the result over ``x``.  ``workspace`` (uint8,
@@ -82,7 +87,13 @@ def scan(x: torch.Tensor, *, exclusive: bool = False, out: torch.Tensor | None =
         raise ValueError(f"prefix scan: workspace needs {need} bytes on {x.device}")
     ws_bytes = workspace.numel() * workspace.element_size()
     s = _stream_handle(stream, x.device)
-    if algo == "decoupled":
+    if op != "sum":
+        if algo != "decoupled":
+            raise ValueError("prefix scan: max/min scans run the decoupled look-back only")
+        name = "ps_scan_op"
+        st = lib.ps_scan_op(OPS[op], code, int(exclusive), x.data_ptr(), out.data_ptr(), n,
+                            workspace.data_ptr(), ws_bytes, s)
+    elif algo == "decoupled":
         kind = "exclusive" if exclusive else "inclusive"
         name = f"ps_scan_{kind}_{_SUFFIX[code]}"
         st = getattr(lib, name)(x.data_ptr(), out.data_ptr(), n, workspace.data_ptr(), ws_bytes, s)

@@ -48,7 +48,7 @@ ps_status check_args(ps_dtype dt, const void *in, const void *out, size_t n, con
 template <typename T>
 ps_status run(ps_algo algo, bool exclusive, const void *in, void *out, size_t n, void *ws,
               size_t ws_bytes, cudaStream_t s, const void *carry_in = nullptr,
-              void *carry_out = nullptr) {
+              void *carry_out = nullptr, ps_op op = PS_OP_SUM) {
     cudaError_t e;
     unsigned char *w = static_cast<unsigned char *>(ws);
     switch (algo) {
@@ -58,7 +58,7 @@ ps_status run(ps_algo algo, bool exclusive, const void *in, void *out, size_t n,
                        (unsigned long long)(ws_bytes & ~(size_t)7), ps::kDefaultMaxPolls};
         e = ps::launch_single_pass<T>(a, exclusive,
                                       algo == PS_ALGO_CHAINED ? ps::Lookback::Chained
-                                                              : ps::Lookback::Decoupled, s);
+                                                              : ps::Lookback::Decoupled, s, op);
         break;
     }
     case PS_ALGO_REDUCE_THEN_SCAN:
@@ -199,6 +199,21 @@ ps_status ps_scan_seeded(ps_dtype dtype, int exclusive, const void *in, void *ou
                          ps_stream_t stream) {
     return ps::scan_seeded(dtype, exclusive, in, out, n, carry_in, carry_out, ws, ws_bytes,
                            (cudaStream_t)stream);
+}
+
+ps_status ps_scan_op(ps_op op, ps_dtype dtype, int exclusive, const void *in, void *out, size_t n,
+                     void *ws, size_t ws_bytes, ps_stream_t stream) {
+    if (!valid_dtype(dtype) || (op != PS_OP_SUM && op != PS_OP_MAX && op != PS_OP_MIN))
+        return PS_ERR_INVALID_ARG;
+    if (n == 0) return PS_OK;
+    const ps_status st = check_args(dtype, in, out, n, ws, ws_bytes);
+    if (st != PS_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (dtype) {
+    case PS_INT32: return run<int32_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes, s, nullptr, nullptr, op);
+    case PS_INT64: return run<int64_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes, s, nullptr, nullptr, op);
+    default: return run<float>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes, s, nullptr, nullptr, op);
+    }
 }
 
 ps_status ps_select(ps_dtype dtype, ps_select_op op, const void *in, const uint8_t *flags,

@@ -175,23 +175,74 @@ __device__ __forceinline__ void report_error(unsigned long long *status, uint32_
 // Inclusive Kogge-Stone scan over the 32 lanes with shuffles (the warp scan
 // of the cumsum page, section 2, and of the Kogge-Stone network, Fig. 1b of
 // the paper summary).  The predecessor's partial is the left operand.
-template <typename U> __device__ __forceinline__ U warp_inclusive(U v, int lane) {
+// ---- associative operators ---------------------------------------------------
+// combine(a, b) is a (+) b with `a` the earlier part of the sequence; the
+// scans only ever combine contiguous parts in that order (section 4.2 of the
+// paper summary: non-commutative operators are allowed), and identity() is
+// the value of an empty part.  U is the lane type of Traits<T>: integers are
+// carried as unsigned bits, so max/min compare them as signed.
+__device__ __forceinline__ uint32_t max_of(uint32_t a, uint32_t b) { return (int32_t)a >= (int32_t)b ? a : b; }
+__device__ __forceinline__ unsigned long long max_of(unsigned long long a, unsigned long long b) {
+    return (long long)a >= (long long)b ? a : b;
+}
+__device__ __forceinline__ float max_of(float a, float b) { return fmaxf(a, b); }
+__device__ __forceinline__ uint32_t min_of(uint32_t a, uint32_t b) { return (int32_t)a <= (int32_t)b ? a : b; }
+__device__ __forceinline__ unsigned long long min_of(unsigned long long a, unsigned long long b) {
+    return (long long)a <= (long long)b ? a : b;
+}
+__device__ __forceinline__ float min_of(float a, float b) { return fminf(a, b); }
+__device__ __forceinline__ uint32_t lowest_of(uint32_t) { return 0x80000000u; }
+__device__ __forceinline__ unsigned long long lowest_of(unsigned long long) { return 0x8000000000000000ull; }
+__device__ __forceinline__ float lowest_of(float) { return __int_as_float(0xff800000); }   // -inf
+__device__ __forceinline__ uint32_t highest_of(uint32_t) { return 0x7fffffffu; }
+__device__ __forceinline__ unsigned long long highest_of(unsigned long long) { return 0x7fffffffffffffffull; }
+__device__ __forceinline__ float highest_of(float) { return __int_as_float(0x7f800000); }  // +inf
+
+struct OpSum {
+    template <typename U> static __device__ __forceinline__ U identity() { return U(0); }
+    template <typename U> static __device__ __forceinline__ U combine(U a, U b) { return a + b; }
+};
+// fp32: fmaxf / fminf, which skip a NaN operand, so the result is the
+// maximum (minimum) of the non-NaN elements and the identity when there is
+// none; exact, associative and commutative.
+struct OpMax {
+    template <typename U> static __device__ __forceinline__ U identity() { return lowest_of(U()); }
+    template <typename U> static __device__ __forceinline__ U combine(U a, U b) { return max_of(a, b); }
+};
+struct OpMin {
+    template <typename U> static __device__ __forceinline__ U identity() { return highest_of(U()); }
+    template <typename U> static __device__ __forceinline__ U combine(U a, U b) { return min_of(a, b); }
+};
+
+// Inclusive Kogge-Stone scan over the 32 lanes with shuffles (the warp scan
+// of the cumsum page, section 2, and of the Kogge-Stone network, Fig. 1b of
+// the paper summary).  The predecessor's partial is the left operand.
+template <typename U, typename Op = OpSum> __device__ __forceinline__ U warp_inclusive(U v, int lane) {
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         U o = __shfl_up_sync(kFull, v, d);
-        if (lane >= d) v = o + v;
+        if (lane >= d) v = Op::combine(o, v);
     }
     return v;
 }
 
-template <typename U> __device__ __forceinline__ U warp_sum(U v) {
+// Reduction over the 32 lanes (butterfly; the operators here are
+// commutative, so the lane order does not matter).
+template <typename U, typename Op = OpSum> __device__ __forceinline__ U warp_reduce(U v) {
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) v = v + __shfl_xor_sync(kFull, v, d);
+    for (int d = 16; d > 0; d >>= 1) v = Op::combine(v, __shfl_xor_sync(kFull, v, d));
     return v;
 }
-template <> __device__ __forceinline__ uint32_t warp_sum<uint32_t>(uint32_t v) {
+template <> __device__ __forceinline__ uint32_t warp_reduce<uint32_t, OpSum>(uint32_t v) {
     return __reduce_add_sync(kFull, v);
 }
+template <> __device__ __forceinline__ uint32_t warp_reduce<uint32_t, OpMax>(uint32_t v) {
+    return (uint32_t)__reduce_max_sync(kFull, (int)v);   // signed
+}
+template <> __device__ __forceinline__ uint32_t warp_reduce<uint32_t, OpMin>(uint32_t v) {
+    return (uint32_t)__reduce_min_sync(kFull, (int)v);
+}
+template <typename U> __device__ __forceinline__ U warp_sum(U v) { return warp_reduce<U, OpSum>(v); }
 
 // Sleep between polls of a descriptor that is not ready yet.
 __device__ __forceinline__ void poll_backoff(uint32_t polls) {
@@ -218,11 +269,12 @@ __device__ __forceinline__ void poll_backoff(uint32_t polls) {
 // A poll cap bounds every wait.  When it is exceeded the status word gets
 // PS_ERR_LOOKBACK_TIMEOUT and the missing tiles count as P with the
 // identity, so the warp finishes (with a wrong value) instead of hanging.
-template <typename U, int DW, int K>
+template <typename U, int DW, int K, typename Op = OpSum>
 __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_t epoch,
                                        uint32_t max_polls, unsigned long long *status) {
     const int lane = threadIdx.x & 31;
-    U excl = U(0);
+    const U ident = Op::template identity<U>();
+    U excl = ident;
     long long base = tile - 1;
     uint32_t polls = 0;
     bool gave_up = false;
@@ -233,7 +285,7 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
         for (int j = 0; j < K; ++j) {
             const long long idx = base - (long long)(lane * K + j);
             f[j] = kFlagP;
-            v[j] = U(0);
+            v[j] = ident;
             if (idx >= 0) Desc<U, DW>::load(desc, idx, epoch, f[j], v[j]);
         }
         bool done;
@@ -260,7 +312,7 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
                     gave_up = true;
 #pragma unroll
                     for (int j = 0; j < K; ++j)
-                        if (f[j] == kFlagX) { f[j] = kFlagP; v[j] = U(0); }
+                        if (f[j] == kFlagX) { f[j] = kFlagP; v[j] = ident; }
                     continue;
                 }
                 poll_backoff(polls);
@@ -274,11 +326,11 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
             }
             // no X before the nearest P (or neither X nor P in the window)
             const int limit = mp ? pos_p : 0x7fffffff;
-            U part = U(0);
+            U part = ident;
 #pragma unroll
             for (int j = K - 1; j >= 0; --j)   // farther tiles on the left
-                if (lane * K + j <= limit) part = v[j] + part;
-            excl = warp_sum<U>(part) + excl;
+                if (lane * K + j <= limit) part = Op::combine(v[j], part);
+            excl = Op::combine(warp_reduce<U, Op>(part), excl);
             done = (mp != 0u);
             break;
         }

@@ -135,13 +135,14 @@ struct PassArgs {
 
 // Enqueue the persistent TMA-fed single-pass kernel (16-byte aligned in/out).
 template <typename T>
-cudaError_t launch_persistent(const PassArgs &a, bool exclusive, cudaStream_t s);
+cudaError_t launch_persistent(const PassArgs &a, bool exclusive, ps_op op, cudaStream_t s);
 
 // Enqueue one single-pass scan (one kernel; the workspace needs no reset).
 // T is int32_t, int64_t or float.  Decoupled look-back on 16-byte aligned
 // arrays runs the persistent kernel; otherwise one CTA per tile.
 template <typename T>
-cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s);
+cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s,
+                               ps_op op = PS_OP_SUM);
 
 // Third kernel of reduce-then-scan: tile scan seeded from the workspace.
 template <typename T>

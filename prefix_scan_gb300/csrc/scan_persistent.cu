@@ -59,11 +59,12 @@ constexpr size_t persistent_smem_bytes() {
 static_assert(kThreads % 32 == 0 && kThreads <= 960, "compute threads per CTA");
 
 
-template <typename T, bool EXCL>
+template <typename T, bool EXCL, typename Op>
 __global__ void __launch_bounds__((kPCW + 3) * 32, kPCtasPerSm)
 persistent_kernel(PassArgs a, long long num_tiles) {
     using Tr = Traits<T>;
     using U = typename Tr::U;
+    const U ident = Op::template identity<U>();
     using V = typename Tr::V;
     constexpr int VEC = Tr::VEC;
     constexpr int ITEMS = PItems<T>::value;
@@ -148,28 +149,28 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 break;
             }
             const unsigned long long tile_base = (unsigned long long)tile * TILE;
-            U acc = U(0);
+            U acc = ident;
             if (tile_base + TILE <= n) {
                 const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE);
 #pragma unroll 8
                 for (int i = lane; i < (int)(TILE / VEC); i += 32) {
                     const V x = src[i];
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) acc = acc + (U)vget(x, j);
+                    for (int j = 0; j < VEC; ++j) acc = Op::combine(acc, (U)vget(x, j));
                 }
             } else {
-                for (unsigned long long i = tile_base + lane; i < n; i += 32) acc = acc + (U)in[i];
+                for (unsigned long long i = tile_base + lane; i < n; i += 32) acc = Op::combine(acc, (U)in[i]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
-            const U agg = warp_sum<U>(acc);
+            const U agg = warp_reduce<U, Op>(acc);
             if (lane == 0) {
                 if (tile == 0) {
                     // the only read of carry_in: it precedes tile 0's P, hence
                     // every other tile's P and the write of carry_out, so
                     // carry_in may alias carry_out
-                    const U c = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : U(0);
-                    Desc<U, Tr::DW>::store(desc, 0, kFlagP, c + agg, epoch);
+                    const U c = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : ident;
+                    Desc<U, Tr::DW>::store(desc, 0, kFlagP, Op::combine(c, agg), epoch);
                     excl_of[s] = c;   // for the look-back warp
                 } else {
                     Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg, epoch);
@@ -197,11 +198,11 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             if (tile == 0) {
                 excl = excl_of[s];   // the carry the aggregator read
             } else {
-                excl = look_back<U, Tr::DW, kLookbackK>(desc, tile, epoch, a.max_polls, &hdr->status);
-                if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg, epoch);
+                excl = look_back<U, Tr::DW, kLookbackK, Op>(desc, tile, epoch, a.max_polls, &hdr->status);
+                if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, Op::combine(excl, agg), epoch);
             }
             if (lane == 0) {
-                if (a.carry_out && tile == num_tiles - 1) *reinterpret_cast<U *>(a.carry_out) = excl + agg;
+                if (a.carry_out && tile == num_tiles - 1) *reinterpret_cast<U *>(a.carry_out) = Op::combine(excl, agg);
                 excl_of[s] = excl;
                 mbar_arrive(&prefix_ready[s]);
             }
@@ -237,45 +238,45 @@ persistent_kernel(PassArgs a, long long num_tiles) {
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) {
                     const unsigned long long i = tile_base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
-                    v[r][j] = i < n ? (U)in[i] : U(0);
+                    v[r][j] = i < n ? (U)in[i] : ident;
                 }
         }
         // a3 + a4
         U off[ROWS];
-        U running = U(0);
+        U running = ident;
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
             U t;
             if (EXCL) {
-                U acc = U(0);
+                U acc = ident;
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) {
                     const U x = v[r][j];
                     v[r][j] = acc;
-                    acc = acc + x;
+                    acc = Op::combine(acc, x);
                 }
                 t = acc;
             } else {
 #pragma unroll
-                for (int j = 1; j < VEC; ++j) v[r][j] = v[r][j - 1] + v[r][j];
+                for (int j = 1; j < VEC; ++j) v[r][j] = Op::combine(v[r][j - 1], v[r][j]);
                 t = v[r][VEC - 1];
             }
-            const U sc = warp_inclusive<U>(t, lane);
+            const U sc = warp_inclusive<U, Op>(t, lane);
             U le = __shfl_up_sync(kFull, sc, 1);
-            if (lane == 0) le = U(0);
+            if (lane == 0) le = ident;
             const U row_total = __shfl_sync(kFull, sc, 31);
-            off[r] = running + le;
-            running = running + row_total;
+            off[r] = Op::combine(running, le);
+            running = Op::combine(running, row_total);
         }
 
         // a5 (double-buffered by iteration, so that no second barrier is needed)
         U *sw = s_warp[k & 1];
         if (lane == 0) sw[warp] = running;
         named_barrier(1, CT);
-        U warp_excl = U(0);
+        U warp_excl = ident;
 #pragma unroll
         for (int w = 0; w < kPCW; ++w)
-            if (w < warp) warp_excl = warp_excl + sw[w];
+            if (w < warp) warp_excl = Op::combine(warp_excl, sw[w]);
 
         // the look-back warp provides the tile's exclusive prefix
         if (!mbar_wait(&prefix_ready[s], (uint32_t)((k / kPStages) & 1)))   // never in a correct run
@@ -283,12 +284,12 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         const U tile_excl = excl_of[s];
 
         // a9
-        const U base = tile_excl + warp_excl;
+        const U base = Op::combine(tile_excl, warp_excl);
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
-            const U o = base + off[r];
+            const U o = Op::combine(base, off[r]);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) v[r][j] = o + v[r][j];
+            for (int j = 0; j < VEC; ++j) v[r][j] = Op::combine(o, v[r][j]);
         }
         if (!cut) {
             V *dst = reinterpret_cast<V *>(out + tile_base + seg) + lane;
@@ -320,7 +321,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     finish_call(hdr, a.ws, a.ws_bytes, epoch);
 }
 
-template <typename T, bool EXCL>
+template <typename T, bool EXCL, typename Op>
 cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
     constexpr size_t smem = persistent_smem_bytes<T>();
     const long long tiles = (long long)((a.n + persistent_tile_elems<T>() - 1) / persistent_tile_elems<T>());
@@ -331,7 +332,7 @@ cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(persistent_kernel<T, EXCL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(persistent_kernel<T, EXCL, Op>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = 1;
@@ -339,17 +340,24 @@ cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     long long grid = (long long)sms * kPCtasPerSm;
     if (grid > tiles) grid = tiles;
-    persistent_kernel<T, EXCL><<<(unsigned int)grid, (kPCW + 3) * 32, smem, s>>>(a, tiles);
+    persistent_kernel<T, EXCL, Op><<<(unsigned int)grid, (kPCW + 3) * 32, smem, s>>>(a, tiles);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_persistent(const PassArgs &a, bool exclusive, cudaStream_t s) {
-    return exclusive ? launch_persistent_kind<T, true>(a, s) : launch_persistent_kind<T, false>(a, s);
+cudaError_t launch_persistent(const PassArgs &a, bool exclusive, ps_op op, cudaStream_t s) {
+    switch (op) {
+    case PS_OP_MAX:
+        return exclusive ? launch_persistent_kind<T, true, OpMax>(a, s) : launch_persistent_kind<T, false, OpMax>(a, s);
+    case PS_OP_MIN:
+        return exclusive ? launch_persistent_kind<T, true, OpMin>(a, s) : launch_persistent_kind<T, false, OpMin>(a, s);
+    default:
+        return exclusive ? launch_persistent_kind<T, true, OpSum>(a, s) : launch_persistent_kind<T, false, OpSum>(a, s);
+    }
 }
 
-template cudaError_t launch_persistent<int32_t>(const PassArgs &, bool, cudaStream_t);
-template cudaError_t launch_persistent<int64_t>(const PassArgs &, bool, cudaStream_t);
-template cudaError_t launch_persistent<float>(const PassArgs &, bool, cudaStream_t);
+template cudaError_t launch_persistent<int32_t>(const PassArgs &, bool, ps_op, cudaStream_t);
+template cudaError_t launch_persistent<int64_t>(const PassArgs &, bool, ps_op, cudaStream_t);
+template cudaError_t launch_persistent<float>(const PassArgs &, bool, ps_op, cudaStream_t);
 
 }  // namespace ps

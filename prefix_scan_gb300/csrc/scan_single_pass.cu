@@ -35,11 +35,12 @@ namespace ps {
 #define PS_MIN_BLOCKS 1
 #endif
 
-template <typename T, int THREADS, int ITEMS, bool EXCL, bool VEC_IO, Lookback LB>
+template <typename T, int THREADS, int ITEMS, bool EXCL, bool VEC_IO, Lookback LB, typename Op>
 __global__ void __launch_bounds__(THREADS, PS_MIN_BLOCKS)
 single_pass_kernel(PassArgs a) {
     using Tr = Traits<T>;
     using U = typename Tr::U;
+    const U ident = Op::template identity<U>();
     using V = typename Tr::V;
     constexpr int VEC = Tr::VEC;
     constexpr int ROWS = ITEMS / VEC;
@@ -91,48 +92,48 @@ single_pass_kernel(PassArgs a) {
 #pragma unroll
             for (int k = 0; k < VEC; ++k) {
                 const unsigned long long i = seg + (unsigned long long)(r * 32 + lane) * VEC + k;
-                v[r][k] = i < n ? (U)in[i] : U(0);
+                v[r][k] = i < n ? (U)in[i] : ident;
             }
     }
 
     // a3 + a4: per-thread sequential scan of each row chunk, warp scan of the
     // chunk totals, rows chained in registers.
     U off[ROWS];
-    U running = U(0);
+    U running = ident;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
         U t;
         if (EXCL) {
-            U acc = U(0);
+            U acc = ident;
 #pragma unroll
             for (int k = 0; k < VEC; ++k) {
                 const U x = v[r][k];
                 v[r][k] = acc;
-                acc = acc + x;
+                acc = Op::combine(acc, x);
             }
             t = acc;
         } else {
 #pragma unroll
-            for (int k = 1; k < VEC; ++k) v[r][k] = v[r][k - 1] + v[r][k];
+            for (int k = 1; k < VEC; ++k) v[r][k] = Op::combine(v[r][k - 1], v[r][k]);
             t = v[r][VEC - 1];
         }
-        const U s = warp_inclusive<U>(t, lane);
+        const U s = warp_inclusive<U, Op>(t, lane);
         U le = __shfl_up_sync(kFull, s, 1);
-        if (lane == 0) le = U(0);
+        if (lane == 0) le = ident;
         const U row_total = __shfl_sync(kFull, s, 31);
-        off[r] = running + le;
-        running = running + row_total;
+        off[r] = Op::combine(running, le);
+        running = Op::combine(running, row_total);
     }
 
     // a5: cross-warp scan through shared memory
     if (lane == 0) s_warp[warp] = running;
     __syncthreads();
-    U warp_excl = U(0), agg = U(0);
+    U warp_excl = ident, agg = ident;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
         const U t = s_warp[w];
-        if (w < warp) warp_excl = warp_excl + t;
-        agg = agg + t;
+        if (w < warp) warp_excl = Op::combine(warp_excl, t);
+        agg = Op::combine(agg, t);
     }
 
     // a6..a8: publish, look back, publish
@@ -145,32 +146,32 @@ single_pass_kernel(PassArgs a) {
             // one read of carry_in, by the lane that then publishes tile 0's
             // P: every other tile's P and the write of carry_out follow it,
             // so carry_in may alias carry_out
-            U c = U(0);
+            U c = ident;
             if (lane == 0 && a.carry_in) c = *reinterpret_cast<const U *>(a.carry_in);
             excl = __shfl_sync(kFull, c, 0);
-            if (lane == 0) Desc<U, Tr::DW>::store(desc, 0, kFlagP, excl + agg, epoch);
+            if (lane == 0) Desc<U, Tr::DW>::store(desc, 0, kFlagP, Op::combine(excl, agg), epoch);
         } else {
             if (LB == Lookback::Decoupled && lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg, epoch);
             excl = (LB == Lookback::Chained)
                        ? chained_wait<U, Tr::DW>(desc, tile, epoch, a.max_polls, &hdr->status)
-                       : look_back<U, Tr::DW, kLookbackK>(desc, tile, epoch, a.max_polls, &hdr->status);
-            if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, excl + agg, epoch);
+                       : look_back<U, Tr::DW, kLookbackK, Op>(desc, tile, epoch, a.max_polls, &hdr->status);
+            if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, Op::combine(excl, agg), epoch);
         }
         if (lane == 0) {
             s_excl = excl;
             const long long last = (long long)((n + TILE - 1) / TILE) - 1;
-            if (a.carry_out && tile == last) *reinterpret_cast<U *>(a.carry_out) = excl + agg;
+            if (a.carry_out && tile == last) *reinterpret_cast<U *>(a.carry_out) = Op::combine(excl, agg);
         }
     }
     __syncthreads();
 
     // a9: seeded output
-    const U base = s_excl + warp_excl;
+    const U base = Op::combine(s_excl, warp_excl);
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
-        const U o = base + off[r];
+        const U o = Op::combine(base, off[r]);
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) v[r][k] = o + v[r][k];
+        for (int k = 0; k < VEC; ++k) v[r][k] = Op::combine(o, v[r][k]);
     }
     if (VEC_IO && full) {
         V *dst = reinterpret_cast<V *>(out + seg) + lane;
@@ -196,18 +197,18 @@ single_pass_kernel(PassArgs a) {
 template <typename T> struct ItemsOf { static constexpr int value = kItems32; };
 template <> struct ItemsOf<int64_t> { static constexpr int value = kItems64; };
 
-template <typename T, bool EXCL, bool VEC_IO, Lookback LB>
+template <typename T, bool EXCL, bool VEC_IO, Lookback LB, typename Op>
 cudaError_t launch_variant(const PassArgs &a, size_t tiles, cudaStream_t s) {
     constexpr int ITEMS = ItemsOf<T>::value;
-    single_pass_kernel<T, kThreads, ITEMS, EXCL, VEC_IO, LB>
+    single_pass_kernel<T, kThreads, ITEMS, EXCL, VEC_IO, LB, Op>
         <<<(unsigned int)tiles, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-template <typename T, bool EXCL, Lookback LB>
+template <typename T, bool EXCL, Lookback LB, typename Op = OpSum>
 cudaError_t launch_kind(const PassArgs &a, bool vec_io, size_t tiles, cudaStream_t s) {
-    return vec_io ? launch_variant<T, EXCL, true, LB>(a, tiles, s)
-                  : launch_variant<T, EXCL, false, LB>(a, tiles, s);
+    return vec_io ? launch_variant<T, EXCL, true, LB, Op>(a, tiles, s)
+                  : launch_variant<T, EXCL, false, LB, Op>(a, tiles, s);
 }
 
 template <typename T> constexpr ps_dtype dtype_of();
@@ -215,17 +216,28 @@ template <> constexpr ps_dtype dtype_of<int32_t>() { return PS_INT32; }
 template <> constexpr ps_dtype dtype_of<int64_t>() { return PS_INT64; }
 template <> constexpr ps_dtype dtype_of<float>() { return PS_FLOAT32; }
 
+template <typename T, typename Op>
+static cudaError_t launch_fallback(const PassArgs &a, bool exclusive, size_t tiles, cudaStream_t s) {
+    // one CTA per tile with bounds-checked scalar I/O (arrays not 16-byte aligned)
+    return exclusive ? launch_kind<T, true, Lookback::Decoupled, Op>(a, false, tiles, s)
+                     : launch_kind<T, false, Lookback::Decoupled, Op>(a, false, tiles, s);
+}
+
 template <typename T>
-cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s) {
+cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s,
+                               ps_op op) {
     constexpr ps_dtype dt = dtype_of<T>();
     const size_t tiles = num_tiles(dt, a.n);
     // a0 needs no work here: descriptors of earlier calls carry another
     // epoch and read as X, and the previous call left the counter at 0
     const bool vec_io = ((reinterpret_cast<uintptr_t>(a.in) | reinterpret_cast<uintptr_t>(a.out)) & 15u) == 0;
     if (lb == Lookback::Decoupled) {
-        if (vec_io) return launch_persistent<T>(a, exclusive, s);
-        return exclusive ? launch_kind<T, true, Lookback::Decoupled>(a, vec_io, tiles, s)
-                         : launch_kind<T, false, Lookback::Decoupled>(a, vec_io, tiles, s);
+        if (vec_io) return launch_persistent<T>(a, exclusive, op, s);
+        switch (op) {
+        case PS_OP_MAX: return launch_fallback<T, OpMax>(a, exclusive, tiles, s);
+        case PS_OP_MIN: return launch_fallback<T, OpMin>(a, exclusive, tiles, s);
+        default: return launch_fallback<T, OpSum>(a, exclusive, tiles, s);
+        }
     }
     return exclusive ? launch_kind<T, true, Lookback::Chained>(a, vec_io, tiles, s)
                      : launch_kind<T, false, Lookback::Chained>(a, vec_io, tiles, s);
@@ -244,9 +256,9 @@ template cudaError_t launch_seeded_tile_scan<int32_t>(const PassArgs &, bool, cu
 template cudaError_t launch_seeded_tile_scan<int64_t>(const PassArgs &, bool, cudaStream_t);
 template cudaError_t launch_seeded_tile_scan<float>(const PassArgs &, bool, cudaStream_t);
 
-template cudaError_t launch_single_pass<int32_t>(const PassArgs &, bool, Lookback, cudaStream_t);
-template cudaError_t launch_single_pass<int64_t>(const PassArgs &, bool, Lookback, cudaStream_t);
-template cudaError_t launch_single_pass<float>(const PassArgs &, bool, Lookback, cudaStream_t);
+template cudaError_t launch_single_pass<int32_t>(const PassArgs &, bool, Lookback, cudaStream_t, ps_op);
+template cudaError_t launch_single_pass<int64_t>(const PassArgs &, bool, Lookback, cudaStream_t, ps_op);
+template cudaError_t launch_single_pass<float>(const PassArgs &, bool, Lookback, cudaStream_t, ps_op);
 
 // ---- test hook: the look-back alone -----------------------------------------
 template <typename T>

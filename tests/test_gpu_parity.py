@@ -245,3 +245,19 @@ def test_lookback_ignores_descriptors_of_other_calls():
     assert st & 0xFF == 5 and st >> 8 == 9
     val, st = _lookback("int64", entries, 3, epoch=9, written_epoch=9)
     assert st == 0 and val == 15
+
+
+def test_deterministic_mode_is_bitwise_reproducible():
+    # fp32 sums depend on association; the deterministic mode fixes it
+    n = (1 << 24) + 777
+    x = inputs.uniform_f32(n, 123)
+    t = torch.from_numpy(x).to(DEV)
+    first = api.scan(t, algo="deterministic")
+    check(first.cpu().numpy(), x, False)
+    for _ in range(20):
+        again = api.scan(t, algo="deterministic")
+        assert torch.equal(again.view(torch.int32), first.view(torch.int32))
+    firste = api.scan(t, exclusive=True, algo="deterministic")
+    for _ in range(5):
+        assert torch.equal(api.scan(t, exclusive=True, algo="deterministic").view(torch.int32),
+                           firste.view(torch.int32))

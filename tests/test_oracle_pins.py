@@ -298,10 +298,60 @@ def pin_flags_predicates(lib):
     assert list(oracle.flags(big, "greater", 0, lib)) == [1, 0]
 
 
+# ---- running max / min pins -----------------------------------------------------
+
+def _ident(op, dt):
+    if np.dtype(dt).kind == "f":
+        return -np.inf if op == "max" else np.inf
+    info = np.iinfo(dt)
+    return info.min if op == "max" else info.max
+
+
+def pin_scan_op_brute_force(lib):
+    rng = np.random.default_rng(90)
+    for dt in (np.int32, np.int64, np.float32):
+        for n in range(0, 65):
+            x = rng.integers(-1000, 1000, n).astype(dt)
+            for op in ("max", "min"):
+                f = max if op == "max" else min
+                inc = [f(x[:i + 1]) for i in range(n)]
+                exc = [_ident(op, dt)] + inc[:-1] if n else []
+                assert list(oracle.scan_op(x, op, False, lib)) == inc, (dt, n, op)
+                assert list(oracle.scan_op(x, op, True, lib)) == exc, (dt, n, op)
+
+
+def pin_scan_op_library_crosscheck(lib):
+    n = 300_007
+    for dt in (np.int32, np.int64):
+        x = inputs.uniform_int(n, -10**9, 10**9, 91).astype(dt)
+        assert np.array_equal(oracle.scan_op(x, "max", False, lib), np.maximum.accumulate(x))
+        assert np.array_equal(oracle.scan_op(x, "min", False, lib), np.minimum.accumulate(x))
+        e = oracle.scan_op(x, "max", True, lib)
+        assert e[0] == np.iinfo(dt).min and np.array_equal(e[1:], np.maximum.accumulate(x)[:-1])
+    xf = inputs.uniform_f32(n, 92)
+    xf[::1013] = np.nan
+    for op, ref in (("max", np.fmax), ("min", np.fmin)):
+        want = ref.accumulate(np.concatenate([[_ident(op, np.float32)], xf]).astype(np.float32))
+        assert np.array_equal(oracle.scan_op(xf, op, False, lib), want[1:])
+        assert np.array_equal(oracle.scan_op(xf, op, True, lib), want[:-1])
+
+
+def pin_scan_op_closed_forms(lib):
+    x = np.arange(-500, 500, dtype=np.int64)            # increasing
+    assert np.array_equal(oracle.scan_op(x, "max", False, lib), x)
+    assert np.all(oracle.scan_op(x, "min", False, lib) == -500)
+    neg = np.full(17, -5, dtype=np.int32)               # all negative: identity matters
+    assert list(oracle.scan_op(neg, "max", True, lib)) == [np.iinfo(np.int32).min] + [-5] * 16
+    nan = np.array([np.nan, np.nan, 2.0, np.nan, 1.0], dtype=np.float32)
+    assert list(oracle.scan_op(nan, "max", False, lib)) == [-np.inf, -np.inf, 2.0, 2.0, 2.0]
+    assert list(oracle.scan_op(nan, "min", False, lib)) == [np.inf, np.inf, 2.0, 2.0, 1.0]
+
+
 PINS = [pin_worked_examples, pin_fig6_snapshot, pin_brute_force_int, pin_brute_force_f32,
         pin_abs_prefix, pin_closed_forms, pin_wraparound, pin_library_crosscheck,
         pin_invariants, pin_degenerate, pin_select_brute_force, pin_select_library_crosscheck,
-        pin_select_closed_forms, pin_flags_predicates]
+        pin_select_closed_forms, pin_flags_predicates, pin_scan_op_brute_force,
+        pin_scan_op_library_crosscheck, pin_scan_op_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -331,6 +381,11 @@ MUTANTS = [
     ("oracle_partition_b64", "out[n - 1 - r++] = x[i];", "out[k + r++] = x[i];"),  # rejected not from the back
     ("oracle_flags_i32", "x[i] > t", "x[i] >= t"),                              # off-by-one predicate
     ("oracle_flags_f32", "x[i] != 0.0f", "x[i] == x[i]"),                       # NaN test instead of nonzero
+    ("oracle_scan_op_i32", "int32_t acc = op == 1 ? INT32_MIN : INT32_MAX;",
+     "int32_t acc = 0;"),                                                       # wrong identity
+    ("oracle_scan_op_i64", "acc = xi > acc ? xi : acc;", "acc = xi < acc ? xi : acc;"),  # max computes min
+    ("oracle_scan_op_f32", "acc = op == 1 ? fmaxf(acc, xi) : fminf(acc, xi);",
+     "acc = op == 1 ? (acc > xi ? acc : xi) : fminf(acc, xi);"),               # NaN let in
 ]
 
 
