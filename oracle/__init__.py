@@ -79,6 +79,14 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [vp, sz, ctypes.c_int, ctypes.c_int, vp]
         fn.restype = None
+    for name in ("oracle_rbk_b32_i32", "oracle_rbk_b64_i32"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, vp, sz, vp, vp]
+        fn.restype = sz
+    for name in ("oracle_rbk_b32_f32", "oracle_rbk_b64_f32"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, vp, sz, vp, vp, vp]
+        fn.restype = sz
     return lib
 
 
@@ -187,3 +195,34 @@ def scan_op(x: np.ndarray, op: str, exclusive_: bool = False,
           np.dtype(np.float32): lib.oracle_scan_op_f32}[x.dtype]
     fn(_ptr(x), x.shape[0], OPS[op], int(bool(exclusive_)), _ptr(y))
     return y
+
+
+# ---- reduce-by-key / run-length encoding ---------------------------------------
+
+
+def reduce_by_key(keys: np.ndarray, values: np.ndarray | None = None,
+                  lib: ctypes.CDLL | None = None):
+    """Runs of bitwise-equal consecutive keys: (unique keys, per-run values).
+
+    values int32 -> int32 run sums (mod 2^32); values fp32 -> (float64 run
+    sums, float64 run sums of |value|); values None -> int32 run lengths.
+    """
+    lib = lib if lib is not None else load()
+    keys = np.ascontiguousarray(keys)
+    n = keys.shape[0]
+    bits = keys.dtype.itemsize * 8
+    kraw = keys.view(np.uint32 if bits == 32 else np.uint64)
+    okeys = np.empty(n, dtype=kraw.dtype)
+    if values is None or values.dtype == np.int32:
+        vals = None if values is None else np.ascontiguousarray(values)
+        if vals is not None and vals.shape[0] != n:
+            raise ValueError("oracle: keys and values differ in length")
+        ov = np.empty(n, dtype=np.int32)
+        m = getattr(lib, f"oracle_rbk_b{bits}_i32")(_ptr(kraw), _ptr(vals) if vals is not None else None,
+                                                     n, _ptr(okeys), _ptr(ov))
+        return okeys[:m].view(keys.dtype), ov[:m]
+    vals = np.ascontiguousarray(values, dtype=np.float32)
+    ov = np.empty(n, dtype=np.float64)
+    oa = np.empty(n, dtype=np.float64)
+    m = getattr(lib, f"oracle_rbk_b{bits}_f32")(_ptr(kraw), _ptr(vals), n, _ptr(okeys), _ptr(ov), _ptr(oa))
+    return okeys[:m].view(keys.dtype), ov[:m], oa[:m]

@@ -7,7 +7,8 @@
  * the CUDA library.
  *
  * What it computes is the plain definition of the scan (and, further down,
- * of stream compaction and of running maximum / minimum) and nothing else:
+ * of stream compaction, running maximum / minimum and reduce-by-key / run-
+ * length encoding) and nothing else:
  *
  *   inclusive  y[i] = x[0] + x[1] + ... + x[i]
  *       ("Prefix Sum" definition, page "CUDA-Operators-6-Cumsum", section 1;
@@ -268,4 +269,106 @@ void oracle_scan_op_f32(const float *x, size_t n, int op, int exclusive, float *
         if (!exclusive)
             y[i] = acc;
     }
+}
+
+/* ---- reduce-by-key and run-length encoding -------------------------------
+ *
+ * The paper summary's other single-pass workloads (section A5: reduce-by-key
+ * and run-length encoding fused with the scan).  Definitions written out
+ * directly: a run is a maximal stretch of consecutive equal keys (keys
+ * compared as raw bits, so fp32 keys are equal when their bits are); for
+ * every run, in order, the output holds its key and the sum of its values
+ * (int32 modulo 2^32; fp32 in double), or, with no values, its length.
+ * Returns the number of runs.
+ */
+size_t oracle_rbk_b32_i32(const uint32_t *keys, const int32_t *vals, size_t n, uint32_t *okeys,
+                          int32_t *ovals)
+{
+    size_t m = 0;
+    uint32_t acc = 0u;
+    for (size_t i = 0; i < n; ++i) {
+        uint32_t v = vals ? (uint32_t)vals[i] : 1u;
+        if (i == 0 || keys[i] != keys[i - 1]) {
+            if (m > 0)
+                ((uint32_t *)ovals)[m - 1] = acc;
+            okeys[m++] = keys[i];
+            acc = 0u;
+        }
+        acc += v;
+    }
+    if (m > 0)
+        ((uint32_t *)ovals)[m - 1] = acc;
+    return m;
+}
+
+size_t oracle_rbk_b64_i32(const uint64_t *keys, const int32_t *vals, size_t n, uint64_t *okeys,
+                          int32_t *ovals)
+{
+    size_t m = 0;
+    uint32_t acc = 0u;
+    for (size_t i = 0; i < n; ++i) {
+        uint32_t v = vals ? (uint32_t)vals[i] : 1u;
+        if (i == 0 || keys[i] != keys[i - 1]) {
+            if (m > 0)
+                ((uint32_t *)ovals)[m - 1] = acc;
+            okeys[m++] = keys[i];
+            acc = 0u;
+        }
+        acc += v;
+    }
+    if (m > 0)
+        ((uint32_t *)ovals)[m - 1] = acc;
+    return m;
+}
+
+/* fp32 values: run sums in double, and the sums of |value| that scale the
+ * accepted fp32 error of each run sum. */
+size_t oracle_rbk_b32_f32(const uint32_t *keys, const float *vals, size_t n, uint32_t *okeys,
+                          double *ovals, double *oabs)
+{
+    size_t m = 0;
+    double acc = 0.0, aacc = 0.0;
+    for (size_t i = 0; i < n; ++i) {
+        if (i == 0 || keys[i] != keys[i - 1]) {
+            if (m > 0) {
+                ovals[m - 1] = acc;
+                oabs[m - 1] = aacc;
+            }
+            okeys[m++] = keys[i];
+            acc = 0.0;
+            aacc = 0.0;
+        }
+        acc += (double)vals[i];
+        aacc += fabs((double)vals[i]);
+    }
+    if (m > 0) {
+        ovals[m - 1] = acc;
+        oabs[m - 1] = aacc;
+    }
+    return m;
+}
+
+size_t oracle_rbk_b64_f32(const uint64_t *keys, const float *vals, size_t n, uint64_t *okeys,
+                          double *ovals, double *oabs)
+{
+    size_t m = 0;
+    double acc = 0.0, aacc = 0.0;
+    for (size_t i = 0; i < n; ++i) {
+        if (i == 0 || keys[i] != keys[i - 1]) {
+            if (m > 0) {
+                ovals[m - 1] = acc;
+                oabs[m - 1] = aacc;
+            }
+            okeys[m++] = keys[i];
+            acc = 0.0;
+            aacc = 0.0;
+        }
+        acc += (double)vals[i];
+        aacc += fabs((double)vals[i]);
+    }
+    if (m > 0) {
+        ovals[m - 1] = acc;
+        oabs[m - 1] = aacc;
+    }
+    return m;
 }

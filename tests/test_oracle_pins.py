@@ -347,11 +347,71 @@ def pin_scan_op_closed_forms(lib):
     assert list(oracle.scan_op(nan, "min", False, lib)) == [np.inf, np.inf, 2.0, 2.0, 1.0]
 
 
+# ---- reduce-by-key / RLE pins ----------------------------------------------------
+
+def _runs_python(keys, vals):
+    out_k, out_v = [], []
+    for k, grp in itertools.groupby(zip(keys.tolist() if keys.dtype.kind != "f" else keys.view(np.uint32).tolist(),
+                                        vals.tolist()), key=lambda kv: kv[0]):
+        out_k.append(k)
+        out_v.append(sum(v for _, v in grp))
+    return out_k, out_v
+
+
+def pin_rbk_brute_force(lib):
+    rng = np.random.default_rng(95)
+    for kdt in (np.int32, np.int64, np.float32):
+        for n in range(0, 65):
+            keys = np.sort(rng.integers(0, 6, n)).astype(kdt) if n % 2 else rng.integers(0, 3, n).astype(kdt)
+            vals = rng.integers(-50, 50, n).astype(np.int32)
+            ok, ov = oracle.reduce_by_key(keys, vals, lib)
+            pk, pv = _runs_python(keys, vals)
+            rawk = ok.view(np.uint32).tolist() if kdt == np.float32 else ok.tolist()
+            assert rawk == pk and ov.tolist() == pv, (kdt, n)
+            ok2, counts = oracle.reduce_by_key(keys, None, lib)
+            assert counts.tolist() == [sum(1 for _ in g) for _, g in itertools.groupby(
+                keys.view(np.uint32).tolist() if kdt == np.float32 else keys.tolist())]
+            vf = (vals / 8).astype(np.float32)
+            okf, ovf, oaf = oracle.reduce_by_key(keys, vf, lib)
+            pkf, pvf = _runs_python(keys, vf.astype(np.float64))
+            _, paf = _runs_python(keys, np.abs(vf.astype(np.float64)))
+            assert np.array_equal(okf, ok) and np.allclose(ovf, pvf, rtol=0, atol=1e-9)
+            assert np.allclose(oaf, paf, rtol=0, atol=1e-9)
+
+
+def pin_rbk_numpy_crosscheck(lib):
+    n = 400_003
+    keys = np.repeat(inputs.uniform_int(n // 3 + 1, 0, 5, 96), 3)[:n].astype(np.int64)
+    vals = inputs.full_range_i32(n, 97)
+    heads = np.flatnonzero(np.r_[True, keys[1:] != keys[:-1]])
+    ok, ov = oracle.reduce_by_key(keys, vals, lib)
+    assert np.array_equal(ok, keys[heads])
+    sums = np.add.reduceat(vals.astype(np.int64), heads)
+    assert np.array_equal(ov, (sums & 0xFFFFFFFF).astype(np.uint32).view(np.int32))
+    _, counts = oracle.reduce_by_key(keys, None, lib)
+    assert np.array_equal(counts, np.diff(np.r_[heads, n])) and counts.sum() == n
+
+
+def pin_rbk_closed_forms(lib):
+    n = 10_000
+    same = np.full(n, 7, dtype=np.int32)
+    ok, ov = oracle.reduce_by_key(same, np.ones(n, np.int32), lib)
+    assert ok.tolist() == [7] and ov.tolist() == [n]
+    distinct = np.arange(n, dtype=np.int32)
+    ok, ov = oracle.reduce_by_key(distinct, distinct, lib)
+    assert np.array_equal(ok, distinct) and np.array_equal(ov, distinct)
+    # fp32 keys by bits: -0.0 and +0.0 are different keys, equal NaN bit patterns one key
+    kf = np.array([0.0, -0.0, -0.0, np.nan, np.nan, 1.0], dtype=np.float32)
+    ok, cnt = oracle.reduce_by_key(kf, None, lib)
+    assert cnt.tolist() == [1, 2, 2, 1]
+
+
 PINS = [pin_worked_examples, pin_fig6_snapshot, pin_brute_force_int, pin_brute_force_f32,
         pin_abs_prefix, pin_closed_forms, pin_wraparound, pin_library_crosscheck,
         pin_invariants, pin_degenerate, pin_select_brute_force, pin_select_library_crosscheck,
         pin_select_closed_forms, pin_flags_predicates, pin_scan_op_brute_force,
-        pin_scan_op_library_crosscheck, pin_scan_op_closed_forms]
+        pin_scan_op_library_crosscheck, pin_scan_op_closed_forms, pin_rbk_brute_force,
+        pin_rbk_numpy_crosscheck, pin_rbk_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -386,6 +446,10 @@ MUTANTS = [
     ("oracle_scan_op_i64", "acc = xi > acc ? xi : acc;", "acc = xi < acc ? xi : acc;"),  # max computes min
     ("oracle_scan_op_f32", "acc = op == 1 ? fmaxf(acc, xi) : fminf(acc, xi);",
      "acc = op == 1 ? (acc > xi ? acc : xi) : fminf(acc, xi);"),               # NaN let in
+    ("oracle_rbk_b32_i32", "if (i == 0 || keys[i] != keys[i - 1]) {",
+     "if (i == 0 || keys[i] < keys[i - 1]) {"),                                  # runs only on descent
+    ("oracle_rbk_b64_i32", "        acc += v;\n", "        acc = v;\n"),           # keeps last value
+    ("oracle_rbk_b32_f32", "aacc += fabs((double)vals[i]);", "aacc += (double)vals[i];"),  # dropped abs
 ]
 
 
