@@ -472,6 +472,7 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
         sweep = run_sweep(args)
     compaction = run_compaction(args) if args.compaction and world == 1 else None
     ops = run_ops(args) if args.ops and world == 1 else None
+    rbk = run_reduce_by_key(args) if args.rbk and world == 1 else None
 
     if rank != 0:
         return
@@ -506,6 +507,8 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
         line["compaction"] = compaction
     if ops:
         line["other_ops"] = ops
+    if rbk:
+        line["reduce_by_key"] = rbk
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -573,6 +576,84 @@ def run_compaction(args, n: int = 1 << 28) -> dict:
     return res
 
 
+def run_reduce_by_key(args, n: int = 1 << 25) -> dict:
+    """Single-pass reduce-by-key of {int32 key, fp32 value} pairs and
+    run-length encoding of the int32 keys, for several mean run lengths, GB/s
+    with the algorithmic bytes: keys (and values) read + one (key, 32-bit
+    aggregate) pair written per run."""
+    import torch
+    from prefix_scan_gb300 import api, inputs
+    dev = torch.device("cuda", 0)
+    ws = torch.zeros(api.reduce_by_key_workspace_size(torch.int32, n), dtype=torch.uint8, device=dev)
+    vt = torch.from_numpy(inputs.uniform_f32(n, 12)).to(dev)
+    uk = torch.empty(n, dtype=torch.int32, device=dev)
+    agg = torch.empty(n, dtype=torch.float32, device=dev)
+    cnts = agg.view(torch.int32)
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    res = {"n": n, "keys": "int32, runs of uniform length in [1, 2L-1]", "values": "fp32 uniform [-1, 1)"}
+    for mean in (1, 16, 256):
+        kt = torch.from_numpy(inputs.run_keys(n, mean, 11 + mean)).to(dev)
+        for name, fn in (("reduce_by_key", lambda: api.reduce_by_key(kt, vt, unique_keys=uk, aggregates=agg,
+                                                                     workspace=ws)),
+                         ("run_length_encode", lambda: api.run_length_encode(kt, unique_keys=uk, counts=cnts,
+                                                                             workspace=ws))):
+            for _ in range(3):
+                _, _, cnt = fn()
+            torch.cuda.synchronize()
+            m = int(cnt.item())
+            reps = max(3, min(args.steps, 20))
+            ev0.record(stream)
+            for _ in range(reps):
+                fn()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            t = ev0.elapsed_time(ev1) / 1e3 / reps
+            b = n * (8 if name == "reduce_by_key" else 4) + m * 8 + 8
+            res[f"{name}_L{mean}"] = {"ms": round(t * 1000, 4), "gbs": round(b / t / 1e9, 2),
+                                       "gpairs_per_s": round(n / t / 1e9, 3), "runs": m,
+                                       "algorithmic_bytes": b}
+        del kt
+    return res
+
+
+PROFILE_CASES = ("rbk_f32_L16", "rle_L16", "select_flagged", "partition_flagged")
+
+
+def run_profile_case(args) -> None:
+    """Launch one kernel case ``args.steps`` times after one warm-up launch and
+    print one short JSON line: the entry point for ncu captures of a single
+    kernel (the cases are the ones the extra bench legs time)."""
+    import torch
+    from prefix_scan_gb300 import api, inputs
+    dev = torch.device("cuda", 0)
+    case = args.profile_case
+    if case in ("rbk_f32_L16", "rle_L16"):
+        n = args.n or 1 << 25
+        kt = torch.from_numpy(inputs.run_keys(n, 16, 27)).to(dev)
+        vt = torch.from_numpy(inputs.uniform_f32(n, 12)).to(dev)
+        ws = torch.zeros(api.reduce_by_key_workspace_size(torch.int32, n), dtype=torch.uint8, device=dev)
+        uk, agg = torch.empty_like(kt), torch.empty_like(vt)
+        if case == "rbk_f32_L16":
+            fn = lambda: api.reduce_by_key(kt, vt, unique_keys=uk, aggregates=agg, workspace=ws)[2]
+        else:
+            fn = lambda: api.run_length_encode(kt, unique_keys=uk, counts=agg.view(torch.int32), workspace=ws)[2]
+    else:
+        n = args.n or 1 << 28
+        x = torch.from_numpy(inputs.full_range_i32(n, 8)).to(dev)
+        f = torch.from_numpy(inputs.bernoulli_half(n, 3).astype(np.uint8)).to(dev)
+        ws = api.alloc_workspace(torch.int32, n, dev)
+        out = torch.empty_like(x)
+        sel = api.select if case == "select_flagged" else api.partition
+        fn = lambda: sel(x, f, out=out, workspace=ws)[1]
+    cnt = fn()
+    for _ in range(args.steps):
+        cnt = fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": case, "n": n, "launches": args.steps + 1, "count": int(cnt.item()),
+                      "status": api.device_status(ws)}), flush=True)
+
+
 def run_ops(args, n: int = 1 << 28) -> dict:
     """Running max / min of int32 (uniform full range) and the fp32 sum of the
     deterministic mode at 2^28, GB/s with 2n*4 bytes."""
@@ -618,12 +699,18 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="also time every workload (extra key)")
     ap.add_argument("--compaction", action="store_true", help="also time select / partition at 2^28")
     ap.add_argument("--ops", action="store_true", help="also time max / min and the deterministic mode at 2^28")
+    ap.add_argument("--rbk", action="store_true", help="also time reduce-by-key / run-length encoding at 2^25")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
+                    help="only launch this kernel case --steps times (for ncu captures)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-sample", type=int, default=1 << 25)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()

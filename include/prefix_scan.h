@@ -251,6 +251,55 @@ ps_status ps_partition(ps_dtype dtype, ps_select_op op, const void *in, const ui
                        void *ws, size_t ws_bytes, ps_stream_t stream);
 
 /*
+ * Single-pass reduce-by-key and run-length encoding: the other fused
+ * workloads of the decoupled look-back paper (Merrill & Garland, "Single-pass
+ * Parallel Prefix Scan with Decoupled Look-back", A5 results on
+ * reduce-by-key and run-length-encode), computed as one scan over (run
+ * count, value since the run began) pairs under the segmented-sum operator
+ * -- associative, not commutative, which the method allows (section 4.2:
+ * only contiguous partials are ever combined).
+ *
+ * A run is a maximal stretch of consecutive keys with equal bits (fp32 keys
+ * compare as their 32-bit patterns: -0.0 and +0.0 are different keys, two
+ * NaNs with the same bits are one).  For the j-th run, in input order:
+ *     unique_keys[j] = its key,
+ *     aggregates[j]  = the sum of its values (ps_reduce_by_key; int32 values
+ *                      wrap modulo 2^32, fp32 values add in fp32 in an order
+ *                      the caller cannot choose), or its length
+ *                      (ps_run_length_encode; 32-bit unsigned count stored in
+ *                      an int32 slot).
+ * *num_runs (device, may be NULL) receives the number of runs m; entries m
+ * and beyond of both outputs are left untouched, so each output needs room
+ * for n entries when m is not known in advance.
+ *
+ *   key_dtype    PS_INT32, PS_INT64 or PS_FLOAT32 (keys are only compared).
+ *   value_dtype  PS_INT32 or PS_FLOAT32 (ps_reduce_by_key only).
+ *   keys, values device arrays of n elements (naturally aligned; 16-byte
+ *                alignment of both selects the bulk-copy fast path).
+ *   unique_keys  device, n entries of key_dtype; aggregates: n entries of
+ *                value_dtype (int32 for run-length encoding).  Neither output
+ *                may overlap an input, the other output, the workspace or
+ *                num_runs (PS_ERR_OVERLAP): unlike select, reduce-by-key is
+ *                not computed in place.
+ *   ws           at least ps_reduce_by_key_workspace_size(key_dtype, n)
+ *                bytes, 16-byte aligned, zero-filled once before first use
+ *                (ps_workspace_init); the same conventions as the scans.
+ *   n            below 2^32; n == 0 writes *num_runs = 0 and nothing else.
+ * Errors: PS_ERR_INVALID_ARG for a bad dtype, NULL array with n > 0,
+ * misaligned pointer or n >= 2^32; PS_ERR_WORKSPACE_TOO_SMALL; PS_ERR_OVERLAP;
+ * PS_ERR_CUDA if the launch fails.  Device-side failures (a look-back that
+ * gave up) are reported by ps_get_device_status.
+ */
+size_t ps_reduce_by_key_workspace_size(ps_dtype key_dtype, size_t n);
+ps_status ps_reduce_by_key(ps_dtype key_dtype, ps_dtype value_dtype, const void *keys,
+                           const void *values, void *unique_keys, void *aggregates,
+                           uint64_t *num_runs, size_t n, void *ws, size_t ws_bytes,
+                           ps_stream_t stream);
+ps_status ps_run_length_encode(ps_dtype key_dtype, const void *keys, void *unique_keys,
+                               int32_t *counts, uint64_t *num_runs, size_t n, void *ws,
+                               size_t ws_bytes, ps_stream_t stream);
+
+/*
  * Waits for `stream`, then reads into *out the device-side status of the
  * last scan that used `ws`: PS_OK, PS_ERR_LOOKBACK_TIMEOUT, or
  * PS_ERR_WORKSPACE_NOT_INITIALIZED (the workspace was never zero-filled).

@@ -198,6 +198,67 @@ def partition(x: torch.Tensor, flags: torch.Tensor | None = None, *, op: str | N
     return _compact(True, x, flags, op, threshold, out, False, workspace, stream)
 
 
+def reduce_by_key_workspace_size(key_dtype: torch.dtype, n: int) -> int:
+    return int(_lib.load().ps_reduce_by_key_workspace_size(dtype_code(key_dtype), n))
+
+
+def _runs(keys: torch.Tensor, values, unique_keys, aggregates, workspace, stream):
+    if not keys.is_cuda or keys.dim() != 1 or not keys.is_contiguous():
+        raise ValueError("reduce_by_key: keys must be a contiguous 1-D CUDA tensor")
+    n = keys.numel()
+    kcode = dtype_code(keys.dtype)
+    if values is not None:
+        if (not values.is_cuda or values.dim() != 1 or not values.is_contiguous() or values.numel() != n
+                or values.dtype not in (torch.int32, torch.float32)):
+            raise ValueError("reduce_by_key: values must be a contiguous int32/fp32 CUDA tensor "
+                             "of the keys' length")
+    adt = values.dtype if values is not None else torch.int32
+    if unique_keys is None:
+        unique_keys = torch.empty_like(keys)
+    if aggregates is None:
+        aggregates = torch.empty(n, dtype=adt, device=keys.device)
+    if unique_keys.dtype != keys.dtype or unique_keys.numel() < n or aggregates.dtype != adt or aggregates.numel() < n:
+        raise ValueError("reduce_by_key: outputs need n entries of the key / aggregate dtype")
+    num_runs = torch.zeros(1, dtype=torch.int64, device=keys.device)
+    lib = _lib.load()
+    if workspace is None:
+        need = int(lib.ps_reduce_by_key_workspace_size(kcode, n))
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=keys.device)
+    sh = _stream_handle(stream, keys.device)
+    ptr = (lambda t: t.data_ptr() if n else None)
+    if values is None:
+        st = lib.ps_run_length_encode(kcode, ptr(keys), ptr(unique_keys), ptr(aggregates), num_runs.data_ptr(),
+                                      n, workspace.data_ptr(), workspace.numel(), sh)
+        _lib.check("ps_run_length_encode", st)
+    else:
+        st = lib.ps_reduce_by_key(kcode, dtype_code(values.dtype), ptr(keys), ptr(values), ptr(unique_keys),
+                                  ptr(aggregates), num_runs.data_ptr(), n, workspace.data_ptr(),
+                                  workspace.numel(), sh)
+        _lib.check("ps_reduce_by_key", st)
+    return unique_keys, aggregates, num_runs
+
+
+def reduce_by_key(keys: torch.Tensor, values: torch.Tensor, *, unique_keys: torch.Tensor | None = None,
+                  aggregates: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                  stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Single-pass reduce-by-key: for each run of consecutive bitwise-equal
+    keys, its key and the sum of its values.  Returns (unique_keys,
+    aggregates, num_runs): full-length outputs whose first ``num_runs``
+    entries are defined; ``num_runs`` is a one-element int64 CUDA tensor
+    (no host synchronisation here)."""
+    if values is None:
+        raise ValueError("reduce_by_key: values are required (run_length_encode counts runs)")
+    return _runs(keys, values, unique_keys, aggregates, workspace, stream)
+
+
+def run_length_encode(keys: torch.Tensor, *, unique_keys: torch.Tensor | None = None,
+                      counts: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Single-pass run-length encoding: (unique_keys, counts, num_runs) as
+    for :func:`reduce_by_key`, with int32 run lengths."""
+    return _runs(keys, None, unique_keys, counts, workspace, stream)
+
+
 def host_staging_size(dtype: torch.dtype, n: int) -> int:
     return int(_lib.load().ps_scan_host_staging_size(dtype_code(dtype), n))
 

@@ -132,6 +132,46 @@ ps_status compact(bool partition, ps_dtype dt, int op, const void *in, const uin
     return e == cudaSuccess ? PS_OK : cuda_fail(e);
 }
 
+ps_status reduce_by_key(ps_dtype kdt, ps_dtype vdt, bool rle, const void *keys, const void *vals,
+                        void *ukeys, void *aggs, uint64_t *num_runs, size_t n, void *ws,
+                        size_t ws_bytes, cudaStream_t s) {
+    if (!valid_dtype(kdt) || (vdt != PS_INT32 && vdt != PS_FLOAT32)) return PS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(num_runs) % 8 != 0) return PS_ERR_INVALID_ARG;
+    if (n == 0) {
+        if (num_runs == nullptr) return PS_OK;
+        const cudaError_t e = cudaMemsetAsync(num_runs, 0, sizeof(uint64_t), s);
+        return e == cudaSuccess ? PS_OK : cuda_fail(e);
+    }
+    if (n > 0xffffffffull) return PS_ERR_INVALID_ARG;   // 32-bit run counts
+    if (keys == nullptr || ukeys == nullptr || aggs == nullptr || ws == nullptr || (!rle && vals == nullptr))
+        return PS_ERR_INVALID_ARG;
+    const size_t kes = ps::elem_bytes(kdt);
+    if ((reinterpret_cast<uintptr_t>(keys) | reinterpret_cast<uintptr_t>(ukeys)) % kes != 0 ||
+        (reinterpret_cast<uintptr_t>(vals) | reinterpret_cast<uintptr_t>(aggs)) % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(ws) % 16 != 0)
+        return PS_ERR_INVALID_ARG;
+    if (ps::rbk_num_tiles(kdt, n) > (size_t)INT_MAX) return PS_ERR_INVALID_ARG;
+    const size_t wsb = ps::rbk_workspace_bytes(kdt, n);
+    if (ws_bytes < wsb) return PS_ERR_WORKSPACE_TOO_SMALL;
+    const size_t kb = n * kes, vb = n * 4;
+    struct Range { const void *p; size_t b; };
+    const Range ins[] = {{keys, kb}, {rle ? nullptr : vals, vb}};
+    const Range outs[] = {{ukeys, kb}, {aggs, vb}, {ws, wsb}, {num_runs, num_runs ? 8u : 0u}};
+    for (const Range &o : outs) {
+        if (o.p == nullptr) continue;
+        for (const Range &i : ins)
+            if (i.p && ranges_overlap(o.p, o.b, i.p, i.b)) return PS_ERR_OVERLAP;
+        for (const Range &o2 : outs)
+            if (&o2 != &o && o2.p && ranges_overlap(o.p, o.b, o2.p, o2.b)) return PS_ERR_OVERLAP;
+    }
+    const bool bulk = ((reinterpret_cast<uintptr_t>(keys) | reinterpret_cast<uintptr_t>(rle ? nullptr : vals)) & 15u) == 0;
+    ps::RbkArgs a{keys, rle ? nullptr : vals, ukeys, aggs, (unsigned long long)n,
+                  static_cast<unsigned char *>(ws), (unsigned long long)(ws_bytes & ~(size_t)7),
+                  reinterpret_cast<unsigned long long *>(num_runs), ps::kDefaultMaxPolls, bulk ? 1 : 0};
+    const cudaError_t e = ps::launch_reduce_by_key(a, kdt, vdt, s);
+    return e == cudaSuccess ? PS_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 ps_status ps::scan_seeded(ps_dtype dt, int exclusive, const void *in, void *out, size_t n,
@@ -228,6 +268,26 @@ ps_status ps_partition(ps_dtype dtype, ps_select_op op, const void *in, const ui
                        size_t ws_bytes, ps_stream_t stream) {
     return compact(true, dtype, (int)op, in, flags, threshold, out, num_selected, n, ws, ws_bytes,
                    (cudaStream_t)stream);
+}
+
+size_t ps_reduce_by_key_workspace_size(ps_dtype key_dtype, size_t n) {
+    if (!valid_dtype(key_dtype)) return 0;
+    return ps::rbk_workspace_bytes(key_dtype, n);
+}
+
+ps_status ps_reduce_by_key(ps_dtype key_dtype, ps_dtype value_dtype, const void *keys,
+                           const void *values, void *unique_keys, void *aggregates,
+                           uint64_t *num_runs, size_t n, void *ws, size_t ws_bytes,
+                           ps_stream_t stream) {
+    return reduce_by_key(key_dtype, value_dtype, false, keys, values, unique_keys, aggregates, num_runs,
+                         n, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+ps_status ps_run_length_encode(ps_dtype key_dtype, const void *keys, void *unique_keys,
+                               int32_t *counts, uint64_t *num_runs, size_t n, void *ws,
+                               size_t ws_bytes, ps_stream_t stream) {
+    return reduce_by_key(key_dtype, PS_INT32, true, keys, nullptr, unique_keys, counts, num_runs, n, ws,
+                         ws_bytes, (cudaStream_t)stream);
 }
 
 ps_status ps_workspace_init(void *ws, size_t ws_bytes, ps_stream_t stream) {

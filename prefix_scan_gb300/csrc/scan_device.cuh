@@ -199,6 +199,7 @@ __device__ __forceinline__ unsigned long long highest_of(unsigned long long) { r
 __device__ __forceinline__ float highest_of(float) { return __int_as_float(0x7f800000); }  // +inf
 
 struct OpSum {
+    static constexpr bool kCommutative = true;
     template <typename U> static __device__ __forceinline__ U identity() { return U(0); }
     template <typename U> static __device__ __forceinline__ U combine(U a, U b) { return a + b; }
 };
@@ -206,10 +207,12 @@ struct OpSum {
 // maximum (minimum) of the non-NaN elements and the identity when there is
 // none; exact, associative and commutative.
 struct OpMax {
+    static constexpr bool kCommutative = true;
     template <typename U> static __device__ __forceinline__ U identity() { return lowest_of(U()); }
     template <typename U> static __device__ __forceinline__ U combine(U a, U b) { return max_of(a, b); }
 };
 struct OpMin {
+    static constexpr bool kCommutative = true;
     template <typename U> static __device__ __forceinline__ U identity() { return highest_of(U()); }
     template <typename U> static __device__ __forceinline__ U combine(U a, U b) { return min_of(a, b); }
 };
@@ -243,6 +246,25 @@ template <> __device__ __forceinline__ uint32_t warp_reduce<uint32_t, OpMin>(uin
     return (uint32_t)__reduce_min_sync(kFull, (int)v);
 }
 template <typename U> __device__ __forceinline__ U warp_sum(U v) { return warp_reduce<U, OpSum>(v); }
+
+// Reduction of a look-back window, in which lane l holds the part l places
+// before lane 0's: the result, in every lane, is
+//     v[31] (+) v[30] (+) ... (+) v[0].
+// Commutative operators take the butterfly; the others fold towards lane 0
+// with each step's farther (earlier) partial on the left, then broadcast.
+template <typename U, typename Op> __device__ __forceinline__ U warp_reduce_window(U v) {
+    if constexpr (Op::kCommutative) {
+        return warp_reduce<U, Op>(v);
+    } else {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const U o = __shfl_down_sync(kFull, v, d);
+            if (lane + d < 32) v = Op::combine(o, v);
+        }
+        return __shfl_sync(kFull, v, 0);
+    }
+}
 
 // Sleep between polls of a descriptor that is not ready yet.
 __device__ __forceinline__ void poll_backoff(uint32_t polls) {
@@ -330,7 +352,7 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
 #pragma unroll
             for (int j = K - 1; j >= 0; --j)   // farther tiles on the left
                 if (lane * K + j <= limit) part = Op::combine(v[j], part);
-            excl = Op::combine(warp_reduce<U, Op>(part), excl);
+            excl = Op::combine(warp_reduce_window<U, Op>(part), excl);
             done = (mp != 0u);
             break;
         }

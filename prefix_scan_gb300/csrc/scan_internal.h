@@ -180,6 +180,37 @@ struct SelectArgs {
 template <typename T>
 cudaError_t launch_select(const SelectArgs &a, int op, bool partition, cudaStream_t s);
 
+// Reduce-by-key / run-length encoding: tiles of 4096 elements for 32-bit
+// keys, 2048 for 64-bit keys (16 KiB of keys plus their 32-bit values per
+// tile), one 16-byte two-word descriptor slot per tile holding the (run
+// count, run value) pair.
+constexpr size_t rbk_tile_elems(ps_dtype key_dt) { return key_dt == PS_INT64 ? 2048 : 4096; }
+constexpr size_t rbk_num_tiles(ps_dtype key_dt, size_t n) {
+    return (n + rbk_tile_elems(key_dt) - 1) / rbk_tile_elems(key_dt);
+}
+constexpr size_t rbk_workspace_bytes(ps_dtype key_dt, size_t n) {
+    if (n == 0) return 0;
+    return kHeaderBytes + round_up(rbk_num_tiles(key_dt, n) * kDescStride64, 256);
+}
+
+struct RbkArgs {
+    const void *keys;
+    const void *vals;                   // null: run-length encoding (every value is 1)
+    void *unique_keys;
+    void *aggs;
+    unsigned long long n;
+    unsigned char *ws;
+    unsigned long long ws_bytes;
+    unsigned long long *num_runs;       // device, may be null
+    uint32_t max_polls;
+    int use_bulk;                       // keys and values 16-byte aligned
+};
+
+// Enqueue a single-pass reduce-by-key (vals != null) or run-length encoding.
+// key_dt: PS_INT32 / PS_FLOAT32 (32-bit keys) or PS_INT64; val_dt: PS_INT32
+// or PS_FLOAT32.
+cudaError_t launch_reduce_by_key(const RbkArgs &a, ps_dtype key_dt, ps_dtype val_dt, cudaStream_t s);
+
 // Records `e` as the calling thread's last CUDA error (ps_last_cuda_error).
 void note_cuda_error(cudaError_t e);
 

@@ -34,10 +34,50 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
+// try_wait with a suspend-time hint: the thread may be suspended until the
+// phase completes or about `ns` nanoseconds have passed, instead of polling.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(ns) : "memory");
+    return ok != 0;
+}
+// Bounded wait that sleeps in the barrier: tries of up to `ns` nanoseconds
+// each, for at most kMbarSpinCap tries or about two seconds, whichever ends
+// first; false if it ran out.
+constexpr unsigned long long kMbarWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    if (mbar_try_wait_for(bar, parity, ns)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 0; i < kMbarSpinCap; ++i) {
+        if (mbar_try_wait_for(bar, parity, ns)) return true;
+        if ((i & 15u) == 15u && global_ns() - t0 > kMbarWaitLimitNs) return false;
+    }
+    return false;
+}
+
 // Bounded wait for the phase with the given parity; false if it ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     for (uint32_t i = 0; i < kMbarSpinCap; ++i)
         if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// The same for warps whose waits are long and off the critical path: after
+// a few tries each retry sleeps `ns` nanoseconds, so the waiting warp stops
+// taking issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    for (uint32_t i = 0; i < kMbarSpinCap; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i >= 2) __nanosleep(ns);
+    }
     return false;
 }
 __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes,

@@ -172,3 +172,29 @@ def hashes(n: int, seed: int, start: int = 0) -> np.ndarray:
     out = np.empty(n, dtype=np.uint64)
     lib, key = _load(), seed_key(seed)
     return _fill(out, lambda s, c, p: lib.gen_hash_u64(key, start + s, c, p))
+
+
+def run_keys(n: int, mean_len: int, seed: int, dtype=np.int32) -> np.ndarray:
+    """Keys in runs: run lengths i.i.d. uniform in [1, 2*mean_len - 1] (mean
+    ``mean_len``), each run's key an i.i.d. draw of the dtype (full-range
+    int32, 64-bit hash, or fp32 uniform on the [-1, 1) grid), truncated to n.
+    Neighbouring runs share a key only when two draws collide, which merges
+    them into one run."""
+    dtype = np.dtype(dtype)
+    if mean_len < 1:
+        raise ValueError("run_keys: mean_len >= 1")
+    if n == 0:
+        return np.empty(0, dtype=dtype)
+    m = -(-n * 11 // (10 * mean_len)) + 1024          # 10% more runs than needed, on average
+    lens = uniform_int(m, 1, 2 * mean_len - 1, seed, dtype=np.int64)
+    if int(lens.sum()) < n:
+        raise RuntimeError("run_keys: drew too few runs")   # far outside the length distribution
+    if dtype == np.dtype(np.int32):
+        vals = full_range_i32(m, seed + 1)
+    elif dtype == np.dtype(np.int64):
+        vals = hashes(m, seed + 1).view(np.int64)
+    elif dtype == np.dtype(np.float32):
+        vals = uniform_f32(m, seed + 1)
+    else:
+        raise ValueError("run_keys: int32, int64 or float32")
+    return np.repeat(vals, lens)[:n]

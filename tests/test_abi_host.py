@@ -151,3 +151,38 @@ def test_python_layer_refuses_cpu_tensors():
     from prefix_scan_gb300 import api
     with pytest.raises(ValueError, match="CUDA"):
         api.scan_inclusive(torch.arange(10, dtype=torch.int32))
+
+
+def test_reduce_by_key_workspace_size(lib):
+    assert lib.ps_reduce_by_key_workspace_size(0, 0) == 0
+    assert lib.ps_reduce_by_key_workspace_size(7, 10) == 0
+    for code, tile in ((0, 4096), (2, 4096), (1, 2048)):
+        for n in (1, tile, tile + 1, 1 << 30):
+            need = lib.ps_reduce_by_key_workspace_size(code, n)
+            assert need >= 256 + -(-n // tile) * 16 and need % 256 == 0
+
+
+def test_reduce_by_key_argument_errors(lib, no_device):
+    n = 10_000
+    ws = lib.ps_reduce_by_key_workspace_size(0, n)
+    K, V, UK, AG, W, C = FAKE, FAKE + (1 << 20), FAKE + (2 << 20), FAKE + (3 << 20), FAKE + (4 << 20), FAKE + (5 << 20)
+    f = lib.ps_reduce_by_key
+    r = lib.ps_run_length_encode
+    assert f(0, 0, None, None, None, None, None, 0, None, 0, None) == _lib.PS_OK        # n == 0, no count
+    assert f(0, 1, K, V, UK, AG, C, n, W, ws, None) == _lib.PS_ERR_INVALID_ARG         # int64 values
+    assert f(9, 0, K, V, UK, AG, C, n, W, ws, None) == _lib.PS_ERR_INVALID_ARG
+    assert f(0, 0, K, None, UK, AG, C, n, W, ws, None) == _lib.PS_ERR_INVALID_ARG      # no values
+    assert f(0, 0, K + 2, V, UK, AG, C, n, W, ws, None) == _lib.PS_ERR_INVALID_ARG     # misaligned key
+    assert f(0, 0, K, V, UK, AG, C + 4, n, W, ws, None) == _lib.PS_ERR_INVALID_ARG     # misaligned count
+    assert f(0, 0, K, V, UK, AG, C, 1 << 32, W, ws, None) == _lib.PS_ERR_INVALID_ARG   # n >= 2^32
+    assert f(0, 0, K, V, UK, AG, C, n, W, ws - 1, None) == _lib.PS_ERR_WORKSPACE_TOO_SMALL
+    assert f(0, 0, K, V, K + 400, AG, C, n, W, ws, None) == _lib.PS_ERR_OVERLAP        # keys out in keys
+    assert f(0, 0, K, V, UK, V, C, n, W, ws, None) == _lib.PS_ERR_OVERLAP              # in place values
+    assert f(0, 0, K, V, UK, UK + 8, C, n, W, ws, None) == _lib.PS_ERR_OVERLAP         # outputs overlap
+    assert f(0, 0, K, V, UK, AG, AG + 64, n, W, ws, None) == _lib.PS_ERR_OVERLAP       # count in output
+    assert f(0, 0, K, V, UK, AG, C, n, UK + 1024, ws, None) == _lib.PS_ERR_OVERLAP     # workspace in output
+    assert r(0, K, UK, AG, C, n, W, ws - 1, None) == _lib.PS_ERR_WORKSPACE_TOO_SMALL
+    assert r(0, K, K, AG, C, n, W, ws, None) == _lib.PS_ERR_OVERLAP
+    ws64 = lib.ps_reduce_by_key_workspace_size(1, n)
+    assert ws64 > ws
+    assert r(1, K + 4, UK, AG, C, n, W, ws64, None) == _lib.PS_ERR_INVALID_ARG         # int64 keys, 4-aligned
