@@ -203,13 +203,18 @@ def replica_stats(local_seconds: float, local_units: float, world: int) -> tuple
 KERNEL_TRAFFIC_FILE = ROOT / "profiles" / "persistent_kernel_i32_excl_2p28_traffic.md"
 
 
+# The headline kernel's translation unit and the headers it includes: a
+# change anywhere else leaves its recorded DRAM traffic valid.
+HEADLINE_KERNEL_SOURCES = ("scan_device.cuh", "scan_internal.h", "scan_persistent.cu", "scan_pipeline.cuh")
+
+
 def kernel_sources_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = ROOT / "prefix_scan_gb300" / "csrc"
-    for p in sorted(list(csrc.glob("*.cu")) + list(csrc.glob("*.cuh")) + list(csrc.glob("*.h"))):
-        h.update(p.name.encode())
-        h.update(p.read_bytes())
+    for name in HEADLINE_KERNEL_SOURCES:
+        h.update(name.encode())
+        h.update((csrc / name).read_bytes())
     return h.hexdigest()
 
 
