@@ -87,6 +87,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, sz, vp, vp, vp]
         fn.restype = sz
+    lib.oracle_scan_pair_i32_f32.argtypes = [vp, vp, sz, ctypes.c_int, vp, vp, vp]
+    lib.oracle_scan_pair_i32_f32.restype = None
+    lib.oracle_scan_affine_f32.argtypes = [vp, vp, sz, ctypes.c_int, vp, vp, vp, vp]
+    lib.oracle_scan_affine_f32.restype = None
     return lib
 
 
@@ -226,3 +230,38 @@ def reduce_by_key(keys: np.ndarray, values: np.ndarray | None = None,
     oa = np.empty(n, dtype=np.float64)
     m = getattr(lib, f"oracle_rbk_b{bits}_f32")(_ptr(kraw), _ptr(vals), n, _ptr(okeys), _ptr(ov), _ptr(oa))
     return okeys[:m].view(keys.dtype), ov[:m], oa[:m]
+
+
+# ---- pair scans ------------------------------------------------------------------
+
+
+def scan_pair_i32_f32(xi: np.ndarray, xf: np.ndarray, exclusive: bool = False,
+                      lib: ctypes.CDLL | None = None):
+    """{int32, fp32} pairs summed field by field: (int32 sums mod 2^32,
+    float64 sums, float64 running sums of |f|)."""
+    lib = lib if lib is not None else load()
+    xi = np.ascontiguousarray(xi, dtype=np.int32)
+    xf = np.ascontiguousarray(xf, dtype=np.float32)
+    n = xi.shape[0]
+    if xf.shape[0] != n:
+        raise ValueError("oracle: pair fields differ in length")
+    yi = np.empty(n, dtype=np.int32)
+    yf = np.empty(n, dtype=np.float64)
+    ya = np.empty(n, dtype=np.float64)
+    lib.oracle_scan_pair_i32_f32(_ptr(xi), _ptr(xf), n, int(exclusive), _ptr(yi), _ptr(yf), _ptr(ya))
+    return yi, yf, ya
+
+
+def scan_affine_f32(a: np.ndarray, b: np.ndarray, exclusive: bool = False,
+                    lib: ctypes.CDLL | None = None):
+    """Composition of the maps x -> a_k x + b_k in input order: (A, B, |A|,
+    |B|-scale), all float64."""
+    lib = lib if lib is not None else load()
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    n = a.shape[0]
+    if b.shape[0] != n:
+        raise ValueError("oracle: map fields differ in length")
+    out = [np.empty(n, dtype=np.float64) for _ in range(4)]
+    lib.oracle_scan_affine_f32(_ptr(a), _ptr(b), n, int(exclusive), *[_ptr(o) for o in out])
+    return tuple(out)

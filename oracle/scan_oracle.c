@@ -7,8 +7,8 @@
  * the CUDA library.
  *
  * What it computes is the plain definition of the scan (and, further down,
- * of stream compaction, running maximum / minimum and reduce-by-key / run-
- * length encoding) and nothing else:
+ * of stream compaction, running maximum / minimum, reduce-by-key / run-
+ * length encoding and the pair scans) and nothing else:
  *
  *   inclusive  y[i] = x[0] + x[1] + ... + x[i]
  *       ("Prefix Sum" definition, page "CUDA-Operators-6-Cumsum", section 1;
@@ -371,4 +371,67 @@ size_t oracle_rbk_b64_f32(const uint64_t *keys, const float *vals, size_t n, uin
         oabs[m - 1] = aacc;
     }
     return m;
+}
+
+/* ---- scans of 8-byte pair elements ----------------------------------------
+ *
+ * The paper summary's evaluation data include {int32, fp32} pairs (A4) and
+ * section 4.2 allows any associative operator, commutative or not.  Two
+ * pair scans, each its plain sequential definition:
+ *
+ * {int32, fp32} pairs, summed field by field: the int32 field wraps modulo
+ * 2^32, the fp32 field is summed in double (with the running sum of |f| that
+ * scales the accepted fp32 error).
+ */
+void oracle_scan_pair_i32_f32(const int32_t *xi, const float *xf, size_t n, int exclusive,
+                              int32_t *yi, double *yf, double *yabs)
+{
+    uint32_t si = 0u;
+    double sf = 0.0, sa = 0.0;
+    for (size_t k = 0; k < n; ++k) {
+        if (exclusive) {
+            yi[k] = (int32_t)si;
+            yf[k] = sf;
+            yabs[k] = sa;
+        }
+        si += (uint32_t)xi[k];
+        sf += (double)xf[k];
+        sa += fabs((double)xf[k]);
+        if (!exclusive) {
+            yi[k] = (int32_t)si;
+            yf[k] = sf;
+            yabs[k] = sa;
+        }
+    }
+}
+
+/* Affine maps f_k(x) = a_k x + b_k, composed in input order: output k is
+ * F_k = f_k o ... o f_0 (exclusive: f_{k-1} o ... o f_0, the identity map
+ * for k = 0), F_k(x) = A_k x + B_k, carried in double.  Beside A and B the
+ * same recurrence over |a|, |b| gives the magnitudes |A|, sum_j |b_j| prod |a|
+ * that scale the accepted fp32 error.  With y_{-1} = 0, B_k is the k-th term
+ * of the recurrence y_k = a_k y_{k-1} + b_k. */
+void oracle_scan_affine_f32(const float *a, const float *b, size_t n, int exclusive, double *ya,
+                            double *yb, double *ya_abs, double *yb_abs)
+{
+    double A = 1.0, B = 0.0, Aa = 1.0, Ba = 0.0;
+    for (size_t k = 0; k < n; ++k) {
+        if (exclusive) {
+            ya[k] = A;
+            yb[k] = B;
+            ya_abs[k] = Aa;
+            yb_abs[k] = Ba;
+        }
+        const double ak = (double)a[k], bk = (double)b[k];
+        A = ak * A;
+        B = ak * B + bk;
+        Aa = fabs(ak) * Aa;
+        Ba = fabs(ak) * Ba + fabs(bk);
+        if (!exclusive) {
+            ya[k] = A;
+            yb[k] = B;
+            ya_abs[k] = Aa;
+            yb_abs[k] = Ba;
+        }
+    }
 }

@@ -406,12 +406,66 @@ def pin_rbk_closed_forms(lib):
     assert cnt.tolist() == [1, 2, 2, 1]
 
 
+# ---- pair-scan pins --------------------------------------------------------------
+
+def pin_pair_fields_match_scalar_scans(lib):
+    # each field of the pair scan is the scalar scan of that field (the
+    # scalar scans are pinned above, by other code)
+    n = 300_007
+    xi = inputs.full_range_i32(n, 101)
+    xf = inputs.uniform_f32(n, 102)
+    for excl in (False, True):
+        yi, yf, ya = oracle.scan_pair_i32_f32(xi, xf, excl, lib)
+        assert np.array_equal(yi, oracle.exclusive(xi) if excl else oracle.inclusive(xi))
+        assert np.array_equal(yf, oracle.exclusive(xf) if excl else oracle.inclusive(xf))
+        assert np.array_equal(ya, oracle.abs_prefix(xf, excl))
+
+
+def pin_affine_closed_forms(lib):
+    n = 5000
+    b = inputs.uniform_f32(n, 103)
+    ones = np.ones(n, dtype=np.float32)
+    A, B, Aa, Ba = oracle.scan_affine_f32(ones, b, False, lib)
+    assert np.all(A == 1.0) and np.allclose(B, np.cumsum(b.astype(np.float64)), rtol=0, atol=1e-9)
+    a = (inputs.uniform_int(n, 1, 99, 104).astype(np.float32) / 64)
+    A, B, _, _ = oracle.scan_affine_f32(a, np.zeros(n, np.float32), False, lib)
+    assert np.all(B == 0.0)
+    logA = np.cumsum(np.log(a.astype(np.float64)))
+    ok = np.abs(logA) < 600
+    assert np.allclose(np.log(A[ok]), logA[ok], rtol=0, atol=1e-9)
+    r = np.float32(0.75)   # a = r, b = 1: B_k = (1 - r^(k+1)) / (1 - r)
+    k = np.arange(200)
+    A, B, _, _ = oracle.scan_affine_f32(np.full(200, r), np.ones(200, np.float32), False, lib)
+    assert np.allclose(B, (1 - 0.75 ** (k + 1)) / 0.25, rtol=1e-12, atol=0)
+    assert np.allclose(A, 0.75 ** (k + 1), rtol=1e-12, atol=0)
+    # exclusive: the identity map first, then the inclusive result shifted
+    Ae, Be, _, _ = oracle.scan_affine_f32(np.full(200, r), np.ones(200, np.float32), True, lib)
+    assert Ae[0] == 1.0 and Be[0] == 0.0 and np.array_equal(Ae[1:], A[:-1]) and np.array_equal(Be[1:], B[:-1])
+
+
+def pin_affine_brute_force_iteration(lib):
+    # F_k(x) = A_k x + B_k must equal applying the maps one by one to x
+    rng = np.random.default_rng(105)
+    a = rng.uniform(-1.5, 1.5, 60).astype(np.float32)
+    b = rng.uniform(-1, 1, 60).astype(np.float32)
+    A, B, Aa, Ba = oracle.scan_affine_f32(a, b, False, lib)
+    for x0 in (0.0, 1.0, -2.5):
+        y = x0
+        for k in range(60):
+            y = float(a[k]) * y + float(b[k])
+            assert abs((A[k] * x0 + B[k]) - y) <= 1e-12 * (1 + abs(y))
+    # the magnitudes: the same recurrence over |a|, |b|
+    assert np.allclose(Ba, oracle.scan_affine_f32(np.abs(a), np.abs(b), False, lib)[1], rtol=1e-15, atol=0)
+    assert np.allclose(Aa, np.abs(A), rtol=1e-15, atol=0)
+
+
 PINS = [pin_worked_examples, pin_fig6_snapshot, pin_brute_force_int, pin_brute_force_f32,
         pin_abs_prefix, pin_closed_forms, pin_wraparound, pin_library_crosscheck,
         pin_invariants, pin_degenerate, pin_select_brute_force, pin_select_library_crosscheck,
         pin_select_closed_forms, pin_flags_predicates, pin_scan_op_brute_force,
         pin_scan_op_library_crosscheck, pin_scan_op_closed_forms, pin_rbk_brute_force,
-        pin_rbk_numpy_crosscheck, pin_rbk_closed_forms]
+        pin_rbk_numpy_crosscheck, pin_rbk_closed_forms, pin_pair_fields_match_scalar_scans,
+        pin_affine_closed_forms, pin_affine_brute_force_iteration]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -450,6 +504,10 @@ MUTANTS = [
      "if (i == 0 || keys[i] < keys[i - 1]) {"),                                  # runs only on descent
     ("oracle_rbk_b64_i32", "        acc += v;\n", "        acc = v;\n"),           # keeps last value
     ("oracle_rbk_b32_f32", "aacc += fabs((double)vals[i]);", "aacc += (double)vals[i];"),  # dropped abs
+    ("oracle_scan_pair_i32_f32", "sf += (double)xf[k];", "sf += (double)xi[k];"),            # wrong field
+    ("oracle_scan_affine_f32", "B = ak * B + bk;", "B = A * B + bk;"),                        # wrong factor
+    ("oracle_scan_affine_f32", "A = ak * A;", "A = ak + A;"),                                 # sum for product
+    ("oracle_scan_affine_f32", "Ba = fabs(ak) * Ba + fabs(bk);", "Ba = Ba + fabs(bk);"),      # dropped factor
 ]
 
 
