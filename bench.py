@@ -660,8 +660,10 @@ def run_profile_case(args) -> None:
 
 
 def run_ops(args, n: int = 1 << 28) -> dict:
-    """Running max / min of int32 (uniform full range) and the fp32 sum of the
-    deterministic mode at 2^28, GB/s with 2n*4 bytes."""
+    """Running max / min of int32 (uniform full range), the fp32 sum of the
+    deterministic mode at 2^28, and the {int32, fp32} pair sum and fp32
+    affine-map composition over 2^27 8-byte elements (the same bytes); GB/s
+    with one read and one write of every element."""
     import torch
     from prefix_scan_gb300 import api, inputs
     dev = torch.device("cuda", 0)
@@ -672,10 +674,19 @@ def run_ops(args, n: int = 1 << 28) -> dict:
     stream = torch.cuda.current_stream(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     res = {"n": n}
+    n8 = n // 2   # 8-byte elements: the same bytes as the int32 cases
+    p8 = torch.empty((n8, 2), dtype=torch.int32, device=dev)
+    p8[:, 0] = torch.from_numpy(inputs.full_range_i32(n8, 13)).to(dev)
+    p8[:, 1] = torch.from_numpy(inputs.uniform_f32(n8, 14).view(np.int32)).to(dev)
+    f8 = torch.from_numpy(np.stack([inputs.uniform_f32(n8, 15), inputs.uniform_f32(n8, 16)], axis=1)).to(dev)
+    o8 = torch.empty_like(p8)
+    ws8 = api.alloc_workspace(torch.int64, n8, dev)
     cases = (("max_int32", lambda: api.scan(x, op="max", out=out, workspace=ws)),
              ("min_int32", lambda: api.scan(x, op="min", out=out, workspace=ws)),
              ("sum_fp32_deterministic", lambda: api.scan(xf, out=out.view(torch.float32), workspace=ws,
-                                                         algo="deterministic")))
+                                                         algo="deterministic")),
+             ("pair_i32_f32_sum", lambda: api.scan_pairs(p8, out=o8, workspace=ws8)),
+             ("affine_f32_compose", lambda: api.scan_affine(f8, out=o8.view(torch.float32), workspace=ws8)))
     for name, fn in cases:
         for _ in range(3):
             fn()

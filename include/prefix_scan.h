@@ -251,6 +251,40 @@ ps_status ps_partition(ps_dtype dtype, ps_select_op op, const void *in, const ui
                        void *ws, size_t ws_bytes, ps_stream_t stream);
 
 /*
+ * Scans of 8-byte pair elements.  The decoupled look-back applies the
+ * reduction operator only to contiguous inputs or partials (Merrill &
+ * Garland, "Single-pass Parallel Prefix Scan with Decoupled Look-back",
+ * section 4.2), so any associative operator works, commutative or not; the
+ * paper's evaluation data include {int32, fp32} pairs (section A4).
+ *
+ * ps_scan_pair_i32_f32: field-wise sums, out[k] = {sum of in[0..k].i modulo
+ * 2^32, sum of in[0..k].f in fp32 (association as in the fp32 scan)}.
+ * ps_scan_affine_f32: each element is the map x -> a x + b; out[k] is the
+ * composition of maps 0..k applied in order (map 0 first):
+ *     out[k] = {a_k A_{k-1},  a_k B_{k-1} + b_k}  (fp32; identity {1, 0}),
+ * so out[k].b is the k-th term of the recurrence y_k = a_k y_{k-1} + b_k
+ * with y_{-1} = 0.  Exclusive: out[0] is the identity and out[k] the
+ * composition of maps 0..k-1.
+ *
+ * Both are ps_scan_* with 8-byte elements: in and out 8-byte aligned
+ * (16-byte alignment of both selects the bulk-copy kernel), out == in scans
+ * in place, partial overlap is PS_ERR_OVERLAP, and the workspace is
+ * ps_scan_workspace_size(PS_INT64, n) bytes with the same conventions.
+ */
+typedef struct ps_pair_i32_f32 {
+    int32_t i;
+    float f;
+} ps_pair_i32_f32;
+typedef struct ps_affine_f32 {
+    float a;
+    float b;
+} ps_affine_f32;
+ps_status ps_scan_pair_i32_f32(int exclusive, const ps_pair_i32_f32 *in, ps_pair_i32_f32 *out, size_t n,
+                               void *ws, size_t ws_bytes, ps_stream_t stream);
+ps_status ps_scan_affine_f32(int exclusive, const ps_affine_f32 *in, ps_affine_f32 *out, size_t n,
+                             void *ws, size_t ws_bytes, ps_stream_t stream);
+
+/*
  * Single-pass reduce-by-key and run-length encoding: the other fused
  * workloads of the decoupled look-back paper (Merrill & Garland, "Single-pass
  * Parallel Prefix Scan with Decoupled Look-back", A5 results on

@@ -50,6 +50,8 @@ PS_OP_SUM, PS_OP_MAX, PS_OP_MIN = 0, 1, 2
 SIGNATURES["ps_select"] = (_int, [_int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp])
 SIGNATURES["ps_partition"] = (_int, [_int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp])
 PS_SELECT_FLAGGED, PS_SELECT_NONZERO, PS_SELECT_GREATER, PS_SELECT_LESS = 0, 1, 2, 3
+SIGNATURES["ps_scan_pair_i32_f32"] = (_int, [_int, _vp, _vp, _sz, _vp, _sz, _vp])
+SIGNATURES["ps_scan_affine_f32"] = (_int, [_int, _vp, _vp, _sz, _vp, _sz, _vp])
 SIGNATURES["ps_reduce_by_key_workspace_size"] = (_sz, [_int, _sz])
 SIGNATURES["ps_reduce_by_key"] = (_int, [_int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp])
 SIGNATURES["ps_run_length_encode"] = (_int, [_int, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp])

@@ -198,6 +198,47 @@ def partition(x: torch.Tensor, flags: torch.Tensor | None = None, *, op: str | N
     return _compact(True, x, flags, op, threshold, out, False, workspace, stream)
 
 
+def _pair_scan(fname: str, x: torch.Tensor, exclusive: bool, out, inplace: bool, workspace, stream):
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError(f"{fname}: input must be a contiguous CUDA tensor")
+    if x.dim() == 2 and x.shape[1] == 2 and x.element_size() == 4:
+        n = x.shape[0]
+    elif x.dim() == 1 and x.element_size() == 8:
+        n = x.shape[0]
+    else:
+        raise ValueError(f"{fname}: expected (n, 2) 32-bit elements or (n,) 8-byte elements")
+    if inplace:
+        out = x
+    elif out is None:
+        out = torch.empty_like(x)
+    if out.data_ptr() != x.data_ptr() and (out.numel() * out.element_size() != n * 8 or not out.is_contiguous()):
+        raise ValueError(f"{fname}: `out` must hold n 8-byte elements")
+    lib = _lib.load()
+    if workspace is None:
+        workspace = alloc_workspace(torch.int64, n, x.device)
+    if n:
+        st = getattr(lib, fname)(int(exclusive), x.data_ptr(), out.data_ptr(), n, workspace.data_ptr(),
+                                 workspace.numel(), _stream_handle(stream, x.device))
+        _lib.check(fname, st)
+    return out
+
+
+def scan_pairs(x: torch.Tensor, *, exclusive: bool = False, out: torch.Tensor | None = None,
+               inplace: bool = False, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Scan of {int32, fp32} pairs summed field by field.  ``x``: an (n,)
+    int64 tensor holding the pairs' bits (int32 field in the low half), or
+    an (n, 2) int32 tensor whose second column holds the fp32 bits."""
+    return _pair_scan("ps_scan_pair_i32_f32", x, exclusive, out, inplace, workspace, stream)
+
+
+def scan_affine(x: torch.Tensor, *, exclusive: bool = False, out: torch.Tensor | None = None,
+                inplace: bool = False, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Composition scan of the fp32 affine maps x -> a x + b given as an
+    (n, 2) float32 tensor of rows (a, b); row k of the result is the
+    composition of maps 0..k (map 0 applied first)."""
+    return _pair_scan("ps_scan_affine_f32", x, exclusive, out, inplace, workspace, stream)
+
+
 def reduce_by_key_workspace_size(key_dtype: torch.dtype, n: int) -> int:
     return int(_lib.load().ps_reduce_by_key_workspace_size(dtype_code(key_dtype), n))
 

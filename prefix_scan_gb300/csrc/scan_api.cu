@@ -48,7 +48,7 @@ ps_status check_args(ps_dtype dt, const void *in, const void *out, size_t n, con
 template <typename T>
 ps_status run(ps_algo algo, bool exclusive, const void *in, void *out, size_t n, void *ws,
               size_t ws_bytes, cudaStream_t s, const void *carry_in = nullptr,
-              void *carry_out = nullptr, ps_op op = PS_OP_SUM) {
+              void *carry_out = nullptr, int op = ps::kOpSum) {
     cudaError_t e;
     unsigned char *w = static_cast<unsigned char *>(ws);
     switch (algo) {
@@ -254,6 +254,24 @@ ps_status ps_scan_op(ps_op op, ps_dtype dtype, int exclusive, const void *in, vo
     case PS_INT64: return run<int64_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes, s, nullptr, nullptr, op);
     default: return run<float>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes, s, nullptr, nullptr, op);
     }
+}
+
+ps_status ps_scan_pair_i32_f32(int exclusive, const ps_pair_i32_f32 *in, ps_pair_i32_f32 *out, size_t n,
+                               void *ws, size_t ws_bytes, ps_stream_t stream) {
+    if (n == 0) return PS_OK;
+    const ps_status st = check_args(PS_INT64, in, out, n, ws, ws_bytes);   // 8-byte elements
+    if (st != PS_OK) return st;
+    return run<int64_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes,
+                        (cudaStream_t)stream, nullptr, nullptr, ps::kOpPairI32F32);
+}
+
+ps_status ps_scan_affine_f32(int exclusive, const ps_affine_f32 *in, ps_affine_f32 *out, size_t n, void *ws,
+                             size_t ws_bytes, ps_stream_t stream) {
+    if (n == 0) return PS_OK;
+    const ps_status st = check_args(PS_INT64, in, out, n, ws, ws_bytes);
+    if (st != PS_OK) return st;
+    return run<int64_t>(PS_ALGO_DECOUPLED_LOOKBACK, exclusive != 0, in, out, n, ws, ws_bytes,
+                        (cudaStream_t)stream, nullptr, nullptr, ps::kOpAffineF32);
 }
 
 ps_status ps_select(ps_dtype dtype, ps_select_op op, const void *in, const uint8_t *flags,

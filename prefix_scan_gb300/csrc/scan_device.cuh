@@ -217,6 +217,35 @@ struct OpMin {
     template <typename U> static __device__ __forceinline__ U combine(U a, U b) { return min_of(a, b); }
 };
 
+// Operators of the two 8-byte pair element types, carried in the int64 lane
+// type (the first field in the low 32 bits, the second in the high 32):
+//   {int32, fp32} pairs, summed field by field (the int32 field wraps);
+//   affine maps x -> a x + b in fp32, {a, b}, composed in sequence order:
+//   combine(earlier, later) is "apply earlier, then later",
+//       (a1, b1) then (a2, b2) = (a2 a1, a2 b1 + b2),
+//   associative but not commutative; the identity is (1, 0).
+__device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
+    return ((unsigned long long)hi << 32) | lo;
+}
+struct OpPairI32F32 {
+    static constexpr bool kCommutative = true;
+    template <typename U> static __device__ __forceinline__ U identity() { return U(0); }
+    template <typename U> static __device__ __forceinline__ U combine(U a, U b) {
+        const uint32_t i = (uint32_t)a + (uint32_t)b;
+        const float f = __uint_as_float((uint32_t)(a >> 32)) + __uint_as_float((uint32_t)(b >> 32));
+        return pack2(i, __float_as_uint(f));
+    }
+};
+struct OpAffineF32 {
+    static constexpr bool kCommutative = false;
+    template <typename U> static __device__ __forceinline__ U identity() { return pack2(0x3f800000u, 0u); }
+    template <typename U> static __device__ __forceinline__ U combine(U e, U l) {
+        const float ea = __uint_as_float((uint32_t)e), eb = __uint_as_float((uint32_t)(e >> 32));
+        const float la = __uint_as_float((uint32_t)l), lb = __uint_as_float((uint32_t)(l >> 32));
+        return pack2(__float_as_uint(la * ea), __float_as_uint(__fmaf_rn(la, eb, lb)));
+    }
+};
+
 // Inclusive Kogge-Stone scan over the 32 lanes with shuffles (the warp scan
 // of the cumsum page, section 2, and of the Kogge-Stone network, Fig. 1b of
 // the paper summary).  The predecessor's partial is the left operand.

@@ -121,6 +121,16 @@ constexpr uint32_t kDefaultMaxPolls = 1u << 21;
 //               reduce-then-scan comparison path; tile id = blockIdx.x).
 enum class Lookback { Decoupled = 0, Chained = 1, Precomputed = 2 };
 
+// Operator of a single-pass scan: the public ps_op values, and the two
+// operators of the 8-byte pair element types (int64_t storage only).
+enum ScanOpCode : int {
+    kOpSum = PS_OP_SUM,
+    kOpMax = PS_OP_MAX,
+    kOpMin = PS_OP_MIN,
+    kOpPairI32F32 = 16,   // {int32, fp32} pairs, field-wise sum
+    kOpAffineF32 = 17     // fp32 affine maps {a, b}, composition
+};
+
 // Launch arguments common to the single-pass kernels.
 struct PassArgs {
     const void *in;
@@ -135,14 +145,14 @@ struct PassArgs {
 
 // Enqueue the persistent TMA-fed single-pass kernel (16-byte aligned in/out).
 template <typename T>
-cudaError_t launch_persistent(const PassArgs &a, bool exclusive, ps_op op, cudaStream_t s);
+cudaError_t launch_persistent(const PassArgs &a, bool exclusive, int op, cudaStream_t s);
 
 // Enqueue one single-pass scan (one kernel; the workspace needs no reset).
 // T is int32_t, int64_t or float.  Decoupled look-back on 16-byte aligned
 // arrays runs the persistent kernel; otherwise one CTA per tile.
 template <typename T>
 cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s,
-                               ps_op op = PS_OP_SUM);
+                               int op = kOpSum);
 
 // Third kernel of reduce-then-scan: tile scan seeded from the workspace.
 template <typename T>

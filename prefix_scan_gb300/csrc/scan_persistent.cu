@@ -149,21 +149,71 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 break;
             }
             const unsigned long long tile_base = (unsigned long long)tile * TILE;
-            U acc = ident;
-            if (tile_base + TILE <= n) {
-                const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE);
+            U agg;
+            if constexpr (Op::kCommutative) {
+                // each lane folds every 32nd vector; the order does not matter
+                U acc = ident;
+                if (tile_base + TILE <= n) {
+                    const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE);
 #pragma unroll 8
-                for (int i = lane; i < (int)(TILE / VEC); i += 32) {
-                    const V x = src[i];
+                    for (int i = lane; i < (int)(TILE / VEC); i += 32) {
+                        const V x = src[i];
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) acc = Op::combine(acc, (U)vget(x, j));
+                        for (int j = 0; j < VEC; ++j) acc = Op::combine(acc, (U)vget(x, j));
+                    }
+                } else {
+                    for (unsigned long long i = tile_base + lane; i < n; i += 32) acc = Op::combine(acc, (U)in[i]);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                agg = warp_reduce<U, Op>(acc);
             } else {
-                for (unsigned long long i = tile_base + lane; i < n; i += 32) acc = Op::combine(acc, (U)in[i]);
+                // in sequence order: lane l folds the l-th 32nd of the tile,
+                // C consecutive vectors, then the lanes' partials are folded
+                // towards lane 0, earlier on the left.  Lane l visits its
+                // vectors starting at r = l mod 8, so that the 8 lanes one
+                // 16-byte shared-memory load serves hit distinct banks: it
+                // folds [r, C) and [0, r) separately and joins them in order.
+                U running = ident;
+                if (tile_base + TILE <= n) {
+                    constexpr int C = (int)(TILE / VEC / 32);
+                    static_assert(C >= 8 && (C & (C - 1)) == 0, "chunk of a power-of-two size >= 8");
+                    const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE) + lane * C;
+                    const int r = lane & 7;
+                    U tail = ident, head = ident;
+#pragma unroll 4
+                    for (int q = 0; q < C; ++q) {
+                        const int vi = (q + r) & (C - 1);
+                        const V x = src[vi];
+                        U p = (U)vget(x, 0);
+#pragma unroll
+                        for (int j = 1; j < VEC; ++j) p = Op::combine(p, (U)vget(x, j));
+                        if (vi >= r) tail = Op::combine(tail, p);
+                        else head = Op::combine(head, p);
+                    }
+                    U p = Op::combine(head, tail);
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const U o = __shfl_down_sync(kFull, p, d);
+                        if (lane + d < 32) p = Op::combine(p, o);
+                    }
+                    running = __shfl_sync(kFull, p, 0);
+                } else {
+                    for (unsigned long long i0 = tile_base; i0 < n; i0 += 32) {
+                        const unsigned long long i = i0 + lane;
+                        U p = i < n ? (U)in[i] : ident;
+#pragma unroll
+                        for (int d = 1; d < 32; d <<= 1) {
+                            const U o = __shfl_down_sync(kFull, p, d);
+                            if (lane + d < 32) p = Op::combine(p, o);
+                        }
+                        running = Op::combine(running, __shfl_sync(kFull, p, 0));
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                agg = running;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            const U agg = warp_reduce<U, Op>(acc);
             if (lane == 0) {
                 if (tile == 0) {
                     // the only read of carry_in: it precedes tile 0's P, hence
@@ -344,20 +394,26 @@ cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <typename T, typename Op>
+static cudaError_t launch_persistent_op(const PassArgs &a, bool exclusive, cudaStream_t s) {
+    return exclusive ? launch_persistent_kind<T, true, Op>(a, s) : launch_persistent_kind<T, false, Op>(a, s);
+}
+
 template <typename T>
-cudaError_t launch_persistent(const PassArgs &a, bool exclusive, ps_op op, cudaStream_t s) {
+cudaError_t launch_persistent(const PassArgs &a, bool exclusive, int op, cudaStream_t s) {
+    if constexpr (sizeof(T) == 8) {   // the pair element types travel as int64 words
+        if (op == kOpPairI32F32) return launch_persistent_op<T, OpPairI32F32>(a, exclusive, s);
+        if (op == kOpAffineF32) return launch_persistent_op<T, OpAffineF32>(a, exclusive, s);
+    }
     switch (op) {
-    case PS_OP_MAX:
-        return exclusive ? launch_persistent_kind<T, true, OpMax>(a, s) : launch_persistent_kind<T, false, OpMax>(a, s);
-    case PS_OP_MIN:
-        return exclusive ? launch_persistent_kind<T, true, OpMin>(a, s) : launch_persistent_kind<T, false, OpMin>(a, s);
-    default:
-        return exclusive ? launch_persistent_kind<T, true, OpSum>(a, s) : launch_persistent_kind<T, false, OpSum>(a, s);
+    case kOpMax: return launch_persistent_op<T, OpMax>(a, exclusive, s);
+    case kOpMin: return launch_persistent_op<T, OpMin>(a, exclusive, s);
+    default: return launch_persistent_op<T, OpSum>(a, exclusive, s);
     }
 }
 
-template cudaError_t launch_persistent<int32_t>(const PassArgs &, bool, ps_op, cudaStream_t);
-template cudaError_t launch_persistent<int64_t>(const PassArgs &, bool, ps_op, cudaStream_t);
-template cudaError_t launch_persistent<float>(const PassArgs &, bool, ps_op, cudaStream_t);
+template cudaError_t launch_persistent<int32_t>(const PassArgs &, bool, int, cudaStream_t);
+template cudaError_t launch_persistent<int64_t>(const PassArgs &, bool, int, cudaStream_t);
+template cudaError_t launch_persistent<float>(const PassArgs &, bool, int, cudaStream_t);
 
 }  // namespace ps

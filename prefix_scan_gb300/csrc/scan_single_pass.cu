@@ -225,7 +225,7 @@ static cudaError_t launch_fallback(const PassArgs &a, bool exclusive, size_t til
 
 template <typename T>
 cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s,
-                               ps_op op) {
+                               int op) {
     constexpr ps_dtype dt = dtype_of<T>();
     const size_t tiles = num_tiles(dt, a.n);
     // a0 needs no work here: descriptors of earlier calls carry another
@@ -233,9 +233,13 @@ cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, c
     const bool vec_io = ((reinterpret_cast<uintptr_t>(a.in) | reinterpret_cast<uintptr_t>(a.out)) & 15u) == 0;
     if (lb == Lookback::Decoupled) {
         if (vec_io) return launch_persistent<T>(a, exclusive, op, s);
+        if constexpr (sizeof(T) == 8) {
+            if (op == kOpPairI32F32) return launch_fallback<T, OpPairI32F32>(a, exclusive, tiles, s);
+            if (op == kOpAffineF32) return launch_fallback<T, OpAffineF32>(a, exclusive, tiles, s);
+        }
         switch (op) {
-        case PS_OP_MAX: return launch_fallback<T, OpMax>(a, exclusive, tiles, s);
-        case PS_OP_MIN: return launch_fallback<T, OpMin>(a, exclusive, tiles, s);
+        case kOpMax: return launch_fallback<T, OpMax>(a, exclusive, tiles, s);
+        case kOpMin: return launch_fallback<T, OpMin>(a, exclusive, tiles, s);
         default: return launch_fallback<T, OpSum>(a, exclusive, tiles, s);
         }
     }
@@ -256,9 +260,9 @@ template cudaError_t launch_seeded_tile_scan<int32_t>(const PassArgs &, bool, cu
 template cudaError_t launch_seeded_tile_scan<int64_t>(const PassArgs &, bool, cudaStream_t);
 template cudaError_t launch_seeded_tile_scan<float>(const PassArgs &, bool, cudaStream_t);
 
-template cudaError_t launch_single_pass<int32_t>(const PassArgs &, bool, Lookback, cudaStream_t, ps_op);
-template cudaError_t launch_single_pass<int64_t>(const PassArgs &, bool, Lookback, cudaStream_t, ps_op);
-template cudaError_t launch_single_pass<float>(const PassArgs &, bool, Lookback, cudaStream_t, ps_op);
+template cudaError_t launch_single_pass<int32_t>(const PassArgs &, bool, Lookback, cudaStream_t, int);
+template cudaError_t launch_single_pass<int64_t>(const PassArgs &, bool, Lookback, cudaStream_t, int);
+template cudaError_t launch_single_pass<float>(const PassArgs &, bool, Lookback, cudaStream_t, int);
 
 // ---- test hook: the look-back alone -----------------------------------------
 template <typename T>

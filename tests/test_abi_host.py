@@ -186,3 +186,14 @@ def test_reduce_by_key_argument_errors(lib, no_device):
     ws64 = lib.ps_reduce_by_key_workspace_size(1, n)
     assert ws64 > ws
     assert r(1, K + 4, UK, AG, C, n, W, ws64, None) == _lib.PS_ERR_INVALID_ARG         # int64 keys, 4-aligned
+
+
+def test_pair_scan_argument_errors(lib, no_device):
+    n = 10_000
+    ws = lib.ps_scan_workspace_size(1, n)   # 8-byte elements use the int64 workspace
+    for f in (lib.ps_scan_pair_i32_f32, lib.ps_scan_affine_f32):
+        assert f(0, None, None, 0, None, 0, None) == _lib.PS_OK
+        assert f(0, FAKE + 4, FAKE + (1 << 20), n, FAKE + (2 << 20), ws, None) == _lib.PS_ERR_INVALID_ARG
+        assert f(0, FAKE, FAKE + (1 << 20), n, FAKE + (2 << 20), ws - 1, None) == _lib.PS_ERR_WORKSPACE_TOO_SMALL
+        assert f(1, FAKE, FAKE + 800, n, FAKE + (2 << 20), ws, None) == _lib.PS_ERR_OVERLAP
+        assert f(0, None, FAKE, n, FAKE + (2 << 20), ws, None) == _lib.PS_ERR_INVALID_ARG
