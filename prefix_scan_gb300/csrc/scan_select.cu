@@ -42,9 +42,13 @@ template <int OP> constexpr int sel_stages() { return OP == 0 ? 2 : kPStages; }
 template <typename T, int OP> constexpr size_t sel_stage_bytes() {
     return (size_t)sel_tile<T>() * sizeof(T) + (OP == 0 ? (size_t)sel_tile<T>() : 0);
 }
+// Per-iteration hand-offs (tile id, count, offset and their two mbarriers)
+// live in a ring of twice as many slots as there are stages, so that a
+// stage can be handed back before its offset has been consumed (select).
+template <int OP> constexpr int sel_ring() { return 2 * sel_stages<OP>(); }
 template <typename T, int OP> constexpr size_t sel_smem_bytes() {
     return (size_t)sel_stages<OP>() * sel_stage_bytes<T, OP>() +
-           ((size_t)sel_stages<OP>() * (4 * 8 + 8 + 4 + 4) + 127) / 128 * 128;
+           ((size_t)sel_stages<OP>() * 2 * 8 + (size_t)sel_ring<OP>() * (2 * 8 + 8 + 4 + 4) + 127) / 128 * 128;
 }
 
 // Raw bits of the element type, for comparisons in the element's own type.
@@ -80,6 +84,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
     constexpr int ROWS = ITEMS / VEC;
     constexpr long long TILE = sel_tile<T>();
     constexpr int S = sel_stages<OP>();
+    constexpr int R = sel_ring<OP>();
     constexpr uint32_t VAL_BYTES = (uint32_t)(TILE * sizeof(T));
     constexpr uint32_t FLAG_BYTES = OP == 0 ? (uint32_t)TILE : 0u;
     constexpr int CT = kSCW * 32;
@@ -90,11 +95,11 @@ select_kernel(SelectArgs a, long long num_tiles) {
     uint8_t *flg = smem + (size_t)S * VAL_BYTES;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * (VAL_BYTES + FLAG_BYTES));
     uint64_t *empty = full + S;
-    uint64_t *agg_done = empty + S;
-    uint64_t *prefix_ready = agg_done + S;
-    long long *tile_of = reinterpret_cast<long long *>(prefix_ready + S);
-    U *agg_of = reinterpret_cast<U *>(tile_of + S);
-    U *excl_of = agg_of + S;
+    uint64_t *agg_done = empty + S;          // the rest: R slots, slot k % R
+    uint64_t *prefix_ready = agg_done + R;
+    long long *tile_of = reinterpret_cast<long long *>(prefix_ready + R);
+    U *agg_of = reinterpret_cast<U *>(tile_of + R);
+    U *excl_of = agg_of + R;
     __shared__ U s_warp[2][kSCW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -112,9 +117,11 @@ select_kernel(SelectArgs a, long long num_tiles) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kSCW + 1);
-            mbar_init(&agg_done[s], 1);
-            mbar_init(&prefix_ready[s], 1);
-            tile_of[s] = num_tiles;
+        }
+        for (int slot = 0; slot < R; ++slot) {
+            mbar_init(&agg_done[slot], 1);
+            mbar_init(&prefix_ready[slot], 1);
+            tile_of[slot] = num_tiles;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -130,7 +137,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
                     break;
                 }
                 const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
-                tile_of[s] = t;
+                tile_of[k % R] = t;
                 if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     mbar_arrive_expect_tx(&full[s], VAL_BYTES + FLAG_BYTES);
                     bulk_load(vals + (size_t)s * TILE, in + t * TILE, VAL_BYTES, &full[s]);
@@ -149,9 +156,10 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
-            const long long tile = tile_of[s];
+            const int slot = (int)(k % R);
+            const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) {
-                if (lane == 0) mbar_arrive(&agg_done[s]);
+                if (lane == 0) mbar_arrive(&agg_done[slot]);
                 break;
             }
             const unsigned long long base = (unsigned long long)tile * TILE;
@@ -187,21 +195,21 @@ select_kernel(SelectArgs a, long long num_tiles) {
             const U agg = __reduce_add_sync(kFull, cnt);
             if (lane == 0) {
                 Desc<U, 1>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
-                agg_of[s] = agg;
-                mbar_arrive(&agg_done[s]);
+                agg_of[slot] = agg;
+                mbar_arrive(&agg_done[slot]);
             }
         }
     } else if (warp == kSCW + 2) {
         // ---------------- look-back: the tile's output offset ----------------
         for (long long k = 0;; ++k) {
-            const int s = (int)(k % S);
-            if (!mbar_wait(&agg_done[s], (uint32_t)((k / S) & 1))) {
+            const int slot = (int)(k % R);
+            if (!mbar_wait(&agg_done[slot], (uint32_t)((k / R) & 1))) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
-            const long long tile = tile_of[s];
+            const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) break;
-            const U agg = agg_of[s];
+            const U agg = agg_of[slot];
             __syncwarp();
             U excl = 0;
             if (tile != 0) {
@@ -210,8 +218,8 @@ select_kernel(SelectArgs a, long long num_tiles) {
             }
             if (lane == 0) {
                 if (a.num_selected && tile == num_tiles - 1) *a.num_selected = (unsigned long long)(excl + agg);
-                excl_of[s] = excl;
-                mbar_arrive(&prefix_ready[s]);
+                excl_of[slot] = excl;
+                mbar_arrive(&prefix_ready[slot]);
             }
         }
     } else {
@@ -222,7 +230,8 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
-            const long long tile = tile_of[s];
+            const int slot = (int)(k % R);
+            const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) break;
             const unsigned long long base = (unsigned long long)tile * TILE;
             const bool staged = a.use_bulk && base + TILE <= n;
@@ -264,6 +273,13 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 }
             }
 
+            if (!PARTITION) {
+                // select scatters from registers: the stage is not read
+                // again, so it goes back to the producer now, before the
+                // offset arrives (the hand-off ring keeps the slots apart)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
             // exclusive count of kept elements before each lane's row chunk
             U off[ROWS];
             U running = 0;
@@ -281,9 +297,9 @@ select_kernel(SelectArgs a, long long num_tiles) {
 #pragma unroll
             for (int w = 0; w < kSCW; ++w)
                 if (w < warp) warp_excl += sw[w];
-            if (!mbar_wait(&prefix_ready[s], (uint32_t)((k / S) & 1)))
+            if (!mbar_wait(&prefix_ready[slot], (uint32_t)((k / R) & 1)))
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
-            const U tile_excl = excl_of[s];
+            const U tile_excl = excl_of[slot];
 
             if (!PARTITION) {
                 // select: kept elements straight to their places; within a
@@ -326,8 +342,10 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 const U w_rej = w_valid - w_sel;
                 for (U q = lane; q < w_rej; q += 32) out[n - 1 - (rej_before + q)] = wbuf[w_sel + q];
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (PARTITION) {   // partition packed its output in the stage
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
         }
     }
 
