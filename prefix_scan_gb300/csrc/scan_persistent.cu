@@ -40,7 +40,17 @@
 namespace ps {
 
 constexpr int kPCW = kThreads / 32;   // compute warps per CTA
-constexpr size_t kStageTailBytes = ((size_t)kPStages * (4 * 8 + 8 + 8 + 8) + 127) / 128 * 128;
+// The compute warps hand a stage back as soon as they hold its data in
+// registers (before the tile's prefix is known) unless this is 0; the
+// per-iteration hand-offs then live in a ring of twice the stages.  A macro
+// so that a tuning sweep can rebuild without it.
+#ifndef PS_PERSIST_EARLY_RELEASE
+#define PS_PERSIST_EARLY_RELEASE 1
+#endif
+constexpr bool kEarlyRelease = PS_PERSIST_EARLY_RELEASE != 0;
+constexpr int kRing = kEarlyRelease ? 2 * kPStages : kPStages;   // hand-off slots: iteration k uses k % kRing
+// per stage: full, empty; per hand-off slot: agg_done, prefix_ready, tile id, aggregate, prefix
+constexpr size_t kStageTailBytes = ((size_t)kPStages * 2 * 8 + (size_t)kRing * (2 * 8 + 8 + 8 + 8) + 127) / 128 * 128;
 
 template <typename T> struct PItems { static constexpr int value = kItems32; };
 template <> struct PItems<int64_t> { static constexpr int value = kItems64; };
@@ -79,10 +89,10 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kPStages * TILE_BYTES);
     uint64_t *empty = full + kPStages;
     uint64_t *agg_done = empty + kPStages;
-    uint64_t *prefix_ready = agg_done + kPStages;
-    long long *tile_of = reinterpret_cast<long long *>(prefix_ready + kPStages);
-    U *agg_of = reinterpret_cast<U *>(tile_of + kPStages);
-    U *excl_of = agg_of + kPStages;
+    uint64_t *prefix_ready = agg_done + kRing;
+    long long *tile_of = reinterpret_cast<long long *>(prefix_ready + kRing);
+    U *agg_of = reinterpret_cast<U *>(tile_of + kRing);
+    U *excl_of = agg_of + kRing;
     __shared__ U s_warp[2][kPCW];
 
     const int tid = threadIdx.x;
@@ -101,9 +111,11 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kPCW + 1);     // compute warps + aggregator
-            mbar_init(&agg_done[s], 1);
-            mbar_init(&prefix_ready[s], 1);
-            tile_of[s] = num_tiles;   // end marker until the producer fills the stage
+        }
+        for (int slot = 0; slot < kRing; ++slot) {
+            mbar_init(&agg_done[slot], 1);
+            mbar_init(&prefix_ready[slot], 1);
+            tile_of[slot] = num_tiles;   // end marker until the producer fills it
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -122,7 +134,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                     }
                 }
                 const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
-                tile_of[s] = t;
+                tile_of[k % kRing] = t;
                 if (t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     mbar_arrive_expect_tx(&full[s], TILE_BYTES);
                     bulk_load(stage_data + (size_t)s * TILE, in + t * TILE, TILE_BYTES, &full[s]);
@@ -143,9 +155,10 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
-            const long long tile = tile_of[s];
+            const int slot = (int)(k % kRing);
+            const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) {   // end marker: pass it on to the look-back warp
-                if (lane == 0) mbar_arrive(&agg_done[s]);
+                if (lane == 0) mbar_arrive(&agg_done[slot]);
                 break;
             }
             const unsigned long long tile_base = (unsigned long long)tile * TILE;
@@ -221,40 +234,40 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                     // carry_in may alias carry_out
                     const U c = a.carry_in ? *reinterpret_cast<const U *>(a.carry_in) : ident;
                     Desc<U, Tr::DW>::store(desc, 0, kFlagP, Op::combine(c, agg), epoch);
-                    excl_of[s] = c;   // for the look-back warp
+                    excl_of[slot] = c;   // for the look-back warp
                 } else {
                     Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg, epoch);
                 }
-                agg_of[s] = agg;
-                mbar_arrive(&agg_done[s]);
+                agg_of[slot] = agg;
+                mbar_arrive(&agg_done[slot]);
             }
         }
     } else if (warp == kPCW + 2) {
         // ---------------- look-back warp ----------------
         // Runs ahead of the compute warps: once a tile's A is out it looks
-        // back, publishes P and leaves the exclusive prefix in excl_of[s]
+        // back, publishes P and leaves the exclusive prefix in excl_of[slot]
         // (steps 4-5 of section 4.1), so the compute warps rarely wait.
         for (long long k = 0;; ++k) {
-            const int s = (int)(k % kPStages);
-            if (!mbar_wait(&agg_done[s], (uint32_t)((k / kPStages) & 1))) {   // never in a correct run
+            const int slot = (int)(k % kRing);
+            if (!mbar_wait(&agg_done[slot], (uint32_t)((k / kRing) & 1))) {   // never in a correct run
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
-            const long long tile = tile_of[s];
+            const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) break;
-            const U agg = agg_of[s];
+            const U agg = agg_of[slot];
             __syncwarp();
             U excl;
             if (tile == 0) {
-                excl = excl_of[s];   // the carry the aggregator read
+                excl = excl_of[slot];   // the carry the aggregator read
             } else {
                 excl = look_back<U, Tr::DW, kLookbackK, Op>(desc, tile, epoch, a.max_polls, &hdr->status);
                 if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, Op::combine(excl, agg), epoch);
             }
             if (lane == 0) {
                 if (a.carry_out && tile == num_tiles - 1) *reinterpret_cast<U *>(a.carry_out) = Op::combine(excl, agg);
-                excl_of[s] = excl;
-                mbar_arrive(&prefix_ready[s]);
+                excl_of[slot] = excl;
+                mbar_arrive(&prefix_ready[slot]);
             }
         }
     } else {
@@ -265,7 +278,8 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
             break;
         }
-        const long long tile = tile_of[s];
+        const int slot = (int)(k % kRing);
+        const long long tile = tile_of[slot];
         if (tile < 0 || tile >= num_tiles) break;
         const unsigned long long tile_base = (unsigned long long)tile * TILE;
         const bool cut = tile_base + TILE > n;
@@ -282,6 +296,16 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             for (int r = 0; r < ROWS; ++r)
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) v[r][j] = (U)vget(buf[r], j);
+            if (kEarlyRelease) {
+                // the tile is in registers: the stage goes back to the
+                // producer before the prefix arrives.  The producer stays
+                // within kPStages iterations of this release and the compute
+                // warps within one of the look-back warp, so a hand-off slot
+                // (and its mbarrier phase) is not reused while a reader still
+                // needs it.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
         } else {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
@@ -329,9 +353,9 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             if (w < warp) warp_excl = Op::combine(warp_excl, sw[w]);
 
         // the look-back warp provides the tile's exclusive prefix
-        if (!mbar_wait(&prefix_ready[s], (uint32_t)((k / kPStages) & 1)))   // never in a correct run
+        if (!mbar_wait(&prefix_ready[slot], (uint32_t)((k / kRing) & 1)))   // never in a correct run
             report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
-        const U tile_excl = excl_of[s];
+        const U tile_excl = excl_of[slot];
 
         // a9
         const U base = Op::combine(tile_excl, warp_excl);
@@ -359,11 +383,14 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                     if (i < n) out[i] = (T)v[r][j];
                 }
         }
-        // Release the stage only now: the look-back warp cannot then run a
-        // whole ring ahead on it, so prefix_ready[s] completes exactly one
-        // phase per use and the parity wait above cannot alias.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        // Without the early release (or for a cut tile, read from global)
+        // the stage goes back only now; the look-back warp then cannot run a
+        // whole ring ahead on it, so each hand-off phase completes once per
+        // use and the parity wait above cannot alias.
+        if (!kEarlyRelease || cut) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
     }
     }
 
