@@ -38,17 +38,24 @@ template <typename T> struct SelItems { static constexpr int value = kItems32; }
 template <> struct SelItems<int64_t> { static constexpr int value = kItems64; };
 
 template <typename T> constexpr long long sel_tile() { return (long long)kThreads * SelItems<T>::value; }
-template <int OP> constexpr int sel_stages() { return OP == 0 ? 2 : kPStages; }
+// Stages: 2 with a flag array (values + flags, 40 KiB per int32 tile), else
+// 3; partition keeps 2 either way to make room for its pack buffer.
+template <int OP, bool PARTITION> constexpr int sel_stages() { return OP == 0 || PARTITION ? 2 : kPStages; }
 template <typename T, int OP> constexpr size_t sel_stage_bytes() {
     return (size_t)sel_tile<T>() * sizeof(T) + (OP == 0 ? (size_t)sel_tile<T>() : 0);
 }
 // Per-iteration hand-offs (tile id, count, offset and their two mbarriers)
 // live in a ring of twice as many slots as there are stages, so that a
 // stage can be handed back before its offset has been consumed (select).
-template <int OP> constexpr int sel_ring() { return 2 * sel_stages<OP>(); }
-template <typename T, int OP> constexpr size_t sel_smem_bytes() {
-    return (size_t)sel_stages<OP>() * sel_stage_bytes<T, OP>() +
-           ((size_t)sel_stages<OP>() * 2 * 8 + (size_t)sel_ring<OP>() * (2 * 8 + 8 + 4 + 4) + 127) / 128 * 128;
+template <int OP, bool PARTITION> constexpr int sel_ring() { return 2 * sel_stages<OP, PARTITION>(); }
+// partition: one tile of values in which each warp packs its output
+template <typename T, bool PARTITION> constexpr size_t sel_pack_bytes() {
+    return PARTITION ? (size_t)sel_tile<T>() * sizeof(T) : 0;
+}
+template <typename T, int OP, bool PARTITION> constexpr size_t sel_smem_bytes() {
+    return (size_t)sel_stages<OP, PARTITION>() * sel_stage_bytes<T, OP>() + sel_pack_bytes<T, PARTITION>() +
+           ((size_t)sel_stages<OP, PARTITION>() * 2 * 8 + (size_t)sel_ring<OP, PARTITION>() * (2 * 8 + 8 + 4 + 4) +
+            127) / 128 * 128;
 }
 
 // Raw bits of the element type, for comparisons in the element's own type.
@@ -83,8 +90,8 @@ select_kernel(SelectArgs a, long long num_tiles) {
     constexpr int ITEMS = SelItems<T>::value;
     constexpr int ROWS = ITEMS / VEC;
     constexpr long long TILE = sel_tile<T>();
-    constexpr int S = sel_stages<OP>();
-    constexpr int R = sel_ring<OP>();
+    constexpr int S = sel_stages<OP, PARTITION>();
+    constexpr int R = sel_ring<OP, PARTITION>();
     constexpr uint32_t VAL_BYTES = (uint32_t)(TILE * sizeof(T));
     constexpr uint32_t FLAG_BYTES = OP == 0 ? (uint32_t)TILE : 0u;
     constexpr int CT = kSCW * 32;
@@ -93,7 +100,9 @@ select_kernel(SelectArgs a, long long num_tiles) {
     extern __shared__ __align__(128) unsigned char smem[];
     T *vals = reinterpret_cast<T *>(smem);
     uint8_t *flg = smem + (size_t)S * VAL_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * (VAL_BYTES + FLAG_BYTES));
+    T *pack = reinterpret_cast<T *>(smem + (size_t)S * (VAL_BYTES + FLAG_BYTES));   // partition only
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * (VAL_BYTES + FLAG_BYTES) +
+                                                  sel_pack_bytes<T, PARTITION>());
     uint64_t *empty = full + S;
     uint64_t *agg_done = empty + S;          // the rest: R slots, slot k % R
     uint64_t *prefix_ready = agg_done + R;
@@ -273,13 +282,11 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 }
             }
 
-            if (!PARTITION) {
-                // select scatters from registers: the stage is not read
-                // again, so it goes back to the producer now, before the
-                // offset arrives (the hand-off ring keeps the slots apart)
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
+            // the tile is in registers and the stage is not read again: it
+            // goes back to the producer now, before the offset arrives (the
+            // hand-off ring keeps the slots apart)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
             // exclusive count of kept elements before each lane's row chunk
             U off[ROWS];
             U running = 0;
@@ -313,13 +320,11 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 }
             } else {
                 // partition: each warp packs its kept elements, then its
-                // rejected ones, into its own slice of the stage buffer --
-                // free now: this warp has read its slice and the aggregator
-                // finished with the stage before the prefix was handed over
-                // -- and writes them as two contiguous runs, consecutive
-                // lanes to consecutive addresses (the rejected run downwards
-                // from the end of `out`).
-                T *wbuf = vals + (size_t)s * TILE + seg;
+                // rejected ones, into its own slice of the pack buffer and
+                // writes them as two contiguous runs, consecutive lanes to
+                // consecutive addresses (the rejected run downwards from the
+                // end of `out`).
+                T *wbuf = pack + seg;
                 const U w_sel = running;   // kept elements of this warp
                 const unsigned long long w_first = base + seg;
                 const U w_valid = w_first >= n ? 0u
@@ -341,10 +346,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 const unsigned long long rej_before = w_first - dst;   // rejected before this warp
                 const U w_rej = w_valid - w_sel;
                 for (U q = lane; q < w_rej; q += 32) out[n - 1 - (rej_before + q)] = wbuf[w_sel + q];
-            }
-            if (PARTITION) {   // partition packed its output in the stage
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
+                __syncwarp();   // the slice is packed again next iteration
             }
         }
     }
@@ -354,7 +356,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
 
 template <typename T, int OP, bool PARTITION>
 static cudaError_t launch_select_variant(const SelectArgs &a, cudaStream_t s) {
-    constexpr size_t smem = sel_smem_bytes<T, OP>();
+    constexpr size_t smem = sel_smem_bytes<T, OP, PARTITION>();
     const long long tiles = (long long)((a.n + sel_tile<T>() - 1) / sel_tile<T>());
     static volatile int configured[64] = {};
     int dev = 0, sms = 0;
