@@ -154,6 +154,13 @@ template <typename T>
 cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, cudaStream_t s,
                                int op = kOpSum);
 
+// Short arrays (n <= small_scan_limit<T>(): two tiles) are scanned by one
+// CTA with no look-back and no workspace update (csrc/scan_small.cu).
+template <typename T>
+unsigned long long small_scan_limit();
+template <typename T>
+cudaError_t launch_small(const PassArgs &a, bool exclusive, int op, cudaStream_t s);
+
 // Third kernel of reduce-then-scan: tile scan seeded from the workspace.
 template <typename T>
 cudaError_t launch_seeded_tile_scan(const PassArgs &a, bool exclusive, cudaStream_t s);

@@ -232,6 +232,7 @@ cudaError_t launch_single_pass(const PassArgs &a, bool exclusive, Lookback lb, c
     // epoch and read as X, and the previous call left the counter at 0
     const bool vec_io = ((reinterpret_cast<uintptr_t>(a.in) | reinterpret_cast<uintptr_t>(a.out)) & 15u) == 0;
     if (lb == Lookback::Decoupled) {
+        if (a.n <= small_scan_limit<T>()) return launch_small<T>(a, exclusive, op, s);
         if (vec_io) return launch_persistent<T>(a, exclusive, op, s);
         if constexpr (sizeof(T) == 8) {
             if (op == kOpPairI32F32) return launch_fallback<T, OpPairI32F32>(a, exclusive, tiles, s);

@@ -55,8 +55,9 @@ def run(x: np.ndarray, exclusive: bool, inplace: bool = False, algo: str = "deco
 
 def sizes_for(dtype: str) -> list[int]:
     T = api.tile_elements(DTYPES[dtype][1])
-    return [1, 2, 3, 16, 31, 32, 33, 127, 1000, T - 1, T, T + 1, 2 * T - 3, 5 * T + 17,
-            33 * T + 5, 65537, (1 << 20) + 3]
+    # up to 2 tiles one CTA scans the whole array; above, the look-back kernel
+    return [1, 2, 3, 16, 31, 32, 33, 127, 1000, T - 1, T, T + 1, 2 * T - 3, 2 * T, 2 * T + 1,
+            5 * T + 17, 33 * T + 5, 65537, (1 << 20) + 3]
 
 
 @pytest.mark.parametrize("dtype", list(DTYPES))

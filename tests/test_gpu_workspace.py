@@ -72,7 +72,9 @@ def test_one_workspace_many_calls_mixed():
         t = torch.from_numpy(x.copy()).to(DEV)
         y = api.scan(t, exclusive=excl, algo=algo, inplace=inplace, workspace=ws)
         check(y.cpu().numpy(), x, excl)
-        if algo != "reduce_then_scan":
+        tdt = {"int32": torch.int32, "int64": torch.int64, "float32": torch.float32}[dt]
+        small = n <= 2 * api.tile_elements(tdt)   # one CTA, no look-back: the header is left as it is
+        if algo != "reduce_then_scan" and not small:
             expected_epoch += 1
         assert epoch_of(ws) == expected_epoch, (k, dt, algo)
         assert api.device_status(ws) == _lib.PS_OK
@@ -90,6 +92,22 @@ def test_workspace_never_zero_filled_refuses_to_run():
     api.scan_inclusive(x, out=out, workspace=ws)
     assert api.device_status(ws) == _lib.PS_OK
     assert torch.equal(out, torch.arange(1, n + 1, dtype=torch.int32, device=DEV))
+
+
+def test_short_arrays_leave_the_workspace_alone_and_respect_an_unzeroed_one():
+    # up to two tiles one CTA scans the array without touching the header
+    ws = api.alloc_workspace(torch.int32, 1 << 20, DEV)
+    for n in (1, 1000, 2 * api.tile_elements(torch.int32)):
+        x = inputs.full_range_i32(n, 90 + n)
+        y = api.scan_inclusive(torch.from_numpy(x).to(DEV), workspace=ws).cpu().numpy()
+        assert np.array_equal(y, oracle.inclusive(x))
+        assert epoch_of(ws) == 0 and api.device_status(ws) == _lib.PS_OK
+    bad = torch.full((api.workspace_size(torch.int32, 1000),), 0xAB, dtype=torch.uint8, device=DEV)
+    x = torch.ones(1000, dtype=torch.int32, device=DEV)
+    out = torch.full_like(x, -7)
+    api.scan_inclusive(x, out=out, workspace=bad)
+    assert api.device_status(bad) == _lib.PS_ERR_WORKSPACE_NOT_INITIALIZED
+    assert torch.all(out == -7)
 
 
 def _plant_stale_descriptors(ws, code: int, epoch: int, count: int) -> None:
@@ -118,8 +136,9 @@ def test_epoch_wraparound_clears_stale_descriptors(dtype):
     # descriptors of epoch 0 that a look-back at epoch 0 would trust
     _plant_stale_descriptors(ws, code, 0, 200)
     set_epoch(ws, EPOCH_MASK)                           # the next call is the last before the wrap
-    small = torch.ones(10, dtype=tdt, device=DEV)
-    assert torch.equal(api.scan_inclusive(small, workspace=ws).cpu(), torch.arange(1, 11, dtype=tdt))
+    m = 3 * api.tile_elements(tdt) + 1                  # long enough for the look-back kernel
+    ones = torch.ones(m, dtype=tdt, device=DEV)
+    assert torch.equal(api.scan_inclusive(ones, workspace=ws).cpu(), torch.arange(1, m + 1, dtype=tdt))
     assert epoch_of(ws) == 0
     # epoch 0 again: a wrong value planted above would now be read unless cleared
     xs = (inputs.full_range_i32(n, 5) if dtype == "int32" else inputs.hashes(n, 5).view(np.int64))
@@ -131,8 +150,9 @@ def test_epoch_wraparound_clears_stale_descriptors(dtype):
 def test_stale_descriptors_of_other_epochs_are_ignored():
     n = 64 * api.tile_elements(torch.int32)
     ws = api.alloc_workspace(torch.int32, n, DEV)
+    m = 3 * api.tile_elements(torch.int32) + 1         # long enough for the look-back kernel
     for e in (1, 2, 3):
-        api.scan_inclusive(torch.ones(100, dtype=torch.int32, device=DEV), workspace=ws)
+        api.scan_inclusive(torch.ones(m, dtype=torch.int32, device=DEV), workspace=ws)
     torch.cuda.synchronize()
     assert epoch_of(ws) == 3
     _plant_stale_descriptors(ws, 0, 2, 64)             # written "two calls ago"
