@@ -53,7 +53,9 @@
  *     and finishes.  Read it with ps_get_device_status().
  *   - One kernel launch per scan (three for reduce-then-scan): there is no
  *     per-call workspace reset, because each tile descriptor carries the
- *     number of the call that wrote it (see ps_workspace_init).
+ *     number of the call that wrote it (see ps_workspace_init).  The device
+ *     entry points never synchronise, so they can be captured in a CUDA
+ *     graph and the graph replayed any number of times.
  */
 #ifndef PREFIX_SCAN_H
 #define PREFIX_SCAN_H
