@@ -261,6 +261,21 @@ def cpu_baseline(w: workloads.Workload, target_s: float = 10.0, sample_n: int = 
             "cpu": _cpu_model()}
 
 
+def cpu_oracle_rate(call, algorithmic_bytes: int, sample: str, target_s: float = 1.5) -> dict:
+    """The oracle's rate for one operation, as it stands, single-threaded:
+    best of as many calls as fit in ``target_s`` (at least two), in GB/s of
+    the operation's algorithmic bytes on the sample."""
+    call()   # load the oracle library outside the timing
+    best, reps, t0 = float("inf"), 0, time.perf_counter()
+    while reps < 2 or time.perf_counter() - t0 < target_s:
+        t = time.perf_counter()
+        call()
+        best = min(best, time.perf_counter() - t)
+        reps += 1
+    return {"value": round(algorithmic_bytes / best / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "sample": f"{sample}, best of {reps}"}
+
+
 def _cpu_model() -> str:
     try:
         for line in Path("/proc/cpuinfo").read_text().splitlines():
@@ -577,7 +592,16 @@ def run_compaction(args, n: int = 1 << 28) -> dict:
         b = n * 4 + n + written * 4
         res[name] = {"ms": round(t * 1000, 4), "gbs": round(b / t / 1e9, 2),
                      "gelem_per_s": round(n / t / 1e9, 3), "kept": k,
-                     "algorithmic_bytes": b}
+                     "algorithmic_bytes": b, "frac_of_peak": round(b / t / 1e9 / hbm_peak()[0], 4)}
+    if not args.no_cpu_baseline:
+        import oracle
+        m = 1 << 24
+        xs, fs = inputs.full_range_i32(m, 8), inputs.bernoulli_half(m, 3).astype(np.uint8)
+        kept = int(np.count_nonzero(fs))
+        res["select"]["cpu_baseline"] = cpu_oracle_rate(lambda: oracle.select(xs, fs), m * 5 + kept * 4,
+                                                        f"first {m} elements")
+        res["partition"]["cpu_baseline"] = cpu_oracle_rate(lambda: oracle.partition(xs, fs), m * 9,
+                                                           f"first {m} elements")
     return res
 
 
@@ -617,8 +641,19 @@ def run_reduce_by_key(args, n: int = 1 << 25) -> dict:
             b = n * (8 if name == "reduce_by_key" else 4) + m * 8 + 8
             res[f"{name}_L{mean}"] = {"ms": round(t * 1000, 4), "gbs": round(b / t / 1e9, 2),
                                        "gpairs_per_s": round(n / t / 1e9, 3), "runs": m,
-                                       "algorithmic_bytes": b}
+                                       "algorithmic_bytes": b,
+                                       "frac_of_peak": round(b / t / 1e9 / hbm_peak()[0], 4)}
         del kt
+        if not args.no_cpu_baseline:
+            import oracle
+            ms_ = 1 << 22
+            ks = inputs.run_keys(ms_, mean, 11 + mean)
+            vs = inputs.uniform_f32(ms_, 12)
+            runs = int(np.count_nonzero(np.r_[True, ks[1:] != ks[:-1]]))
+            res[f"reduce_by_key_L{mean}"]["cpu_baseline"] = cpu_oracle_rate(
+                lambda: oracle.reduce_by_key(ks, vs), ms_ * 8 + runs * 8, f"first {ms_} pairs")
+            res[f"run_length_encode_L{mean}"]["cpu_baseline"] = cpu_oracle_rate(
+                lambda: oracle.reduce_by_key(ks, None), ms_ * 4 + runs * 8, f"first {ms_} keys")
     return res
 
 
@@ -698,7 +733,22 @@ def run_ops(args, n: int = 1 << 28) -> dict:
         ev1.record(stream)
         torch.cuda.synchronize()
         t = ev0.elapsed_time(ev1) / 1e3 / reps
-        res[name] = {"ms": round(t * 1000, 4), "gbs": round(8 * n / t / 1e9, 2)}
+        res[name] = {"ms": round(t * 1000, 4), "gbs": round(8 * n / t / 1e9, 2),
+                     "frac_of_peak": round(8 * n / t / 1e9 / hbm_peak()[0], 4)}
+    if not args.no_cpu_baseline:
+        import oracle
+        m = 1 << 24
+        xi, xf = inputs.full_range_i32(m, 9), inputs.uniform_f32(m, 10)
+        a8, b8 = inputs.uniform_f32(m // 2, 15), inputs.uniform_f32(m // 2, 16)
+        i8 = inputs.full_range_i32(m // 2, 13)
+        smp = f"first {m} 4-byte elements ({m // 2} 8-byte ones)"
+        res["max_int32"]["cpu_baseline"] = cpu_oracle_rate(lambda: oracle.scan_op(xi, "max"), 8 * m, smp)
+        res["min_int32"]["cpu_baseline"] = cpu_oracle_rate(lambda: oracle.scan_op(xi, "min"), 8 * m, smp)
+        res["sum_fp32_deterministic"]["cpu_baseline"] = cpu_oracle_rate(lambda: oracle.inclusive(xf), 8 * m, smp)
+        res["pair_i32_f32_sum"]["cpu_baseline"] = cpu_oracle_rate(
+            lambda: oracle.scan_pair_i32_f32(i8, a8), 8 * m, smp)
+        res["affine_f32_compose"]["cpu_baseline"] = cpu_oracle_rate(
+            lambda: oracle.scan_affine_f32(a8, b8), 8 * m, smp)
     return res
 
 
