@@ -87,6 +87,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     extern __shared__ __align__(128) unsigned char smem[];
     T *stage_data = reinterpret_cast<T *>(smem);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kPStages * TILE_BYTES);
+    __shared__ int s_abort;   // a compute warp's wait ran out: all of them leave
     uint64_t *empty = full + kPStages;
     uint64_t *agg_done = empty + kPStages;
     uint64_t *prefix_ready = agg_done + kRing;
@@ -108,6 +109,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA: nothing runs
 
     if (tid == 0) {
+        s_abort = 0;
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kPCW + 1);     // compute warps + aggregator
@@ -276,6 +278,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         const int s = (int)(k % kPStages);
         if (!mbar_wait(&full[s], (uint32_t)((k / kPStages) & 1))) {   // never in a correct run
             report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+            abort_meet(&s_abort, 1, CT);
             break;
         }
         const int slot = (int)(k % kRing);
@@ -347,6 +350,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         U *sw = s_warp[k & 1];
         if (lane == 0) sw[warp] = running;
         named_barrier(1, CT);
+        if (aborted(&s_abort)) break;
         U warp_excl = ident;
 #pragma unroll
         for (int w = 0; w < kPCW; ++w)

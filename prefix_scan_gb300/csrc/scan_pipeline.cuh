@@ -90,4 +90,14 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
 
+// The compute warps of a CTA meet at a named barrier once per tile.  A warp
+// whose bounded wait for its tile ran out must not leave the others waiting
+// there: it raises the CTA's abort flag and meets them one last time; after
+// that barrier every warp reads the flag and leaves the loop with it.
+__device__ __forceinline__ void abort_meet(volatile int *flag, int id, int threads) {
+    *flag = 1;
+    named_barrier(id, threads);
+}
+__device__ __forceinline__ bool aborted(const volatile int *flag) { return *flag != 0; }
+
 }  // namespace ps

@@ -163,6 +163,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     P *agg_of = reinterpret_cast<P *>(tile_of + S);
     P *excl_of = agg_of + S;
     __shared__ P s_warp[2][kRCW];
+    __shared__ int s_abort;   // a compute warp's wait ran out: all of them leave
     __shared__ uint32_t s_ah[2][kAgg], s_av[2][kAgg];   // aggregator shares: heads, values
     __shared__ int s_al[2][kAgg];                       // and last head
     // stage s: [halo vector][TILE keys][TILE values]
@@ -182,6 +183,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA
 
     if (tid == 0) {
+        s_abort = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kRCW + kAgg);
@@ -369,6 +371,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             const int s = (int)(k % S);
             if (!role_wait(&full[s], (uint32_t)((k / S) & 1))) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                abort_meet(&s_abort, 1, CT);
                 break;
             }
             const long long tile = tile_of[s];
@@ -472,6 +475,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             P *sw = s_warp[k & 1];
             if (lane == 0) sw[warp] = pair_of(rc, rv);
             named_barrier(1, CT);
+            if (aborted(&s_abort)) break;
             P warp_excl = 0;
 #pragma unroll
             for (int w = 0; w < kRCW; ++w)

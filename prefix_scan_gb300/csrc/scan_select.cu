@@ -110,6 +110,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
     U *agg_of = reinterpret_cast<U *>(tile_of + R);
     U *excl_of = agg_of + R;
     __shared__ U s_warp[2][kSCW];
+    __shared__ int s_abort;   // a compute warp's wait ran out: all of them leave
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     Header *hdr = reinterpret_cast<Header *>(a.ws);
@@ -123,6 +124,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
     if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA
 
     if (tid == 0) {
+        s_abort = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kSCW + 1);
@@ -237,6 +239,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
             const int s = (int)(k % S);
             if (!mbar_wait(&full[s], (uint32_t)((k / S) & 1))) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                abort_meet(&s_abort, 1, CT);
                 break;
             }
             const int slot = (int)(k % R);
@@ -300,6 +303,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
             U *sw = s_warp[k & 1];
             if (lane == 0) sw[warp] = running;
             named_barrier(1, CT);
+            if (aborted(&s_abort)) break;
             U warp_excl = 0;
 #pragma unroll
             for (int w = 0; w < kSCW; ++w)
