@@ -34,13 +34,23 @@ namespace {
 
 constexpr int kSCW = kThreads / 32;   // compute warps per CTA
 
-template <typename T> struct SelItems { static constexpr int value = kItems32; };
+// Elements per thread of a select / partition tile and the stages of the
+// flag-array form (macros so that a tuning sweep can rebuild with others).
+#ifndef PS_SEL_ITEMS32
+#define PS_SEL_ITEMS32 PS_ITEMS32
+#endif
+#ifndef PS_SEL_FLAG_STAGES
+#define PS_SEL_FLAG_STAGES 2
+#endif
+template <typename T> struct SelItems { static constexpr int value = PS_SEL_ITEMS32; };
 template <> struct SelItems<int64_t> { static constexpr int value = kItems64; };
 
 template <typename T> constexpr long long sel_tile() { return (long long)kThreads * SelItems<T>::value; }
 // Stages: 2 with a flag array (values + flags, 40 KiB per int32 tile), else
 // 3; partition keeps 2 either way to make room for its pack buffer.
-template <int OP, bool PARTITION> constexpr int sel_stages() { return OP == 0 || PARTITION ? 2 : kPStages; }
+template <int OP, bool PARTITION> constexpr int sel_stages() {
+    return OP == 0 ? PS_SEL_FLAG_STAGES : PARTITION ? 2 : kPStages;
+}
 template <typename T, int OP> constexpr size_t sel_stage_bytes() {
     return (size_t)sel_tile<T>() * sizeof(T) + (OP == 0 ? (size_t)sel_tile<T>() : 0);
 }
