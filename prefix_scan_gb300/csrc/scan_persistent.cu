@@ -26,9 +26,12 @@
 //
 // Per tile the compute warps do steps a2-a5 and a9 as the one-tile-per-CTA
 // kernel (scan_single_pass.cu) does: read the tile from shared memory in
-// rows of 16-byte vectors (conflict-free), scan in registers, combine warp
-// totals, wait for the prefix, add it and store with 16-byte streaming
-// stores, then release the buffer.
+// rows of 16-byte vectors (conflict-free) and hand the buffer straight back
+// to the producer, scan in registers, combine warp totals, wait for the
+// prefix, add it and store with 16-byte streaming stores.  Handing the
+// buffer back before the prefix arrives keeps one more tile's read in
+// flight per CTA; the per-iteration hand-offs between the roles therefore
+// live in a ring of twice the stages (see kRing).
 //
 // A tile that is cut by the end of the array is not copied; the compute
 // warps read it from global memory with bounds checks.  Every wait on an
