@@ -208,13 +208,22 @@ KERNEL_TRAFFIC_FILE = ROOT / "profiles" / "persistent_kernel_i32_excl_2p28_traff
 HEADLINE_KERNEL_SOURCES = ("scan_device.cuh", "scan_internal.h", "scan_persistent.cu", "scan_pipeline.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace collapsed, so that
+    editing a comment does not read as a kernel change."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_sources_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = ROOT / "prefix_scan_gb300" / "csrc"
     for name in HEADLINE_KERNEL_SOURCES:
         h.update(name.encode())
-        h.update((csrc / name).read_bytes())
+        h.update(_code_only((csrc / name).read_text()).encode())
     return h.hexdigest()
 
 
