@@ -523,7 +523,7 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": n * w.itemsize, "d2h_bytes_per_step": n * w.itemsize,
                 "steps": e2e_steps,
-                "path": "ps_scan_host: pinned host buffers, 64 MiB chunks, H2D/scan/D2H overlapped"},
+                "path": "ps_scan_host: pinned host buffers, 32 MiB chunks in 3 device buffers, H2D/scan/D2H overlapped"},
         "gpu_launches": args.steps * h.launches_per_step,
         "clocks": sampler.summary(),
         "parity_spot_check": ok,

@@ -190,15 +190,17 @@ ps_status ps_scan_seeded(ps_dtype dtype, int exclusive, const void *in, void *ou
 
 /*
  * Scan of arrays in HOST memory (the end-to-end path).  The array is
- * streamed through the GPU in 64 MiB chunks: the host-to-device copy of
- * chunk i+1, the seeded scan of chunk i and the device-to-host copy of
- * chunk i-1 run at the same time on three streams, and the running total
- * is carried on the device from chunk to chunk.
+ * streamed through the GPU in 32 MiB chunks rotating through three device
+ * buffers: host-to-device copies of the next chunks, the seeded scan of
+ * chunk i and the device-to-host copy of an earlier chunk run at the same
+ * time on three streams, and the running total is carried on the device
+ * from chunk to chunk.
  *   h_in, h_out : host arrays of n elements (h_out == h_in scans in place);
  *                 page-locked memory lets the copies overlap, pageable
  *                 memory works but the copies then serialise.
  *   d_staging   : device buffer of at least ps_scan_host_staging_size(dtype,
- *                 n) bytes, 256-byte aligned (two chunk buffers + a carry).
+ *                 n) bytes, 256-byte aligned (three chunk buffers of up to
+ *                 32 MiB + a carry).
  *   ws          : device workspace of at least ps_scan_workspace_size(dtype,
  *                 min(n, chunk)) bytes; ps_scan_workspace_size(dtype, n)
  *                 always suffices.

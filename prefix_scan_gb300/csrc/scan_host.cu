@@ -1,7 +1,7 @@
 // scan_host.cu -- scan of arrays in HOST memory, streamed through the GPU.
 //
-// The array is cut into chunks of 64 MiB.  Each chunk is copied to one of
-// two device staging buffers, scanned there in place with the seeded
+// The array is cut into chunks of 32 MiB.  Each chunk is copied to one of
+// three device staging buffers, scanned there in place with the seeded
 // single-pass scan (the carry -- the running total of all earlier chunks --
 // lives in device memory after the staging buffers, so no chunk waits for
 // the host), and copied back.  Three streams overlap the host-to-device
@@ -18,7 +18,21 @@
 
 namespace {
 
-constexpr size_t kChunkBytes = (size_t)64 << 20;
+// Chunk size: the first chunk's host-to-device copy and the last chunk's
+// device-to-host copy run alone, so smaller chunks shorten the pipeline's
+// fill and drain; each chunk costs one scan launch.  (A macro so that a
+// tuning sweep can rebuild with other sizes.)
+#ifndef PS_HOST_CHUNK_MIB
+#define PS_HOST_CHUNK_MIB 32
+#endif
+constexpr size_t kChunkBytes = (size_t)PS_HOST_CHUNK_MIB << 20;
+// Device staging buffers the chunks rotate through: with more than two,
+// host-to-device copies can run ahead while a chunk is scanned.
+#ifndef PS_HOST_BUFFERS
+#define PS_HOST_BUFFERS 3
+#endif
+constexpr int kBuffers = PS_HOST_BUFFERS;
+static_assert(kBuffers >= 2 && kBuffers <= 8, "2 to 8 staging buffers");
 
 bool host_dtype_ok(int dt) { return dt == PS_INT32 || dt == PS_INT64 || dt == PS_FLOAT32; }
 size_t chunk_elems(ps_dtype dt) { return kChunkBytes / ps::elem_bytes(dt); }
@@ -30,22 +44,26 @@ size_t stage_bytes(ps_dtype dt, size_t n) {
 struct Pipeline {
     cudaStream_t h2d = nullptr, d2h = nullptr;
     cudaEvent_t start = nullptr, done = nullptr;
-    cudaEvent_t loaded[2] = {}, scanned[2] = {}, freed[2] = {};
+    cudaEvent_t loaded[kBuffers] = {}, scanned[kBuffers] = {}, freed[kBuffers] = {};
 
     cudaError_t create() {
         cudaError_t e;
         if ((e = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking)) != cudaSuccess) return e;
         if ((e = cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking)) != cudaSuccess) return e;
-        for (cudaEvent_t *ev : {&start, &done, &loaded[0], &loaded[1], &scanned[0], &scanned[1],
-                                &freed[0], &freed[1]})
+        for (cudaEvent_t *ev : {&start, &done})
             if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+        for (int b = 0; b < kBuffers; ++b)
+            for (cudaEvent_t *ev : {&loaded[b], &scanned[b], &freed[b]})
+                if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
         return cudaSuccess;
     }
     // Resources are released once their pending work completes.
     ~Pipeline() {
-        for (cudaEvent_t ev : {start, done, loaded[0], loaded[1], scanned[0], scanned[1], freed[0],
-                               freed[1]})
+        for (cudaEvent_t ev : {start, done})
             if (ev) cudaEventDestroy(ev);
+        for (int b = 0; b < kBuffers; ++b)
+            for (cudaEvent_t ev : {loaded[b], scanned[b], freed[b]})
+                if (ev) cudaEventDestroy(ev);
         if (h2d) cudaStreamDestroy(h2d);
         if (d2h) cudaStreamDestroy(d2h);
     }
@@ -55,7 +73,7 @@ struct Pipeline {
 
 extern "C" size_t ps_scan_host_staging_size(ps_dtype dtype, size_t n) {
     if (!host_dtype_ok(dtype) || n == 0) return 0;
-    return 2 * stage_bytes(dtype, n) + 256;
+    return kBuffers * stage_bytes(dtype, n) + 256;
 }
 
 extern "C" ps_status ps_scan_host(ps_dtype dtype, int exclusive, const void *h_in, void *h_out,
@@ -78,9 +96,9 @@ extern "C" ps_status ps_scan_host(ps_dtype dtype, int exclusive, const void *h_i
     if (ws_bytes < ps::workspace_bytes(dtype, n < C ? n : C)) return PS_ERR_WORKSPACE_TOO_SMALL;
 
     cudaStream_t s = (cudaStream_t)stream;
-    unsigned char *stage[2] = {static_cast<unsigned char *>(d_staging),
-                               static_cast<unsigned char *>(d_staging) + stage_bytes(dtype, n)};
-    void *carry = static_cast<unsigned char *>(d_staging) + 2 * stage_bytes(dtype, n);
+    unsigned char *stage[kBuffers];
+    for (int b = 0; b < kBuffers; ++b) stage[b] = static_cast<unsigned char *>(d_staging) + b * stage_bytes(dtype, n);
+    void *carry = static_cast<unsigned char *>(d_staging) + kBuffers * stage_bytes(dtype, n);
     const unsigned char *src = static_cast<const unsigned char *>(h_in);
     unsigned char *dst = static_cast<unsigned char *>(h_out);
 
@@ -94,9 +112,9 @@ extern "C" ps_status ps_scan_host(ps_dtype dtype, int exclusive, const void *h_i
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p.d2h, p.start, 0);
     const size_t chunks = (n + C - 1) / C;
     for (size_t i = 0; i < chunks && e == cudaSuccess && st == PS_OK; ++i) {
-        const int b = (int)(i & 1);
+        const int b = (int)(i % kBuffers);
         const size_t off = i * C, len = (n - off < C) ? n - off : C;
-        if (i >= 2) e = cudaStreamWaitEvent(p.h2d, p.freed[b], 0);
+        if (i >= (size_t)kBuffers) e = cudaStreamWaitEvent(p.h2d, p.freed[b], 0);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(stage[b], src + off * es, len * es, cudaMemcpyHostToDevice, p.h2d);
         if (e == cudaSuccess) e = cudaEventRecord(p.loaded[b], p.h2d);

@@ -112,8 +112,8 @@ def test_chunked_scan_with_carries_equals_whole_scan():
 @pytest.mark.parametrize("dtype", list(NP))
 @pytest.mark.parametrize("exclusive", [False, True], ids=["incl", "excl"])
 def test_host_scan_multi_chunk(dtype, exclusive):
-    chunk = (64 << 20) // np.dtype(NP[dtype]).itemsize
-    n = 2 * chunk + chunk // 2 + 3            # two and a half chunks, ragged tail
+    chunk = (32 << 20) // np.dtype(NP[dtype]).itemsize
+    n = 4 * chunk + chunk // 2 + 3            # four and a half chunks (buffers reused), ragged tail
     x = make(dtype, n, 42)
     xt = torch.from_numpy(x).pin_memory()
     y = api.scan_host(xt, exclusive=exclusive).numpy()
@@ -126,7 +126,7 @@ def test_host_scan_multi_chunk(dtype, exclusive):
 
 
 def test_host_scan_in_place_pageable_and_small():
-    for n in (1, 1000, (64 << 20) // 4 + 1):
+    for n in (1, 1000, (32 << 20) // 4 + 1, 7 * (32 << 20) // 4 + 5):
         x = make("int32", n, 3 + n)
         xt = torch.from_numpy(x.copy())           # pageable, scanned in place
         api.scan_host(xt, out=xt)
