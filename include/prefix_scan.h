@@ -339,8 +339,10 @@ ps_status ps_run_length_encode(ps_dtype key_dtype, const void *keys, void *uniqu
 
 /*
  * Waits for `stream`, then reads into *out the device-side status of the
- * last scan that used `ws`: PS_OK, PS_ERR_LOOKBACK_TIMEOUT, or
- * PS_ERR_WORKSPACE_NOT_INITIALIZED (the workspace was never zero-filled).
+ * last call that ran a look-back kernel on `ws`: PS_OK,
+ * PS_ERR_LOOKBACK_TIMEOUT, or PS_ERR_WORKSPACE_NOT_INITIALIZED (the
+ * workspace was never zero-filled).  Scans of up to two tiles (see
+ * ps_tile_elements) run no look-back and leave the status as it was.
  * Returns PS_ERR_CUDA if the wait or the copy fails.
  */
 ps_status ps_get_device_status(const void *ws, ps_stream_t stream, ps_status *out);
