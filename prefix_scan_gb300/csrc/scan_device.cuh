@@ -430,13 +430,41 @@ __device__ __forceinline__ bool begin_call(const Header *hdr, uint32_t *epoch) {
     return (magic == kWorkspaceMagic && e <= kEpochMask) || (magic == 0u && e == 0u);
 }
 
+// Puts the header back for the next call: tile counter and done count to 0,
+// epoch + 1, and the largest size any call declared (the extent an epoch
+// wrap clears).
+__device__ __forceinline__ void ready_next_call(Header *hdr, unsigned long long ws_bytes, uint32_t epoch) {
+    const unsigned long long cap = hdr->capacity > ws_bytes ? hdr->capacity : ws_bytes;
+    hdr->capacity = cap;
+    hdr->tile_counter = 0ull;
+    hdr->done = 0u;
+    hdr->epoch = (epoch + 1u) & kEpochMask;
+    hdr->magic = kWorkspaceMagic;
+}
+
+// The early end of a call, for kernels whose CTAs take their tile ids one
+// producer thread each: that thread calls it once, when it takes no more
+// ids (past the end, or after a failed wait).  The last of them readies the
+// header at once instead of after the last CTA's stores: by then no claim
+// of the call is left and every CTA has read the header (each reads it
+// before its producer starts), and nothing else of the header is read or
+// written during the call but the status word.  Not for the call before an
+// epoch wrap, whose clearing of the descriptors needs every CTA done
+// (finish_call).
+__device__ __forceinline__ void claims_done(Header *hdr, unsigned long long ws_bytes, uint32_t epoch) {
+    __threadfence();   // this CTA's last claim precedes its count
+    if (atomicAdd(&hdr->done, 1u) == gridDim.x * gridDim.y * gridDim.z - 1) {
+        __threadfence();
+        ready_next_call(hdr, ws_bytes, epoch);
+    }
+}
+
 // End of a call, by every thread of every CTA once the CTA's work is done.
 // The last CTA to finish (counted with a fenced atomic, so all other CTAs'
-// writes precede it) puts the header back for the next call: tile counter
-// and done count to 0, epoch + 1.  When the epoch wraps it first clears
-// every descriptor slot the workspace has ever been declared to hold, so no
-// descriptor written 2^30 calls ago can pass for a current one.  No CTA
-// waits for another here.
+// writes precede it) puts the header back for the next call.  When the
+// epoch wraps it first clears every descriptor slot the workspace has ever
+// been declared to hold, so no descriptor written 2^30 calls ago can pass
+// for a current one.  No CTA waits for another here.
 __device__ __forceinline__ void finish_call(Header *hdr, unsigned char *ws, unsigned long long ws_bytes,
                                             uint32_t epoch) {
     __shared__ int s_last;
@@ -457,13 +485,7 @@ __device__ __forceinline__ void finish_call(Header *hdr, unsigned char *ws, unsi
         __threadfence();
         __syncthreads();
     }
-    if (threadIdx.x == 0) {
-        hdr->capacity = cap;
-        hdr->tile_counter = 0ull;
-        hdr->done = 0u;
-        hdr->epoch = (epoch + 1u) & kEpochMask;
-        hdr->magic = kWorkspaceMagic;
-    }
+    if (threadIdx.x == 0) ready_next_call(hdr, cap, epoch);
 }
 
 }  // namespace ps

@@ -51,6 +51,12 @@ constexpr int kPCW = kThreads / 32;   // compute warps per CTA
 #define PS_PERSIST_EARLY_RELEASE 1
 #endif
 constexpr bool kEarlyRelease = PS_PERSIST_EARLY_RELEASE != 0;
+// At the start of a call thread 0 of each CTA prefetches into L2 the tiles
+// the first round of claims will take, so their reads from memory overlap
+// the header read and the tile-id atomics; 0 turns it off.
+#ifndef PS_PERSIST_PREFETCH
+#define PS_PERSIST_PREFETCH 1
+#endif
 constexpr int kRing = kEarlyRelease ? 2 * kPStages : kPStages;   // hand-off slots: iteration k uses k % kRing
 // per stage: full, empty; per hand-off slot: agg_done, prefix_ready, tile id, aggregate, prefix
 constexpr size_t kStageTailBytes = ((size_t)kPStages * 2 * 8 + (size_t)kRing * (2 * 8 + 8 + 8 + 8) + 127) / 128 * 128;
@@ -108,10 +114,26 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     const T *in = reinterpret_cast<const T *>(a.in);
     T *out = reinterpret_cast<T *>(a.out);
 
-    uint32_t epoch;
-    if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA: nothing runs
-
+    // Thread 0 alone reads the header and hands the verdict to the CTA: one
+    // request per CTA to that L2 line, not one per warp (with 304 CTAs of 11
+    // warps the per-warp reads queued for microseconds at the line's slice).
+    __shared__ uint32_t s_epoch;
+    __shared__ int s_ok;
     if (tid == 0) {
+        if (PS_PERSIST_PREFETCH) {
+            // The producers take up to kPStages tile ids each before any
+            // stage comes back, so the first claims fall on the first
+            // kPStages x gridDim.x tiles, in whatever order: CTA b warms
+            // tiles b, b + grid and b + 2 grid (those the bulk copy will
+            // read).  Each is bulk-loaded soon after, so this adds no traffic.
+            for (int j = 0; j < kPStages; ++j) {
+                const unsigned long long t = blockIdx.x + (unsigned long long)j * gridDim.x;
+                if ((t + 1) * (unsigned long long)TILE <= n) prefetch_l2(in + t * TILE, TILE_BYTES);
+            }
+        }
+        uint32_t e;
+        s_ok = begin_call(hdr, &e) ? 1 : 0;
+        s_epoch = e;
         s_abort = 0;
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(&full[s], 1);
@@ -125,6 +147,8 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    if (!s_ok) return;   // same verdict in every CTA: nothing runs
+    const uint32_t epoch = s_epoch;
 
     if (warp == kPCW) {
         // ---------------- producer warp ----------------
@@ -148,6 +172,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 }
                 if (t >= num_tiles) break;
             }
+            if (epoch != kEpochMask) claims_done(hdr, a.ws_bytes, epoch);
         }
     } else if (warp == kPCW + 1) {
         // ---------------- aggregator warp ----------------
@@ -401,8 +426,9 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     }
     }
 
-    // every warp of the CTA is done: the last CTA readies the workspace
-    finish_call(hdr, a.ws, a.ws_bytes, epoch);
+    // The last producer to take its last tile id readied the workspace
+    // (claims_done); before an epoch wrap the last CTA to finish does.
+    if (epoch == kEpochMask) finish_call(hdr, a.ws, a.ws_bytes, epoch);
 }
 
 template <typename T, bool EXCL, typename Op>

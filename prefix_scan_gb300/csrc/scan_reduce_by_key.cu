@@ -179,10 +179,13 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     KU *ukeys = reinterpret_cast<KU *>(a.unique_keys);
     uint32_t *aggs = reinterpret_cast<uint32_t *>(a.aggs);
 
-    uint32_t epoch;
-    if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA
-
+    // thread 0 alone reads the header (one request per CTA to its line)
+    __shared__ uint32_t s_epoch;
+    __shared__ int s_ok;
     if (tid == 0) {
+        uint32_t e;
+        s_ok = begin_call(hdr, &e) ? 1 : 0;
+        s_epoch = e;
         s_abort = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
@@ -195,6 +198,8 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    if (!s_ok) return;   // same verdict in every CTA
+    const uint32_t epoch = s_epoch;
 
     if (warp == kRCW) {
         // ---------------- producer ----------------
@@ -221,6 +226,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 }
                 if (t >= num_tiles && ++ends == kLB) break;
             }
+            if (epoch != kEpochMask) claims_done(hdr, a.ws_bytes, epoch);
         }
     } else if (warp > kRCW && warp <= kRCW + kLB) {
         // ---------------- look-back warps: the tile's exclusive pair ----------------
@@ -519,7 +525,9 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
         }
     }
 
-    finish_call(hdr, a.ws, a.ws_bytes, epoch);
+    // the last producer readied the workspace; before an epoch wrap the
+    // last CTA to finish does
+    if (epoch == kEpochMask) finish_call(hdr, a.ws, a.ws_bytes, epoch);
 }
 
 template <typename KU, typename VU, bool HAS_VALS>

@@ -130,10 +130,13 @@ select_kernel(SelectArgs a, long long num_tiles) {
     T *out = reinterpret_cast<T *>(a.out);
     const T thr = from_raw<T>(a.threshold_bits);
 
-    uint32_t epoch;
-    if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA
-
+    // thread 0 alone reads the header (one request per CTA to its line)
+    __shared__ uint32_t s_epoch;
+    __shared__ int s_ok;
     if (tid == 0) {
+        uint32_t e;
+        s_ok = begin_call(hdr, &e) ? 1 : 0;
+        s_epoch = e;
         s_abort = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
@@ -147,6 +150,8 @@ select_kernel(SelectArgs a, long long num_tiles) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    if (!s_ok) return;   // same verdict in every CTA
+    const uint32_t epoch = s_epoch;
 
     if (warp == kSCW) {
         // ---------------- producer ----------------
@@ -168,6 +173,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 }
                 if (t >= num_tiles) break;
             }
+            if (epoch != kEpochMask) claims_done(hdr, a.ws_bytes, epoch);
         }
     } else if (warp == kSCW + 1) {
         // ---------------- aggregator: count and publish ----------------
@@ -365,7 +371,9 @@ select_kernel(SelectArgs a, long long num_tiles) {
         }
     }
 
-    finish_call(hdr, a.ws, a.ws_bytes, epoch);
+    // the last producer readied the workspace; before an epoch wrap the
+    // last CTA to finish does
+    if (epoch == kEpochMask) finish_call(hdr, a.ws, a.ws_bytes, epoch);
 }
 
 template <typename T, int OP, bool PARTITION>

@@ -64,9 +64,19 @@ single_pass_kernel(PassArgs a) {
     if (LB == Lookback::Precomputed) {
         tile = blockIdx.x;
     } else {
-        if (!begin_call(hdr, &epoch)) return;   // same verdict in every CTA
-        if (tid == 0) s_tile = (long long)atomicAdd(&hdr->tile_counter, 1ull);
+        // thread 0 alone reads the header (one request per CTA to its line)
+        // and, for a workspace it may use, takes the tile id
+        __shared__ uint32_t s_epoch;
+        __shared__ int s_ok;
+        if (tid == 0) {
+            uint32_t e;
+            s_ok = begin_call(hdr, &e) ? 1 : 0;
+            s_epoch = e;
+            if (s_ok) s_tile = (long long)atomicAdd(&hdr->tile_counter, 1ull);
+        }
         __syncthreads();
+        if (!s_ok) return;   // same verdict in every CTA
+        epoch = s_epoch;
         tile = s_tile;
     }
     const unsigned long long n = a.n;

@@ -1,7 +1,9 @@
 """The workspace across calls: zero-filled once, never reset by a call.
 
-Descriptors carry the number (epoch) of the call that wrote them, and the
-last CTA of each call puts the tile counter back and advances the epoch.
+Descriptors carry the number (epoch) of the call that wrote them, and each
+call leaves the header ready for the next: tile counter and done count back
+at 0, epoch advanced (by the last CTA to take a tile id, or, in the call
+before an epoch wrap, by the last CTA to finish).
 These tests drive one workspace through many calls of mixed lengths,
 dtypes and algorithms, a workspace that was never zero-filled, and the
 epoch wrap-around, always checking the results against the oracle.
@@ -9,6 +11,7 @@ epoch wrap-around, always checking the results against the oracle.
 from __future__ import annotations
 
 import ctypes
+import struct
 
 import numpy as np
 import pytest
@@ -39,6 +42,14 @@ def epoch_of(ws) -> int:
 def set_epoch(ws, epoch: int) -> None:
     _lib.check("ps_testing_set_workspace_epoch",
                _lib.load().ps_testing_set_workspace_epoch(ws.data_ptr(), epoch, None))
+
+
+def header(ws) -> dict:
+    """The workspace header as the library lays it out: u64 tile counter,
+    u64 status, u64 capacity, u32 done count, u32 epoch, u32 magic."""
+    raw = ws[:36].cpu().numpy().tobytes()
+    tc, status, cap, done, epoch, magic = struct.unpack_from("<QQQIII", raw)
+    return {"tile_counter": tc, "status": status, "capacity": cap, "done": done, "epoch": epoch, "magic": magic}
 
 
 def check(y, x, exclusive):
@@ -159,3 +170,57 @@ def test_stale_descriptors_of_other_epochs_are_ignored():
     x = inputs.full_range_i32(n, 6)
     y = api.scan_inclusive(torch.from_numpy(x).to(DEV), workspace=ws).cpu().numpy()
     assert np.array_equal(y, oracle.inclusive(x))
+
+
+def test_every_kernel_leaves_the_header_ready_for_the_next_call():
+    # The persistent scan, select, partition and reduce-by-key ready the
+    # header when their last CTA takes its last tile id, while other CTAs may
+    # still be storing; the one-tile-per-CTA fallback when its last CTA
+    # finishes.  After each: counter and done count 0, epoch + 1, and the
+    # results right -- including calls that run right after one another.
+    n = (1 << 21) + 77
+    need = max(api.workspace_size(torch.int32, n), api.reduce_by_key_workspace_size(torch.int32, n))
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    x = inputs.full_range_i32(n + 1, 31)
+    xt = torch.from_numpy(x).to(DEV)
+    f = inputs.bernoulli_half(n, 32).astype(np.uint8)
+    ft = torch.from_numpy(f).to(DEV)
+    k = inputs.run_keys(n, 16, 33)
+    kt = torch.from_numpy(k).to(DEV)
+    epoch = 0
+    for rep in range(2):
+        y = api.scan(xt[:n], workspace=ws)                          # persistent kernel
+        epoch += 1
+        assert header(ws) == {"tile_counter": 0, "status": 0, "capacity": need, "done": 0,
+                              "epoch": epoch, "magic": 0x50534742}, rep
+        assert np.array_equal(y.cpu().numpy(), oracle.inclusive(x[:n]))
+        y = api.scan(xt[1:], exclusive=True, workspace=ws)         # 4-byte offset: fallback kernel
+        epoch += 1
+        assert np.array_equal(y.cpu().numpy(), oracle.exclusive(x[1:]))
+        sel, cnt = api.select(xt[:n], ft, workspace=ws)
+        epoch += 1
+        want = oracle.select(x[:n], f)
+        assert int(cnt.item()) == want.shape[0] and np.array_equal(sel[:want.shape[0]].cpu().numpy(), want)
+        part, cnt = api.partition(xt[:n], ft, workspace=ws)
+        epoch += 1
+        assert int(cnt.item()) == want.shape[0] and np.array_equal(part[:want.shape[0]].cpu().numpy(), want)
+        uk, agg, runs = api.reduce_by_key(kt, xt[:n], workspace=ws)
+        epoch += 1
+        ok_k, ok_v = oracle.reduce_by_key(k, x[:n])
+        r = int(runs.item())
+        assert r == ok_k.shape[0] and np.array_equal(uk[:r].cpu().numpy(), ok_k)
+        assert np.array_equal(agg[:r].cpu().numpy(), ok_v)
+        h = header(ws)
+        assert (h["tile_counter"], h["done"], h["epoch"]) == (0, 0, epoch), rep
+        assert api.device_status(ws) == _lib.PS_OK
+    # the call before the wrap: the last CTA to finish clears and readies
+    set_epoch(ws, EPOCH_MASK)
+    y = api.scan(xt[:n], exclusive=True, workspace=ws)
+    h = header(ws)
+    assert (h["tile_counter"], h["done"], h["epoch"]) == (0, 0, 0)
+    assert np.array_equal(y.cpu().numpy(), oracle.exclusive(x[:n]))
+    sel, cnt = api.select(xt[:n], ft, workspace=ws)
+    h = header(ws)
+    assert (h["tile_counter"], h["done"], h["epoch"]) == (0, 0, 1)
+    assert int(cnt.item()) == want.shape[0] and np.array_equal(sel[:want.shape[0]].cpu().numpy(), want)
+    assert api.device_status(ws) == _lib.PS_OK
