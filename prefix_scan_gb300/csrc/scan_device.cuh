@@ -101,6 +101,11 @@ __device__ __forceinline__ void st_stream(float4 *p, const float4 &v) {
 __device__ __forceinline__ void st_stream(ulonglong2 *p, const ulonglong2 &v) {
     asm volatile("st.global.cs.v2.u64 [%0], {%1,%2};" :: "l"(p), "l"(v.x), "l"(v.y) : "memory");
 }
+// Two consecutive 16-byte vectors in one 32-byte store (p 32-byte aligned).
+__device__ __forceinline__ void st_stream_pair(ulonglong2 *p, const ulonglong2 &a, const ulonglong2 &b) {
+    asm volatile("st.global.cs.v4.u64 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "l"(a.x), "l"(a.y), "l"(b.x), "l"(b.y) : "memory");
+}
 
 // ---- tile status descriptors ----------------------------------------------
 // Flag and value share one single-copy-atomic 64-bit word, so a reader that

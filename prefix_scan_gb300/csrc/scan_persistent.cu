@@ -57,6 +57,17 @@ constexpr bool kEarlyRelease = PS_PERSIST_EARLY_RELEASE != 0;
 #ifndef PS_PERSIST_PREFETCH
 #define PS_PERSIST_PREFETCH 1
 #endif
+// 16-byte vectors each compute lane holds per row for 8-byte elements: with
+// two, a row's warp scan covers four elements per lane, as it does for 32-bit
+// ones, so an int64 tile needs half the (two-shuffle) 64-bit warp scans.
+#ifndef PS_PERSIST_VPL64
+#define PS_PERSIST_VPL64 2
+#endif
+// The aggregator of an 8-byte commutative scan keeps one running value per
+// vector element (two independent add-with-carry chains instead of one).
+#ifndef PS_PERSIST_AGG_SPLIT64
+#define PS_PERSIST_AGG_SPLIT64 1
+#endif
 constexpr int kRing = kEarlyRelease ? 2 * kPStages : kPStages;   // hand-off slots: iteration k uses k % kRing
 // per stage: full, empty; per hand-off slot: agg_done, prefix_ready, tile id, aggregate, prefix
 constexpr size_t kStageTailBytes = ((size_t)kPStages * 2 * 8 + (size_t)kRing * (2 * 8 + 8 + 8 + 8) + 127) / 128 * 128;
@@ -87,11 +98,14 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     using V = typename Tr::V;
     constexpr int VEC = Tr::VEC;
     constexpr int ITEMS = PItems<T>::value;
-    constexpr int ROWS = ITEMS / VEC;
+    constexpr int VPL = sizeof(T) == 8 ? PS_PERSIST_VPL64 : 1;   // vectors per lane per row
+    constexpr int EPL = VEC * VPL;                                // elements per lane per row
+    constexpr int ROWS = ITEMS / EPL;
+    static_assert(VPL == 1 || VPL == 2, "one or two vectors per lane per row");
     constexpr long long TILE = persistent_tile_elems<T>();
     constexpr uint32_t TILE_BYTES = (uint32_t)(TILE * sizeof(T));
     constexpr int CT = kPCW * 32;   // compute threads
-    static_assert(ITEMS % VEC == 0, "ITEMS must be a multiple of the vector width");
+    static_assert(ITEMS % EPL == 0, "ITEMS must be a multiple of a lane's share of a row");
 
     extern __shared__ __align__(128) unsigned char smem[];
     T *stage_data = reinterpret_cast<T *>(smem);
@@ -195,18 +209,24 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             U agg;
             if constexpr (Op::kCommutative) {
                 // each lane folds every 32nd vector; the order does not matter
-                U acc = ident;
+                constexpr int AC = (sizeof(U) == 8 && PS_PERSIST_AGG_SPLIT64) ? VEC : 1;
+                U accs[AC];
+#pragma unroll
+                for (int c = 0; c < AC; ++c) accs[c] = ident;
                 if (tile_base + TILE <= n) {
                     const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE);
 #pragma unroll 8
                     for (int i = lane; i < (int)(TILE / VEC); i += 32) {
                         const V x = src[i];
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) acc = Op::combine(acc, (U)vget(x, j));
+                        for (int j = 0; j < VEC; ++j) accs[j % AC] = Op::combine(accs[j % AC], (U)vget(x, j));
                     }
                 } else {
-                    for (unsigned long long i = tile_base + lane; i < n; i += 32) acc = Op::combine(acc, (U)in[i]);
+                    for (unsigned long long i = tile_base + lane; i < n; i += 32) accs[0] = Op::combine(accs[0], (U)in[i]);
                 }
+                U acc = accs[0];
+#pragma unroll
+                for (int c = 1; c < AC; ++c) acc = Op::combine(acc, accs[c]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 agg = warp_reduce<U, Op>(acc);
@@ -317,16 +337,27 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         const int seg = warp * 32 * ITEMS;   // element offset of this warp in the tile
 
         // a2: rows of 16-byte vectors from the stage (or bounded global loads)
-        U v[ROWS][VEC];
+        // With two vectors per lane, lanes 4-7 of each quarter-warp read
+        // their pair in swapped order, so that the eight 16-byte reads of a
+        // quarter-warp fall in distinct bank groups; the pair is put back in
+        // order in registers.
+        U v[ROWS][EPL];
         if (!cut) {
-            const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE + seg) + lane;
-            V buf[ROWS];
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) buf[r] = src[r * 32];
+            const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE + seg) + lane * VPL;
+            const int rot = VPL == 2 ? (lane >> 2) & 1 : 0;
+            V buf[ROWS][VPL];
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) v[r][j] = (U)vget(buf[r], j);
+                for (int t = 0; t < VPL; ++t) buf[r][t] = src[r * 32 * VPL + (t ^ rot)];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int t = 0; t < VPL; ++t) {
+                    const V x = rot ? buf[r][t ^ 1] : buf[r][t];
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) v[r][t * VEC + j] = (U)vget(x, j);
+                }
             if (kEarlyRelease) {
                 // the tile is in registers: the stage goes back to the
                 // producer before the prefix arrives.  The producer stays
@@ -341,13 +372,18 @@ persistent_kernel(PassArgs a, long long num_tiles) {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const unsigned long long i = tile_base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
+                for (int j = 0; j < EPL; ++j) {
+                    const unsigned long long i = tile_base + seg + (unsigned long long)(r * 32 + lane) * EPL + j;
                     v[r][j] = i < n ? (U)in[i] : ident;
                 }
         }
-        // a3 + a4
-        U off[ROWS];
+        // a3 + a4.  For 8-byte inclusive scans each row's offset within the warp
+        // is folded into its values at once rather than kept until the
+        // prefix arrives: ROWS more live 64-bit words would push the
+        // compute warps past the 80 registers that two CTAs of this size
+        // per SM allow (the cap is per SM sub-partition), and they spilled.
+        constexpr bool kFoldRows = sizeof(U) == 8 && !EXCL;
+        U off[kFoldRows ? 1 : ROWS];
         U running = ident;
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
@@ -355,7 +391,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             if (EXCL) {
                 U acc = ident;
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
+                for (int j = 0; j < EPL; ++j) {
                     const U x = v[r][j];
                     v[r][j] = acc;
                     acc = Op::combine(acc, x);
@@ -363,14 +399,20 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 t = acc;
             } else {
 #pragma unroll
-                for (int j = 1; j < VEC; ++j) v[r][j] = Op::combine(v[r][j - 1], v[r][j]);
-                t = v[r][VEC - 1];
+                for (int j = 1; j < EPL; ++j) v[r][j] = Op::combine(v[r][j - 1], v[r][j]);
+                t = v[r][EPL - 1];
             }
             const U sc = warp_inclusive<U, Op>(t, lane);
             U le = __shfl_up_sync(kFull, sc, 1);
             if (lane == 0) le = ident;
             const U row_total = __shfl_sync(kFull, sc, 31);
-            off[r] = Op::combine(running, le);
+            if constexpr (kFoldRows) {
+                const U o = Op::combine(running, le);
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) v[r][j] = Op::combine(o, v[r][j]);
+            } else {
+                off[r] = Op::combine(running, le);
+            }
             running = Op::combine(running, row_total);
         }
 
@@ -393,25 +435,46 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         const U base = Op::combine(tile_excl, warp_excl);
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
-            const U o = Op::combine(base, off[r]);
+            const U o = kFoldRows ? base : Op::combine(base, off[r]);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) v[r][j] = Op::combine(o, v[r][j]);
+            for (int j = 0; j < EPL; ++j) v[r][j] = Op::combine(o, v[r][j]);
         }
         if (!cut) {
-            V *dst = reinterpret_cast<V *>(out + tile_base + seg) + lane;
+            if constexpr (VPL == 2) {
+                // a lane's 32 bytes of a row in one store when `out` allows it
+                // (the bulk-copy path needs only 16-byte alignment)
+                V *dst = reinterpret_cast<V *>(out + tile_base + seg) + lane * 2;
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                V w;
+                for (int r = 0; r < ROWS; ++r) {
+                    V w0, w1;
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) vset(w, j, v[r][j]);
-                st_stream(dst + r * 32, w);
+                    for (int j = 0; j < VEC; ++j) {
+                        vset(w0, j, v[r][j]);
+                        vset(w1, j, v[r][VEC + j]);
+                    }
+                    if ((reinterpret_cast<uintptr_t>(out) & 31) == 0) {
+                        st_stream_pair(dst + r * 64, w0, w1);
+                    } else {
+                        st_stream(dst + r * 64, w0);
+                        st_stream(dst + r * 64 + 1, w1);
+                    }
+                }
+            } else {
+                V *dst = reinterpret_cast<V *>(out + tile_base + seg) + lane;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    V w;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) vset(w, j, v[r][j]);
+                    st_stream(dst + r * 32, w);
+                }
             }
         } else {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const unsigned long long i = tile_base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
+                for (int j = 0; j < EPL; ++j) {
+                    const unsigned long long i = tile_base + seg + (unsigned long long)(r * 32 + lane) * EPL + j;
                     if (i < n) out[i] = (T)v[r][j];
                 }
         }

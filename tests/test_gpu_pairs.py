@@ -112,6 +112,25 @@ def test_unaligned_arrays_take_the_fallback_kernel():
         check_affine(y.cpu().numpy(), a[1:], b[1:], excl)
 
 
+def test_16_byte_but_not_32_byte_aligned():
+    # the bulk-copy kernel with an output off a 32-byte boundary: each lane's
+    # 32 bytes of a row go out as two 16-byte stores
+    n = 7 * T + 19
+    xi, xf, packed = pairs(n + 2, 31)
+    buf = torch.from_numpy(packed).to(DEV)
+    assert buf.data_ptr() % 32 == 0
+    out = torch.empty((n + 2, 2), dtype=torch.int32, device=DEV)[2:]
+    for excl in (False, True):
+        y = api.scan_pairs(buf[2:], exclusive=excl, out=out)
+        check_pairs(y.cpu().numpy(), xi[2:], xf[2:], excl)
+    a = inputs.uniform_f32(n + 2, 41)
+    b = inputs.uniform_f32(n + 2, 42)
+    ab = torch.from_numpy(np.stack([a, b], axis=1)).to(DEV)
+    for excl in (False, True):
+        y = api.scan_affine(ab[2:], exclusive=excl)
+        check_affine(y.cpu().numpy(), a[2:], b[2:], excl)
+
+
 def test_int64_view_and_empty():
     xi, xf, packed = pairs(5000, 21)
     t64 = torch.from_numpy(packed.view(np.int64).reshape(-1)).to(DEV)

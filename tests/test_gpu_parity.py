@@ -99,6 +99,26 @@ def test_unaligned_pointers(dtype):
             check(y, x[off:], excl)
 
 
+@pytest.mark.parametrize("dtype", list(DTYPES))
+def test_16_byte_but_not_32_byte_aligned(dtype):
+    # 16-byte aligned arrays take the bulk-copy path; an output that is not
+    # also 32-byte aligned makes the 8-byte kernels store each lane's pair of
+    # vectors with two 16-byte stores instead of one 32-byte store
+    T = api.tile_elements(DTYPES[dtype][1])
+    n = 5 * T + 37
+    off = 16 // np.dtype(DTYPES[dtype][0]).itemsize
+    x = make(dtype, n + off, 90)
+    base = torch.from_numpy(x).to(DEV)
+    assert base.data_ptr() % 32 == 0
+    t = base[off:]
+    o = torch.empty(n + off, dtype=t.dtype, device=DEV)[off:]
+    for excl in (False, True):
+        y = api.scan(t, exclusive=excl, out=o).cpu().numpy()
+        check(y, x[off:], excl)
+    y = api.scan(t, out=t).cpu().numpy()   # in place at the same offset
+    check(y, x[off:], False)
+
+
 @pytest.mark.parametrize("algo", ["reduce_then_scan", "chained"])
 @pytest.mark.parametrize("dtype", list(DTYPES))
 def test_comparison_paths(algo, dtype):
