@@ -627,15 +627,16 @@ def run_reduce_by_key(args, n: int = 1 << 25) -> dict:
     uk = torch.empty(n, dtype=torch.int32, device=dev)
     agg = torch.empty(n, dtype=torch.float32, device=dev)
     cnts = agg.view(torch.int32)
+    nr = torch.zeros(1, dtype=torch.int64, device=dev)   # reused: no allocation or fill per call
     stream = torch.cuda.current_stream(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     res = {"n": n, "keys": "int32, runs of uniform length in [1, 2L-1]", "values": "fp32 uniform [-1, 1)"}
     for mean in (1, 16, 256):
         kt = torch.from_numpy(inputs.run_keys(n, mean, 11 + mean)).to(dev)
         for name, fn in (("reduce_by_key", lambda: api.reduce_by_key(kt, vt, unique_keys=uk, aggregates=agg,
-                                                                     workspace=ws)),
+                                                                     workspace=ws, num_runs=nr)),
                          ("run_length_encode", lambda: api.run_length_encode(kt, unique_keys=uk, counts=cnts,
-                                                                             workspace=ws))):
+                                                                             workspace=ws, num_runs=nr))):
             for _ in range(3):
                 _, _, cnt = fn()
             torch.cuda.synchronize()

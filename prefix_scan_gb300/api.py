@@ -243,7 +243,7 @@ def reduce_by_key_workspace_size(key_dtype: torch.dtype, n: int) -> int:
     return int(_lib.load().ps_reduce_by_key_workspace_size(dtype_code(key_dtype), n))
 
 
-def _runs(keys: torch.Tensor, values, unique_keys, aggregates, workspace, stream):
+def _runs(keys: torch.Tensor, values, unique_keys, aggregates, workspace, stream, num_runs=None):
     if not keys.is_cuda or keys.dim() != 1 or not keys.is_contiguous():
         raise ValueError("reduce_by_key: keys must be a contiguous 1-D CUDA tensor")
     n = keys.numel()
@@ -260,7 +260,10 @@ def _runs(keys: torch.Tensor, values, unique_keys, aggregates, workspace, stream
         aggregates = torch.empty(n, dtype=adt, device=keys.device)
     if unique_keys.dtype != keys.dtype or unique_keys.numel() < n or aggregates.dtype != adt or aggregates.numel() < n:
         raise ValueError("reduce_by_key: outputs need n entries of the key / aggregate dtype")
-    num_runs = torch.zeros(1, dtype=torch.int64, device=keys.device)
+    if num_runs is None:
+        num_runs = torch.zeros(1, dtype=torch.int64, device=keys.device)
+    elif not num_runs.is_cuda or num_runs.dtype != torch.int64 or num_runs.numel() < 1:
+        raise ValueError("reduce_by_key: num_runs must be an int64 CUDA tensor of at least one entry")
     lib = _lib.load()
     if workspace is None:
         need = int(lib.ps_reduce_by_key_workspace_size(kcode, n))
@@ -281,23 +284,25 @@ def _runs(keys: torch.Tensor, values, unique_keys, aggregates, workspace, stream
 
 def reduce_by_key(keys: torch.Tensor, values: torch.Tensor, *, unique_keys: torch.Tensor | None = None,
                   aggregates: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                  stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+                  stream=None, num_runs: torch.Tensor | None = None
+                  ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Single-pass reduce-by-key: for each run of consecutive bitwise-equal
     keys, its key and the sum of its values.  Returns (unique_keys,
     aggregates, num_runs): full-length outputs whose first ``num_runs``
     entries are defined; ``num_runs`` is a one-element int64 CUDA tensor
-    (no host synchronisation here)."""
+    (no host synchronisation here), allocated when not given."""
     if values is None:
         raise ValueError("reduce_by_key: values are required (run_length_encode counts runs)")
-    return _runs(keys, values, unique_keys, aggregates, workspace, stream)
+    return _runs(keys, values, unique_keys, aggregates, workspace, stream, num_runs)
 
 
 def run_length_encode(keys: torch.Tensor, *, unique_keys: torch.Tensor | None = None,
                       counts: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                      stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+                      stream=None, num_runs: torch.Tensor | None = None
+                      ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Single-pass run-length encoding: (unique_keys, counts, num_runs) as
     for :func:`reduce_by_key`, with int32 run lengths."""
-    return _runs(keys, None, unique_keys, counts, workspace, stream)
+    return _runs(keys, None, unique_keys, counts, workspace, stream, num_runs)
 
 
 def host_staging_size(dtype: torch.dtype, n: int) -> int:

@@ -168,7 +168,7 @@ ps_status reduce_by_key(ps_dtype kdt, ps_dtype vdt, bool rle, const void *keys, 
     ps::RbkArgs a{keys, rle ? nullptr : vals, ukeys, aggs, (unsigned long long)n,
                   static_cast<unsigned char *>(ws), (unsigned long long)(ws_bytes & ~(size_t)7),
                   reinterpret_cast<unsigned long long *>(num_runs), ps::kDefaultMaxPolls, bulk ? 1 : 0};
-    const cudaError_t e = ps::launch_reduce_by_key(a, kdt, vdt, s);
+    const cudaError_t e = rle ? ps::launch_run_length_encode(a, kdt, s) : ps::launch_reduce_by_key(a, kdt, vdt, s);
     return e == cudaSuccess ? PS_OK : cuda_fail(e);
 }
 

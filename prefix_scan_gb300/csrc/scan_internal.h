@@ -228,6 +228,10 @@ struct RbkArgs {
 // or PS_FLOAT32.
 cudaError_t launch_reduce_by_key(const RbkArgs &a, ps_dtype key_dt, ps_dtype val_dt, cudaStream_t s);
 
+// Enqueue a single-pass run-length encoding (a.vals unused): tiles of 32 KiB
+// of keys, so the reduce-by-key workspace size covers it.
+cudaError_t launch_run_length_encode(const RbkArgs &a, ps_dtype key_dt, cudaStream_t s);
+
 // Records `e` as the calling thread's last CUDA error (ps_last_cuda_error).
 void note_cuda_error(cudaError_t e);
 

@@ -190,3 +190,53 @@ def test_full_size_32m_pairs(vkind):
     uk, agg, runs = run(keys, vals)
     check(keys, vals, uk, agg, runs)
     torch.cuda.empty_cache()
+
+
+RLE_TILE = {"int32": 8192, "float32": 8192, "int64": 4096}   # keys per run-length-encoding tile
+
+
+@pytest.mark.parametrize("kdt", list(KEYS))
+def test_rle_tile_geometry(kdt):
+    # run-length encoding has tiles of its own (32 KiB of keys): lengths
+    # around them, and runs cut at tile, warp (1/8 tile) and row boundaries
+    T = RLE_TILE[kdt]
+    for k, n in enumerate([T - 1, T, T + 1, 2 * T, 2 * T + 1, 3 * T - 1, 7 * T + 5]):
+        for mean in (1, 2, 7, 1024, T):
+            keys = inputs.run_keys(n, mean, 500 + 10 * k + mean, KEYS[kdt])
+            uk, cnt, runs = run(keys, None)
+            check(keys, None, uk, cnt, runs)
+    n = 6 * T + 3
+    cuts = sorted({0, T // 8 - 1, T // 8, T // 32, T // 32 + 1, T - 1, T, 2 * T - T // 8, 2 * T + 1,
+                   4 * T - 1, 4 * T, 5 * T + T // 2})
+    keys = np.zeros(n, dtype=np.int64)
+    for j, c in enumerate(cuts):
+        keys[c:] = j + 1
+    keys = keys.astype(KEYS[kdt])
+    uk, cnt, runs = run(keys, None)
+    check(keys, None, uk, cnt, runs)
+
+
+def test_positions_above_2p31():
+    # n > 2^31: run positions and lengths need unsigned 32-bit arithmetic.
+    # Keys i // L (built on the device), so run j is key j of length L, the
+    # last one shorter; checked against that closed form on the device.
+    n, L = (1 << 31) + 12345, 1000
+    keys = torch.empty(n, dtype=torch.int32, device=DEV)
+    step = 1 << 28
+    for s in range(0, n, step):
+        e = min(n, s + step)
+        keys[s:e] = (torch.arange(s, e, dtype=torch.int64, device=DEV) // L).to(torch.int32)
+    m = (n + L - 1) // L
+    uk, cnt, nr = api.run_length_encode(keys)
+    assert int(nr.item()) == m
+    want = torch.arange(m, dtype=torch.int32, device=DEV)
+    assert torch.equal(uk[:m], want)
+    assert bool((cnt[:m - 1] == L).all()) and int(cnt[m - 1].item()) == n - (m - 1) * L
+    del cnt
+    ones = torch.ones(n, dtype=torch.int32, device=DEV)
+    uk, sums, nr = api.reduce_by_key(keys, ones, unique_keys=uk)
+    assert int(nr.item()) == m
+    assert torch.equal(uk[:m], want)
+    assert bool((sums[:m - 1] == L).all()) and int(sums[m - 1].item()) == n - (m - 1) * L
+    del keys, ones, uk, sums, want
+    torch.cuda.empty_cache()
