@@ -41,6 +41,14 @@ namespace {
 constexpr int kLCW = kThreads / 32;   // compute warps per CTA
 constexpr int kLStages = 3;
 constexpr int kLRing = 2 * kLStages;  // hand-off slots: iteration k uses k % kLRing
+// Aggregator warps: each reduces an equal part of a tile.  One warp took
+// about 2 us per 32 KiB tile, which capped each CTA at one tile per
+// aggregation; twelve warps of 80 registers still fit two CTAs per SM.
+#ifndef PS_RLE_AGG_WARPS
+#define PS_RLE_AGG_WARPS 2
+#endif
+constexpr int kLAgg = PS_RLE_AGG_WARPS;
+constexpr int kLThreads = (kLCW + 2 + kLAgg) * 32;   // compute, producer, look-back, aggregators
 
 // Role waits suspend in the barrier for up to this many nanoseconds per try
 // (0: poll), so that waiting warps leave the issue slots to working ones; a
@@ -97,7 +105,7 @@ template <typename KU> constexpr size_t rle_smem_bytes() {
 
 
 template <typename KU>
-__global__ void __launch_bounds__((kLCW + 3) * 32, kPCtasPerSm)
+__global__ void __launch_bounds__(kLThreads, kPCtasPerSm)
 rle_kernel(RbkArgs a, long long num_tiles) {
     using KV = RleVec<KU>;
     using V = typename KV::V;
@@ -124,6 +132,8 @@ rle_kernel(RbkArgs a, long long num_tiles) {
     P *excl_of = agg_of + R;
     __shared__ P s_warp[2][kLCW];
     __shared__ int s_abort;   // a compute warp's wait ran out: all of them leave
+    __shared__ P s_part[kLRing][kLAgg];   // the aggregators' parts of a tile's pair
+    __shared__ int s_parts_done[kLRing];  // parts in: the last one publishes
     // stage s: [halo vector][TILE keys]
     auto stage_keys = [&](int s) { return reinterpret_cast<KU *>(smem + (size_t)s * STAGE + 16); };
 
@@ -145,12 +155,13 @@ rle_kernel(RbkArgs a, long long num_tiles) {
         s_abort = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kLCW + 1);   // compute warps + aggregator
+            mbar_init(&empty[s], kLCW + kLAgg);   // compute warps + aggregators
         }
         for (int slot = 0; slot < R; ++slot) {
             mbar_init(&agg_done[slot], 1);
             mbar_init(&prefix_ready[slot], 1);
             tile_of[slot] = num_tiles;   // end marker until the producer fills it
+            s_parts_done[slot] = 0;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -185,83 +196,6 @@ rle_kernel(RbkArgs a, long long num_tiles) {
             if (epoch != kEpochMask) claims_done(hdr, a.ws_bytes, epoch);
         }
     } else if (warp == kLCW + 1) {
-        // ---------------- aggregator: the tile's pair, published at once ----------------
-        for (long long k = 0;; ++k) {
-            const int s = (int)(k % S);
-            if (!rle_wait(&full[s], (uint32_t)((k / S) & 1))) {
-                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
-                break;
-            }
-            const int slot = (int)(k % R);
-            const long long tile = tile_of[slot];
-            if (tile < 0 || tile >= num_tiles) {   // end marker: pass it on to the look-back warp
-                if (lane == 0) mbar_arrive(&agg_done[slot]);
-                break;
-            }
-            const unsigned long long base = (unsigned long long)tile * TILE;
-            uint32_t heads = 0;
-            uint32_t last = 0;   // position of the tile's last head (0: none)
-            if (a.use_bulk && base + TILE <= n) {
-                // lane l takes the C consecutive vectors [l C, l C + C), so
-                // the key before a vector is the last key of the one it read
-                // before (a register); it visits them from vector r = l mod 8
-                // on and wraps round, so that the 8 lanes one 16-byte load
-                // serves hit distinct bank groups.  Only two keys come from
-                // elsewhere: the one before the chunk (the halo for lane 0;
-                // tile 0 starts with a value that differs from element 0)
-                // and the one before vector r, which comes round last.
-                constexpr int C = NV / 32;
-                static_assert(C >= 8 && (C & (C - 1)) == 0, "chunk of a power-of-two size >= 8");
-                const KU *ks = stage_keys(s);
-                const V *kv = reinterpret_cast<const V *>(ks) + lane * C;
-                const int r0 = lane & 7;
-                const int e_chunk = lane * C * VK;   // tile index of the chunk's first key
-                const KU before_chunk = (tile == 0 && lane == 0) ? (KU)~ks[0] : ks[e_chunk - 1];
-                KU carry = r0 == 0 ? before_chunk : ks[e_chunk + r0 * VK - 1];
-                int last_vec = -1;   // highest vector of the chunk that holds a head
-#pragma unroll 8
-                for (int q = 0; q < C; ++q) {
-                    const int vi = (q + r0) & (C - 1);
-                    const V x = kv[vi];
-                    const KU prev = vi == 0 ? before_chunk : carry;
-                    carry = KV::key(x, VK - 1);
-                    uint32_t h = 0;
-#pragma unroll
-                    for (int j = 0; j < VK; ++j) h += (uint32_t)(KV::key(x, j) != (j ? KV::key(x, j - 1) : prev));
-                    heads += h;
-                    last_vec = (h && vi > last_vec) ? vi : last_vec;
-                }
-                // the tile's last head: in the highest lane that has one, in
-                // that lane's highest vector with one (same in every lane)
-                const int lv_lane = __reduce_max_sync(kFull, last_vec >= 0 ? lane : -1);
-                if (lv_lane >= 0) {
-                    const int lv = lv_lane * C + __shfl_sync(kFull, last_vec, lv_lane);
-                    const V x = reinterpret_cast<const V *>(ks)[lv];
-                    const KU prev = lv > 0 ? ks[lv * VK - 1] : tile == 0 ? (KU)~KV::key(x, 0) : ks[-1];
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int j = 0; j < VK; ++j) m |= (uint32_t)(KV::key(x, j) != (j ? KV::key(x, j - 1) : prev)) << j;
-                    last = (uint32_t)(base + (unsigned long long)(lv * VK + 31 - __clz(m)));
-                }
-            } else {
-                const unsigned long long end = base + TILE < n ? base + TILE : n;
-                int le = -1;
-                for (unsigned long long i = base + lane; i < end; i += 32)
-                    if (i == 0 || keys[i] != keys[i - 1]) { ++heads; le = (int)(i - base); }
-                le = __reduce_max_sync(kFull, le);
-                last = le >= 0 ? (uint32_t)(base + (unsigned long long)le) : 0u;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            heads = __reduce_add_sync(kFull, heads);
-            if (lane == 0) {
-                const P agg = ((P)heads << 32) | last;
-                Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
-                agg_of[slot] = agg;
-                mbar_arrive(&agg_done[slot]);
-            }
-        }
-    } else if (warp == kLCW + 2) {
         // ---------------- look-back: the tile's exclusive pair ----------------
         for (long long k = 0;; ++k) {
             const int slot = (int)(k % R);
@@ -289,6 +223,103 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 }
                 excl_of[slot] = excl;
                 mbar_arrive(&prefix_ready[slot]);
+            }
+        }
+    } else if (warp >= kLCW + 2) {
+        // ---------------- aggregators: the tile's pair, published at once ----------------
+        // kLAgg warps, each over an equal part of the tile; the last to
+        // finish combines the parts and publishes the pair.
+        const int g = warp - (kLCW + 2);
+        for (long long k = 0;; ++k) {
+            const int s = (int)(k % S);
+            if (!rle_wait(&full[s], (uint32_t)((k / S) & 1))) {
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                break;
+            }
+            const int slot = (int)(k % R);
+            const long long tile = tile_of[slot];
+            if (tile < 0 || tile >= num_tiles) {   // end marker: pass it on to the look-back warp
+                if (g == 0 && lane == 0) mbar_arrive(&agg_done[slot]);
+                break;
+            }
+            const unsigned long long base = (unsigned long long)tile * TILE;
+            uint32_t heads = 0;
+            uint32_t last = 0;   // position of the part's last head (0: none)
+            if (a.use_bulk && base + TILE <= n) {
+                // lane l takes the C consecutive vectors of its chunk, so
+                // the key before a vector is the last key of the one it read
+                // before (a register); it visits them from vector r = l mod 8
+                // on and wraps round, so that the 8 lanes one 16-byte load
+                // serves hit distinct bank groups.  Only two keys come from
+                // elsewhere: the one before the chunk (the halo for the
+                // tile's first chunk; tile 0 starts with a value that differs
+                // from element 0) and the one before vector r, which comes
+                // round last.
+                constexpr int PV = NV / kLAgg;   // vectors per part
+                constexpr int C = PV / 32;
+                static_assert(PV % 32 == 0 && C >= 8 && (C & (C - 1)) == 0, "chunk of a power-of-two size >= 8");
+                const KU *ks = stage_keys(s);
+                const int v_chunk = g * PV + lane * C;   // the chunk's first vector
+                const V *kv = reinterpret_cast<const V *>(ks) + v_chunk;
+                const int r0 = lane & 7;
+                const int e_chunk = v_chunk * VK;   // tile index of the chunk's first key
+                const KU before_chunk = (tile == 0 && e_chunk == 0) ? (KU)~ks[0] : ks[e_chunk - 1];
+                KU carry = r0 == 0 ? before_chunk : ks[e_chunk + r0 * VK - 1];
+                int last_vec = -1;   // highest vector of the chunk that holds a head
+#pragma unroll 8
+                for (int q = 0; q < C; ++q) {
+                    const int vi = (q + r0) & (C - 1);
+                    const V x = kv[vi];
+                    const KU prev = vi == 0 ? before_chunk : carry;
+                    carry = KV::key(x, VK - 1);
+                    uint32_t h = 0;
+#pragma unroll
+                    for (int j = 0; j < VK; ++j) h += (uint32_t)(KV::key(x, j) != (j ? KV::key(x, j - 1) : prev));
+                    heads += h;
+                    last_vec = (h && vi > last_vec) ? vi : last_vec;
+                }
+                // the part's last head: in the highest lane that has one, in
+                // that lane's highest vector with one (same in every lane)
+                const int lv_lane = __reduce_max_sync(kFull, last_vec >= 0 ? lane : -1);
+                if (lv_lane >= 0) {
+                    const int lv = g * PV + lv_lane * C + __shfl_sync(kFull, last_vec, lv_lane);
+                    const V x = reinterpret_cast<const V *>(ks)[lv];
+                    const KU prev = lv > 0 ? ks[lv * VK - 1] : tile == 0 ? (KU)~KV::key(x, 0) : ks[-1];
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int j = 0; j < VK; ++j) m |= (uint32_t)(KV::key(x, j) != (j ? KV::key(x, j - 1) : prev)) << j;
+                    last = (uint32_t)(base + (unsigned long long)(lv * VK + 31 - __clz(m)));
+                }
+            } else {
+                constexpr long long PART = TILE / kLAgg;
+                const unsigned long long lo = base + (unsigned long long)(g * PART);
+                const unsigned long long hi = base + (unsigned long long)((g + 1) * PART);
+                const unsigned long long end = hi < n ? hi : n;
+                long long le = -1;
+                for (unsigned long long i = lo + lane; i < end; i += 32)
+                    if (i == 0 || keys[i] != keys[i - 1]) { ++heads; le = (long long)(i - base); }
+                const int lmax = __reduce_max_sync(kFull, (int)le);
+                last = lmax >= 0 ? (uint32_t)(base + (unsigned long long)lmax) : 0u;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            heads = __reduce_add_sync(kFull, heads);
+            if (lane == 0) {
+                // parts later in the tile have larger positions, so the
+                // parts combine in any order
+                volatile P *part = s_part[slot];
+                part[g] = ((P)heads << 32) | last;
+                __threadfence_block();
+                if (atomicAdd(&s_parts_done[slot], 1) == kLAgg - 1) {
+                    __threadfence_block();
+                    P agg = 0;
+#pragma unroll
+                    for (int gg = 0; gg < kLAgg; ++gg) agg = OpRle::combine(agg, (P)part[gg]);
+                    s_parts_done[slot] = 0;   // the slot's next use is kLRing iterations on
+                    Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
+                    agg_of[slot] = agg;
+                    mbar_arrive(&agg_done[slot]);
+                }
             }
         }
     } else {
@@ -490,7 +521,7 @@ static cudaError_t launch_rle_keys(const RbkArgs &a, cudaStream_t s) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     long long grid = (long long)sms * kPCtasPerSm;
     if (grid > tiles) grid = tiles;
-    rle_kernel<KU><<<(unsigned int)grid, (kLCW + 3) * 32, smem, s>>>(a, tiles);
+    rle_kernel<KU><<<(unsigned int)grid, kLThreads, smem, s>>>(a, tiles);
     return cudaGetLastError();
 }
 
