@@ -292,10 +292,12 @@ ps_status ps_scan_affine_f32(int exclusive, const ps_affine_f32 *in, ps_affine_f
  * Single-pass reduce-by-key and run-length encoding: the other fused
  * workloads of the decoupled look-back paper (Merrill & Garland, "Single-pass
  * Parallel Prefix Scan with Decoupled Look-back", A5 results on
- * reduce-by-key and run-length-encode), computed as one scan over (run
- * count, value since the run began) pairs under the segmented-sum operator
- * -- associative, not commutative, which the method allows (section 4.2:
- * only contiguous partials are ever combined).
+ * reduce-by-key and run-length-encode).  Reduce-by-key is one scan over
+ * (run count, value since the run began) pairs under the segmented-sum
+ * operator -- associative, not commutative, which the method allows (section
+ * 4.2: only contiguous partials are ever combined).  Run-length encoding is
+ * one scan over (run count, position of the last run start) pairs: a run's
+ * length is the distance from its first element to the next run's.
  *
  * A run is a maximal stretch of consecutive keys with equal bits (fp32 keys
  * compare as their 32-bit patterns: -0.0 and +0.0 are different keys, two

@@ -1,6 +1,6 @@
-// scan_reduce_by_key.cu -- single-pass reduce-by-key and run-length
-// encoding (decoupled look-back paper summary, A5: the fused compaction
-// workloads besides select and partition).
+// scan_reduce_by_key.cu -- single-pass reduce-by-key (decoupled look-back
+// paper summary, A5: one of the fused compaction workloads besides select
+// and partition).
 //
 // Element i opens a run ("head") when i == 0 or its key bits differ from
 // those of element i-1.  With the pair p_i = (head_i, value_i) and the
@@ -13,7 +13,8 @@
 // and the number of runs.  The operator is associative but not commutative;
 // the method only ever combines contiguous partials (section 4.2), so the
 // look-back works unchanged once its window reduction keeps the order.
-// Run-length encoding is the same scan with every value equal to 1.
+// (Run-length encoding needs no value sums -- a run's length is the
+// distance between two heads -- and has its own kernel, scan_rle.cu.)
 //
 // The pair travels as one 64-bit word, count << 32 | value bits, and a tile
 // descriptor is the two-word form the int64 scan uses.
@@ -67,7 +68,7 @@ __device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity) {
 }
 
 template <typename VU> struct RunValue;
-template <> struct RunValue<uint32_t> {   // int32 values, modulo 2^32; also run lengths
+template <> struct RunValue<uint32_t> {   // int32 values, modulo 2^32
     static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) { return a + b; }
     static __device__ __forceinline__ uint32_t warp_total(uint32_t v) { return __reduce_add_sync(kFull, v); }
 };
@@ -122,19 +123,17 @@ template <typename KU> constexpr long long rbk_tile() { return sizeof(KU) == 4 ?
 template <typename KU> constexpr uint32_t rbk_key_bytes() {   // the tile's keys and the halo vector
     return (uint32_t)(rbk_tile<KU>() * sizeof(KU) + 16);
 }
-// The value region exists without values too: the scatter packs each
-// warp's run values (lengths) there.
-template <typename KU, bool HAS_VALS> constexpr uint32_t rbk_stage_bytes() {
+template <typename KU> constexpr uint32_t rbk_stage_bytes() {
     return rbk_key_bytes<KU>() + (uint32_t)(rbk_tile<KU>() * 4);
 }
-template <typename KU, bool HAS_VALS> constexpr size_t rbk_smem_bytes() {
-    return (size_t)kRStages * rbk_stage_bytes<KU, HAS_VALS>() + ((size_t)kRStages * (4 * 8 + 8 * 3) + 8 + 127) / 128 * 128;
+template <typename KU> constexpr size_t rbk_smem_bytes() {
+    return (size_t)kRStages * rbk_stage_bytes<KU>() + ((size_t)kRStages * (4 * 8 + 8 * 3) + 8 + 127) / 128 * 128;
 }
 
 }  // namespace
 
 
-template <typename KU, typename VU, bool HAS_VALS>
+template <typename KU, typename VU>
 __global__ void __launch_bounds__(kRbkThreads, kPCtasPerSm)
 reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     using KV = KeyVec<KU>;
@@ -148,8 +147,8 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     constexpr int ROWS = ITEMS / VK;
     constexpr int S = kRStages;
     constexpr uint32_t KEY_BYTES = rbk_key_bytes<KU>();
-    constexpr uint32_t STAGE = rbk_stage_bytes<KU, HAS_VALS>();
-    constexpr uint32_t VAL_BYTES = HAS_VALS ? (uint32_t)(TILE * 4) : 0u;
+    constexpr uint32_t STAGE = rbk_stage_bytes<KU>();
+    constexpr uint32_t VAL_BYTES = (uint32_t)(TILE * 4);
     constexpr int CT = kRCW * 32;
     static_assert(ITEMS % VK == 0 && STAGE % 16 == 0, "tile geometry");
 
@@ -220,7 +219,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                         bulk_load(stage_keys(s), keys, kb, &full[s]);
                     else
                         bulk_load(stage_keys(s) - VK, keys + t * TILE - VK, kb, &full[s]);
-                    if constexpr (HAS_VALS) bulk_load(stage_vals(s), vals + t * TILE, VAL_BYTES, &full[s]);
+                    bulk_load(stage_vals(s), vals + t * TILE, VAL_BYTES, &full[s]);
                 } else {
                     mbar_arrive(&full[s]);   // end marker, or a tile read from global
                 }
@@ -337,29 +336,25 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
 #pragma unroll
             for (int g = 0; g < kAgg; ++g) { C += s_ah[b][g]; L = s_al[b][g] > L ? s_al[b][g] : L; }
             const int from = L < 0 ? 0 : L;   // the tile's trailing run starts here
-            uint32_t val = 0u;
-            if constexpr (!HAS_VALS) {
-                val = (uint32_t)(len - from);
-            } else {
-                uint32_t acc = 0u;   // +0.0f for fp32
-                if (staged) {
-                    const W *wv = reinterpret_cast<const W *>(stage_vals(s));
-                    const int v0 = ag * PART, v1 = v0 + PART;
-                    for (int vi = (from / VK > v0 ? from / VK : v0) + lane; vi < v1; vi += 32) {
-                        const W w = wv[vi];
+            uint32_t val = 0u;   // +0.0f for fp32
+            uint32_t acc = 0u;
+            if (staged) {
+                const W *wv = reinterpret_cast<const W *>(stage_vals(s));
+                const int v0 = ag * PART, v1 = v0 + PART;
+                for (int vi = (from / VK > v0 ? from / VK : v0) + lane; vi < v1; vi += 32) {
+                    const W w = wv[vi];
 #pragma unroll
-                        for (int j = 0; j < VK; ++j)
-                            if (vi * VK + j >= from) acc = RunValue<VU>::add(acc, KV::val(w, j));
-                    }
-                } else if (ag == 0) {
-                    for (int e = from + lane; e < len; e += 32) acc = RunValue<VU>::add(acc, vals[base + e]);
+                    for (int j = 0; j < VK; ++j)
+                        if (vi * VK + j >= from) acc = RunValue<VU>::add(acc, KV::val(w, j));
                 }
-                acc = RunValue<VU>::warp_total(acc);
-                if (lane == 0) s_av[b][ag] = acc;
-                if (!meet()) break;
-#pragma unroll
-                for (int g = 0; g < kAgg; ++g) val = RunValue<VU>::add(val, s_av[b][g]);
+            } else if (ag == 0) {
+                for (int e = from + lane; e < len; e += 32) acc = RunValue<VU>::add(acc, vals[base + e]);
             }
+            acc = RunValue<VU>::warp_total(acc);
+            if (lane == 0) s_av[b][ag] = acc;
+            if (!meet()) break;
+#pragma unroll
+            for (int g = 0; g < kAgg; ++g) val = RunValue<VU>::add(val, s_av[b][g]);
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&empty[s]);
@@ -406,14 +401,9 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
 #pragma unroll
                     for (int j = 0; j < VK; ++j) m |= (uint32_t)(kk[r][j] != (j ? kk[r][j - 1] : prev)) << j;
                     if (tile == 0 && e0 == 0) m |= 1u;
-                    if constexpr (HAS_VALS) {
-                        const W w = reinterpret_cast<const W *>(stage_vals(s))[e0 / VK];
+                    const W w = reinterpret_cast<const W *>(stage_vals(s))[e0 / VK];
 #pragma unroll
-                        for (int j = 0; j < VK; ++j) vv[r][j] = KV::val(w, j);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < VK; ++j) vv[r][j] = 1u;
-                    }
+                    for (int j = 0; j < VK; ++j) vv[r][j] = KV::val(w, j);
                 } else {
 #pragma unroll
                     for (int j = 0; j < VK; ++j) {
@@ -421,8 +411,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                         if (i < n) {
                             kk[r][j] = keys[i];
                             m |= (uint32_t)(i == 0 || kk[r][j] != keys[i - 1]) << j;
-                            if constexpr (HAS_VALS) vv[r][j] = vals[i];
-                            else vv[r][j] = 1u;
+                            vv[r][j] = vals[i];
                         } else {
                             kk[r][j] = KU(0);
                             vv[r][j] = 0u;   // past the end: neither a head nor a value
@@ -530,16 +519,16 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     if (epoch == kEpochMask) finish_call(hdr, a.ws, a.ws_bytes, epoch);
 }
 
-template <typename KU, typename VU, bool HAS_VALS>
+template <typename KU, typename VU>
 static cudaError_t launch_rbk_variant(const RbkArgs &a, cudaStream_t s) {
-    constexpr size_t smem = rbk_smem_bytes<KU, HAS_VALS>();
+    constexpr size_t smem = rbk_smem_bytes<KU>();
     const long long tiles = (long long)((a.n + rbk_tile<KU>() - 1) / rbk_tile<KU>());
     static volatile int configured[64] = {};
     int dev = 0, sms = 0;
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(reduce_by_key_kernel<KU, VU, HAS_VALS>,
+        e = cudaFuncSetAttribute(reduce_by_key_kernel<KU, VU>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = 1;
@@ -547,15 +536,14 @@ static cudaError_t launch_rbk_variant(const RbkArgs &a, cudaStream_t s) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     long long grid = (long long)sms * kPCtasPerSm;
     if (grid > tiles) grid = tiles;
-    reduce_by_key_kernel<KU, VU, HAS_VALS><<<(unsigned int)grid, kRbkThreads, smem, s>>>(a, tiles);
+    reduce_by_key_kernel<KU, VU><<<(unsigned int)grid, kRbkThreads, smem, s>>>(a, tiles);
     return cudaGetLastError();
 }
 
 template <typename KU>
 static cudaError_t launch_rbk_keys(const RbkArgs &a, ps_dtype val_dt, cudaStream_t s) {
-    if (a.vals == nullptr) return launch_rbk_variant<KU, uint32_t, false>(a, s);
-    if (val_dt == PS_FLOAT32) return launch_rbk_variant<KU, float, true>(a, s);
-    return launch_rbk_variant<KU, uint32_t, true>(a, s);
+    if (val_dt == PS_FLOAT32) return launch_rbk_variant<KU, float>(a, s);
+    return launch_rbk_variant<KU, uint32_t>(a, s);
 }
 
 cudaError_t launch_reduce_by_key(const RbkArgs &a, ps_dtype key_dt, ps_dtype val_dt, cudaStream_t s) {
