@@ -47,13 +47,13 @@ def test_scans_on_concurrent_streams():
 
 def test_different_kernels_concurrently():
     n = (1 << 23) + 5
-    s1, s2, s3 = (torch.cuda.Stream(device=DEV) for _ in range(3))
+    s1, s2, s3, s4 = (torch.cuda.Stream(device=DEV) for _ in range(4))
     x = inputs.full_range_i32(n, 950)
     f = inputs.bernoulli_half(n, 951).astype(np.uint8)
     k = inputs.run_keys(n, 16, 952)
     xt, ft, kt = (torch.from_numpy(a).to(DEV) for a in (x, f, k))
     ws = [torch.zeros(max(api.workspace_size(torch.int32, n), api.reduce_by_key_workspace_size(torch.int32, n)),
-                      dtype=torch.uint8, device=DEV) for _ in range(3)]
+                      dtype=torch.uint8, device=DEV) for _ in range(4)]
     torch.cuda.synchronize()
     for rep in range(4):
         with torch.cuda.stream(s1):
@@ -62,6 +62,8 @@ def test_different_kernels_concurrently():
             sel, cnt = api.select(xt, ft, workspace=ws[1], stream=s2)
         with torch.cuda.stream(s3):
             uk, agg, runs = api.reduce_by_key(kt, xt, workspace=ws[2], stream=s3)
+        with torch.cuda.stream(s4):
+            uk2, lens, runs2 = api.run_length_encode(kt, workspace=ws[3], stream=s4)
     torch.cuda.synchronize()
     assert np.array_equal(y.cpu().numpy(), oracle.inclusive(x))
     want = oracle.select(x, f)
@@ -71,5 +73,9 @@ def test_different_kernels_concurrently():
     r = int(runs.item())
     assert r == ok_k.shape[0]
     assert np.array_equal(uk[:r].cpu().numpy(), ok_k) and np.array_equal(agg[:r].cpu().numpy(), ok_v)
+    lk, lc = oracle.reduce_by_key(k, None)
+    r = int(runs2.item())
+    assert r == lk.shape[0]
+    assert np.array_equal(uk2[:r].cpu().numpy(), lk) and np.array_equal(lens[:r].cpu().numpy(), lc)
     for w in ws:
         assert api.device_status(w) == _lib.PS_OK

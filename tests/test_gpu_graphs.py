@@ -65,6 +65,8 @@ def test_graph_of_several_kernels_sharing_one_workspace():
     sel = torch.empty_like(x)
     uk = torch.empty_like(k)
     agg = torch.empty_like(k)
+    uk2 = torch.empty_like(k)
+    lens = torch.empty_like(k)
     need = max(api.workspace_size(torch.int32, n), api.reduce_by_key_workspace_size(torch.int32, n))
     ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
     box = {}
@@ -74,6 +76,7 @@ def test_graph_of_several_kernels_sharing_one_workspace():
         api.scan(x, out=y, workspace=ws, stream=st)
         _, box["cnt"] = api.select(x, f, out=sel, workspace=ws, stream=st)
         _, _, box["runs"] = api.reduce_by_key(k, x, unique_keys=uk, aggregates=agg, workspace=ws, stream=st)
+        _, _, box["rle"] = api.run_length_encode(k, unique_keys=uk2, counts=lens, workspace=ws, stream=st)
 
     g = _capture(body)
     for seed in range(4):
@@ -93,4 +96,8 @@ def test_graph_of_several_kernels_sharing_one_workspace():
         r = int(box["runs"].item())
         assert r == okeys.shape[0]
         assert np.array_equal(uk[:r].cpu().numpy(), okeys) and np.array_equal(agg[:r].cpu().numpy(), ovals)
+        lkeys, lcounts = oracle.reduce_by_key(ks, None)
+        r = int(box["rle"].item())
+        assert r == lkeys.shape[0]
+        assert np.array_equal(uk2[:r].cpu().numpy(), lkeys) and np.array_equal(lens[:r].cpu().numpy(), lcounts)
     assert api.device_status(ws) == _lib.PS_OK

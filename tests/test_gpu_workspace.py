@@ -173,11 +173,12 @@ def test_stale_descriptors_of_other_epochs_are_ignored():
 
 
 def test_every_kernel_leaves_the_header_ready_for_the_next_call():
-    # The persistent scan, select, partition and reduce-by-key ready the
-    # header when their last CTA takes its last tile id, while other CTAs may
-    # still be storing; the one-tile-per-CTA fallback when its last CTA
-    # finishes.  After each: counter and done count 0, epoch + 1, and the
-    # results right -- including calls that run right after one another.
+    # The persistent scan, select, partition, reduce-by-key and run-length
+    # encoding ready the header when their last CTA takes its last tile id,
+    # while other CTAs may still be storing; the one-tile-per-CTA fallback
+    # when its last CTA finishes.  After each: counter and done count 0,
+    # epoch + 1, and the results right -- including calls that run right
+    # after one another.
     n = (1 << 21) + 77
     need = max(api.workspace_size(torch.int32, n), api.reduce_by_key_workspace_size(torch.int32, n))
     ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
@@ -210,6 +211,12 @@ def test_every_kernel_leaves_the_header_ready_for_the_next_call():
         r = int(runs.item())
         assert r == ok_k.shape[0] and np.array_equal(uk[:r].cpu().numpy(), ok_k)
         assert np.array_equal(agg[:r].cpu().numpy(), ok_v)
+        uk, lens, runs = api.run_length_encode(kt, workspace=ws)
+        epoch += 1
+        lk, lc = oracle.reduce_by_key(k, None)
+        r = int(runs.item())
+        assert r == lk.shape[0] and np.array_equal(uk[:r].cpu().numpy(), lk)
+        assert np.array_equal(lens[:r].cpu().numpy(), lc)
         h = header(ws)
         assert (h["tile_counter"], h["done"], h["epoch"]) == (0, 0, epoch), rep
         assert api.device_status(ws) == _lib.PS_OK
@@ -223,4 +230,13 @@ def test_every_kernel_leaves_the_header_ready_for_the_next_call():
     h = header(ws)
     assert (h["tile_counter"], h["done"], h["epoch"]) == (0, 0, 1)
     assert int(cnt.item()) == want.shape[0] and np.array_equal(sel[:want.shape[0]].cpu().numpy(), want)
+    # and run-length encoding as the call before a wrap
+    set_epoch(ws, EPOCH_MASK)
+    for want_epoch in (0, 1):
+        uk, lens, runs = api.run_length_encode(kt, workspace=ws)
+        h = header(ws)
+        assert (h["tile_counter"], h["done"], h["epoch"]) == (0, 0, want_epoch)
+        r = int(runs.item())
+        assert r == lk.shape[0] and np.array_equal(uk[:r].cpu().numpy(), lk)
+        assert np.array_equal(lens[:r].cpu().numpy(), lc)
     assert api.device_status(ws) == _lib.PS_OK
