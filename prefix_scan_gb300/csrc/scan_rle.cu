@@ -24,13 +24,15 @@
 // Structure as in the persistent scan and the select kernel: a producer warp
 // takes tile ids and bulk-copies the tile's keys -- starting one 16-byte
 // vector early, so the key before the tile (the "halo") is in shared memory
-// too -- into a 3-stage ring; an aggregator warp counts the tile's heads,
-// finds the last one and publishes the pair at once; a look-back warp
-// resolves the tile's exclusive pair; eight compute warps find the heads of
-// their rows, count them with a warp scan and write each head's key and the
-// length of the run it closes straight to global memory.  The compute warps
-// hand the stage back as soon as the keys are in registers.  Counts and
-// positions are 32-bit (n < 2^32).
+// too -- into a 3-stage ring; two aggregator warps count the heads of half
+// the tile each and find the last one, and the second to finish publishes
+// the tile's pair; a look-back warp resolves the tile's exclusive pair;
+// eight compute warps find the heads of their rows, count them with warp
+// scans and write each head's key and the length of the run it closes.  A
+// warp with few heads writes them straight from registers and hands the
+// stage back as soon as the keys are in registers; a warp dense in heads
+// packs each row's runs in its slice of the stage first, so that they go out
+// as contiguous ranges.  Counts and positions are 32-bit (n < 2^32).
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
 
