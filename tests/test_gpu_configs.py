@@ -54,3 +54,18 @@ def test_workload_full_size(w):
 @pytest.mark.parametrize("n", workloads.I32_INPLACE_SWEEP.sweep)
 def test_inplace_length_sweep(n):
     _run_and_check(workloads.I32_INPLACE_SWEEP, n)
+
+
+def test_inclusive_scan_above_2p31_elements():
+    # 2^31 + 12345 ones scanned in place: y[i] = i + 1 modulo 2^32 (as int32),
+    # past the 2^31 mark where 32-bit signed indices would overflow; checked
+    # on the device in chunks.
+    n, step = (1 << 31) + 12345, 1 << 28
+    x = torch.ones(n, dtype=torch.int32, device=DEV)
+    api.scan(x, inplace=True)
+    for s in range(0, n, step):
+        i = torch.arange(s, min(n, s + step), dtype=torch.int64, device=DEV) + 1
+        want = (i - (i >= 2 ** 31).to(torch.int64) * 2 ** 32).to(torch.int32)
+        assert torch.equal(x[s:s + i.numel()], want)
+    del x
+    torch.cuda.empty_cache()

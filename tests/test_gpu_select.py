@@ -127,3 +127,39 @@ def test_compaction_offsets_workload_full_size():
     want = oracle.select(x, f)
     assert k == want.shape[0]
     assert np.array_equal(out[:k].cpu().numpy(), want)
+
+
+def _wrap_i32(idx: torch.Tensor) -> torch.Tensor:
+    """int64 values as int32 modulo 2^32."""
+    return (idx - (idx >= 2 ** 31).to(torch.int64) * 2 ** 32).to(torch.int32)
+
+
+def test_select_and_partition_above_2p31():
+    # n > 2^31: output positions and counts need unsigned 32-bit arithmetic.
+    # x[i] = i (as int32, modulo 2^32), kept where i % 3 == 0; checked in
+    # chunks on the device against the closed forms: kept element j is
+    # x[3 j]; partition's r-th rejected element (at out[n-1-r]) is x[i] for
+    # i = 3 (r // 2) + 1 + r % 2.
+    n, step = (1 << 31) + 4099, 1 << 28
+    x = torch.empty(n, dtype=torch.int32, device=DEV)
+    f = torch.empty(n, dtype=torch.uint8, device=DEV)
+    for s in range(0, n, step):
+        idx = torch.arange(s, min(n, s + step), dtype=torch.int64, device=DEV)
+        x[s:s + idx.numel()] = _wrap_i32(idx)
+        f[s:s + idx.numel()] = (idx % 3 == 0).to(torch.uint8)
+    kept = (n + 2) // 3
+    out = torch.empty_like(x)
+    for part in (False, True):
+        _, cnt = (api.partition if part else api.select)(x, f, out=out)
+        assert int(cnt.item()) == kept
+        for s in range(0, kept, step):
+            j = torch.arange(s, min(kept, s + step), dtype=torch.int64, device=DEV)
+            assert torch.equal(out[s:s + j.numel()], _wrap_i32(3 * j))
+        if part:
+            rejected = n - kept
+            for s in range(0, rejected, step):
+                r = torch.arange(s, min(rejected, s + step), dtype=torch.int64, device=DEV)
+                got = out[n - 1 - (s + r.numel() - 1): n - s].flip(0)
+                assert torch.equal(got, _wrap_i32(3 * (r // 2) + 1 + r % 2))
+    del x, f, out
+    torch.cuda.empty_cache()
