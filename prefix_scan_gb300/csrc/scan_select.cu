@@ -42,6 +42,22 @@ constexpr int kSCW = kThreads / 32;   // compute warps per CTA
 #ifndef PS_SEL_FLAG_STAGES
 #define PS_SEL_FLAG_STAGES 2
 #endif
+// Look-back warps per CTA; warp j resolves iterations j, j + LB, ...  Two
+// for partition, whose 2 stages plus pack buffer hold each tile longer, so
+// that a CTA has two look-backs in flight: at 2^28, 436.6 -> 425.2 us; one
+// for select, which a second made slower (310.6 -> 319.1 us).  Macros so
+// that a tuning sweep can rebuild.
+#ifndef PS_SEL_LOOKBACK_WARPS
+#define PS_SEL_LOOKBACK_WARPS 1
+#endif
+#ifndef PS_PART_LOOKBACK_WARPS
+#define PS_PART_LOOKBACK_WARPS 2
+#endif
+template <bool PARTITION> constexpr int sel_lookback_warps() {
+    return PARTITION ? PS_PART_LOOKBACK_WARPS : PS_SEL_LOOKBACK_WARPS;
+}
+// compute, producer, aggregator and look-back warps
+template <bool PARTITION> constexpr int sel_threads() { return (kSCW + 2 + sel_lookback_warps<PARTITION>()) * 32; }
 template <typename T> struct SelItems { static constexpr int value = PS_SEL_ITEMS32; };
 template <> struct SelItems<int64_t> { static constexpr int value = kItems64; };
 
@@ -92,7 +108,7 @@ template <> __device__ __forceinline__ int64_t vget_t<int64_t>(const ulonglong2 
 
 
 template <typename T, int OP, bool PARTITION>
-__global__ void __launch_bounds__((kSCW + 3) * 32, kPCtasPerSm)
+__global__ void __launch_bounds__(sel_threads<PARTITION>(), kPCtasPerSm)
 select_kernel(SelectArgs a, long long num_tiles) {
     using V = typename Traits<T>::V;
     using U = uint32_t;                     // counts
@@ -105,6 +121,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
     constexpr uint32_t VAL_BYTES = (uint32_t)(TILE * sizeof(T));
     constexpr uint32_t FLAG_BYTES = OP == 0 ? (uint32_t)TILE : 0u;
     constexpr int CT = kSCW * 32;
+    constexpr int LB = sel_lookback_warps<PARTITION>();
     static_assert(ITEMS % VEC == 0, "ITEMS must be a multiple of the vector width");
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -156,13 +173,14 @@ select_kernel(SelectArgs a, long long num_tiles) {
     if (warp == kSCW) {
         // ---------------- producer ----------------
         if (lane == 0) {
+            int ends = 0;   // end markers sent: one per look-back warp
             for (long long k = 0;; ++k) {
                 const int s = (int)(k % S);
                 if (k >= S && !mbar_wait(&empty[s], (uint32_t)((k / S - 1) & 1))) {
                     report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                     break;
                 }
-                const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
+                const long long t = ends ? num_tiles : (long long)atomicAdd(&hdr->tile_counter, 1ull);
                 tile_of[k % R] = t;
                 if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     mbar_arrive_expect_tx(&full[s], VAL_BYTES + FLAG_BYTES);
@@ -171,12 +189,13 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 } else {
                     mbar_arrive(&full[s]);   // end marker, or a tile read from global
                 }
-                if (t >= num_tiles) break;
+                if (t >= num_tiles && ++ends == LB) break;
             }
             if (epoch != kEpochMask) claims_done(hdr, a.ws_bytes, epoch);
         }
     } else if (warp == kSCW + 1) {
         // ---------------- aggregator: count and publish ----------------
+        int ends = 0;   // end markers passed on: one per look-back warp
         for (long long k = 0;; ++k) {
             const int s = (int)(k % S);
             if (!mbar_wait(&full[s], (uint32_t)((k / S) & 1))) {
@@ -185,9 +204,10 @@ select_kernel(SelectArgs a, long long num_tiles) {
             }
             const int slot = (int)(k % R);
             const long long tile = tile_of[slot];
-            if (tile < 0 || tile >= num_tiles) {
+            if (tile < 0 || tile >= num_tiles) {   // end marker: pass it on to the look-back warps
                 if (lane == 0) mbar_arrive(&agg_done[slot]);
-                break;
+                if (++ends == LB) break;
+                continue;
             }
             const unsigned long long base = (unsigned long long)tile * TILE;
             U cnt = 0;
@@ -226,9 +246,10 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 mbar_arrive(&agg_done[slot]);
             }
         }
-    } else if (warp == kSCW + 2) {
-        // ---------------- look-back: the tile's output offset ----------------
-        for (long long k = 0;; ++k) {
+    } else if (warp >= kSCW + 2) {
+        // ---------------- look-back warps: the tile's output offset ----------------
+        // warp j takes iterations j, j + LB, ...
+        for (long long k = warp - (kSCW + 2);; k += LB) {
             const int slot = (int)(k % R);
             if (!mbar_wait(&agg_done[slot], (uint32_t)((k / R) & 1))) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
@@ -393,7 +414,7 @@ static cudaError_t launch_select_variant(const SelectArgs &a, cudaStream_t s) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     long long grid = (long long)sms * kPCtasPerSm;
     if (grid > tiles) grid = tiles;
-    select_kernel<T, OP, PARTITION><<<(unsigned int)grid, (kSCW + 3) * 32, smem, s>>>(a, tiles);
+    select_kernel<T, OP, PARTITION><<<(unsigned int)grid, sel_threads<PARTITION>(), smem, s>>>(a, tiles);
     return cudaGetLastError();
 }
 
