@@ -63,6 +63,9 @@ constexpr int kRbkThreads = (kRCW + 1 + kLB + kAgg) * 32;   // compute, producer
 #define PS_RBK_LOOKBACK_K PS_LOOKBACK_K
 #endif
 
+// Position of packed entry q in a warp's slice: XOR-swizzled within each 32
+// entries (a permutation of the block, so the slice's bounds hold).
+__device__ __forceinline__ uint32_t rbk_sw(uint32_t q) { return q ^ ((q >> 5) & 7u); }
 __device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity) {
     return PS_RBK_WAIT_NS ? mbar_wait_suspend(bar, parity, PS_RBK_WAIT_NS) : mbar_wait(bar, parity);
 }
@@ -144,13 +147,18 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     constexpr int VK = KV::N;
     constexpr long long TILE = rbk_tile<KU>();
     constexpr int ITEMS = (int)(TILE / kThreads);
-    constexpr int ROWS = ITEMS / VK;
+    // A compute lane's share of a row: two key vectors (EPL keys) and their
+    // EPL 32-bit values (one or two 16-byte vectors), so that a tile takes
+    // half as many segmented warp scans as with one key vector per row.
+    constexpr int EPL = 2 * VK;
+    constexpr int ROWS = ITEMS / EPL;
+    constexpr int WV = EPL / 4;   // 16-byte value vectors per lane per row
     constexpr int S = kRStages;
     constexpr uint32_t KEY_BYTES = rbk_key_bytes<KU>();
     constexpr uint32_t STAGE = rbk_stage_bytes<KU>();
     constexpr uint32_t VAL_BYTES = (uint32_t)(TILE * 4);
     constexpr int CT = kRCW * 32;
-    static_assert(ITEMS % VK == 0 && STAGE % 16 == 0, "tile geometry");
+    static_assert(ITEMS % EPL == 0 && (WV == 1 || WV == 2) && STAGE % 16 == 0, "tile geometry");
 
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * STAGE);
@@ -381,32 +389,52 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             const bool staged = a.use_bulk && base + TILE <= n;
             const int seg = warp * 32 * ITEMS;
 
-            KU kk[ROWS][VK];
-            uint32_t vv[ROWS][VK];
+            KU kk[ROWS][EPL];
+            uint32_t vv[ROWS][EPL];
             uint32_t hm[ROWS];              // bit j: element j of this lane's chunk opens a run
             uint32_t offc[ROWS], offv[ROWS];   // exclusive pair of the chunk within the warp
             uint32_t rc = 0u, rv = 0u;      // pair of the warp's rows so far
             const uint32_t lt_mask = (1u << lane) - 1u;
+            // lanes 4-7 of each quarter-warp read a pair of 16-byte vectors
+            // in swapped order, so that the quarter-warp's reads fall in
+            // distinct bank groups; the pair is put back in order in registers
+            const int rot = (lane >> 2) & 1;
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
-                const int e0 = seg + (r * 32 + lane) * VK;   // tile-local index of the chunk
+                const int e0 = seg + (r * 32 + lane) * EPL;   // tile-local index of the chunk
                 uint32_t m = 0;
                 if (staged) {
                     const KU *ks = stage_keys(s);
-                    const V x = reinterpret_cast<const V *>(ks)[e0 / VK];
-#pragma unroll
-                    for (int j = 0; j < VK; ++j) kk[r][j] = KV::key(x, j);
-                    KU prev = __shfl_up_sync(kFull, kk[r][VK - 1], 1);
-                    if (lane == 0) prev = ks[e0 - 1];   // e0 == 0 reads the halo
-#pragma unroll
-                    for (int j = 0; j < VK; ++j) m |= (uint32_t)(kk[r][j] != (j ? kk[r][j - 1] : prev)) << j;
-                    if (tile == 0 && e0 == 0) m |= 1u;
-                    const W w = reinterpret_cast<const W *>(stage_vals(s))[e0 / VK];
-#pragma unroll
-                    for (int j = 0; j < VK; ++j) vv[r][j] = KV::val(w, j);
-                } else {
+                    const V *kv = reinterpret_cast<const V *>(ks) + e0 / VK;
+                    const V x0 = kv[rot], x1 = kv[rot ^ 1];
+                    const V klo = rot ? x1 : x0, khi = rot ? x0 : x1;
 #pragma unroll
                     for (int j = 0; j < VK; ++j) {
+                        kk[r][j] = KV::key(klo, j);
+                        kk[r][VK + j] = KV::key(khi, j);
+                    }
+                    KU prev = __shfl_up_sync(kFull, kk[r][EPL - 1], 1);
+                    if (lane == 0) prev = ks[e0 - 1];   // e0 == 0 reads the halo
+#pragma unroll
+                    for (int j = 0; j < EPL; ++j) m |= (uint32_t)(kk[r][j] != (j ? kk[r][j - 1] : prev)) << j;
+                    if (tile == 0 && e0 == 0) m |= 1u;
+                    const uint4 *wv = reinterpret_cast<const uint4 *>(stage_vals(s)) + e0 / 4;
+                    if constexpr (WV == 2) {
+                        const uint4 w0 = wv[rot], w1 = wv[rot ^ 1];
+                        const uint4 vlo = rot ? w1 : w0, vhi = rot ? w0 : w1;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            vv[r][j] = vget(vlo, j);
+                            vv[r][4 + j] = vget(vhi, j);
+                        }
+                    } else {
+                        const uint4 w = wv[0];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) vv[r][j] = vget(w, j);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < EPL; ++j) {
                         const unsigned long long i = base + (unsigned long long)(e0 + j);
                         if (i < n) {
                             kk[r][j] = keys[i];
@@ -432,7 +460,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             for (int r = 0; r < ROWS; ++r) {
                 uint32_t v = 0u;
 #pragma unroll
-                for (int j = 0; j < VK; ++j) {
+                for (int j = 0; j < EPL; ++j) {
                     const bool h = (hm[r] >> j) & 1u;
                     const uint32_t sum = RunValue<VU>::add(v, vv[r][j]);
                     v = h ? vv[r][j] : sum;
@@ -484,7 +512,9 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             // over -- keyed by run index relative to the warp's first run,
             // then write them out as two contiguous ranges: keys of runs
             // cw .. cw+rc-1 and values of runs cw-1 .. cw+rc-2 (each head
-            // closes the run before it).
+            // closes the run before it).  Entries are XOR-swizzled within
+            // each 32 (rbk_sw), so lanes packing entries EPL apart (every key
+            // a head) and lanes reading 32 consecutive ones hit distinct banks.
             const uint32_t cw = pair_count(pre), pv = pair_value(pre);
             KU *pk = stage_keys(s) + seg;
             uint32_t *pvals = stage_vals(s) + seg;
@@ -493,11 +523,11 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 uint32_t q = offc[r];   // run index - cw of this chunk's first head
                 uint32_t v = offc[r] ? offv[r] : RunValue<VU>::add(pv, offv[r]);
 #pragma unroll
-                for (int j = 0; j < VK; ++j) {
+                for (int j = 0; j < EPL; ++j) {
                     const bool h = (hm[r] >> j) & 1u;
                     if (h) {
-                        pk[q] = kk[r][j];
-                        pvals[q] = v;
+                        pk[rbk_sw(q)] = kk[r][j];
+                        pvals[rbk_sw(q)] = v;
                     }
                     const uint32_t sum = RunValue<VU>::add(v, vv[r][j]);
                     v = h ? vv[r][j] : sum;
@@ -506,8 +536,8 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             }
             __syncwarp();
             for (uint32_t q = lane; q < rc; q += 32) {
-                ukeys[cw + q] = pk[q];
-                if (cw + q > 0u) aggs[cw + q - 1u] = pvals[q];
+                ukeys[cw + q] = pk[rbk_sw(q)];
+                if (cw + q > 0u) aggs[cw + q - 1u] = pvals[rbk_sw(q)];
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
