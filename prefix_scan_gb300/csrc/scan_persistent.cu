@@ -37,6 +37,8 @@
 // warps read it from global memory with bounds checks.  Every wait on an
 // mbarrier is bounded; a wait that runs out records PS_ERR_LOOKBACK_TIMEOUT
 // and the loop moves on (results are then unspecified, but the kernel ends).
+#include <type_traits>
+
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
 
@@ -67,6 +69,12 @@ constexpr bool kEarlyRelease = PS_PERSIST_EARLY_RELEASE != 0;
 // vector element (two independent add-with-carry chains instead of one).
 #ifndef PS_PERSIST_AGG_SPLIT64
 #define PS_PERSIST_AGG_SPLIT64 1
+#endif
+// ... and of an fp32 scan one per vector element: four FADD chains of 64
+// instead of one of 256 (the order of an fp32 tile sum is unspecified
+// anyway; integer sums fold two additions per IADD3 already).
+#ifndef PS_PERSIST_AGG_SPLIT_F32
+#define PS_PERSIST_AGG_SPLIT_F32 1
 #endif
 constexpr int kRing = kEarlyRelease ? 2 * kPStages : kPStages;   // hand-off slots: iteration k uses k % kRing
 // per stage: full, empty; per hand-off slot: agg_done, prefix_ready, tile id, aggregate, prefix
@@ -209,7 +217,8 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             U agg;
             if constexpr (Op::kCommutative) {
                 // each lane folds every 32nd vector; the order does not matter
-                constexpr int AC = (sizeof(U) == 8 && PS_PERSIST_AGG_SPLIT64) ? VEC : 1;
+                constexpr int AC = (sizeof(U) == 8 && PS_PERSIST_AGG_SPLIT64) ? VEC
+                                   : (std::is_same<U, float>::value && PS_PERSIST_AGG_SPLIT_F32) ? VEC : 1;
                 U accs[AC];
 #pragma unroll
                 for (int c = 0; c < AC; ++c) accs[c] = ident;
