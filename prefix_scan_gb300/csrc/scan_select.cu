@@ -373,12 +373,18 @@ select_kernel(SelectArgs a, long long num_tiles) {
                                                                                     : (U)(n - w_first));
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
+                    // c: kept elements of the warp before element e (a running
+                    // count over the chunk); a rejected element goes after the
+                    // warp's kept ones, at its count of rejected predecessors
+                    U c = off[r];
+                    const U e0 = (U)((r * 32 + lane) * VEC);   // index within the warp's slice
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
-                        const U e = (U)((r * 32 + lane) * VEC + j);   // index within the warp's slice
-                        const U sel_before = off[r] + (U)__popc(sel[r] & ((1u << j) - 1u));
-                        if ((sel[r] >> j) & 1u) wbuf[sel_before] = v[r][j];
-                        else if (e < w_valid) wbuf[w_sel + (e - sel_before)] = v[r][j];
+                        const U e = e0 + (U)j;
+                        const bool kp = (sel[r] >> j) & 1u;
+                        const U pos = kp ? c : w_sel + (e - c);
+                        if (kp || e < w_valid) wbuf[pos] = v[r][j];
+                        c += kp ? 1u : 0u;
                     }
                 }
                 __syncwarp();
