@@ -56,6 +56,42 @@ def hbm_peak() -> tuple[float, str]:
 
 # ---------------------------------------------------------------- clocks ----
 
+def nvml_handle(torch_device_index: int):
+    """(NVML library, device handle) for a torch CUDA device, matched by PCI
+    bus id (NVML and CUDA may number devices differently); read-only use."""
+    import torch
+    props = torch.cuda.get_device_properties(torch_device_index)
+    bus = (f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:"
+           f"{props.pci_device_id:02X}.0")
+    nv = ctypes.CDLL("libnvidia-ml.so.1")
+    if nv.nvmlInit_v2() != 0:
+        raise RuntimeError("nvmlInit failed")
+    h = ctypes.c_void_p()
+    if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+        raise RuntimeError("no NVML handle for " + bus)
+    return nv, h
+
+
+def bind_to_gpu_cpus(torch_device_index: int) -> str:
+    """Runs this process on the CPUs that NVML reports as local to the GPU,
+    so that pinned host buffers allocated afterwards sit on the GPU's NUMA
+    node (a host-side setting of this process only).  Returns what it did."""
+    try:
+        nv, h = nvml_handle(torch_device_index)
+        words = ((os.cpu_count() or 64) + 63) // 64
+        mask = (ctypes.c_ulong * words)()
+        if nv.nvmlDeviceGetCpuAffinity(h, ctypes.c_uint(words), mask) != 0:
+            return "unbound (NVML reported no CPU affinity)"
+        bits = 8 * ctypes.sizeof(ctypes.c_ulong)
+        cpus = {w * bits + b for w in range(words) for b in range(bits) if (mask[w] >> b) & 1}
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return "unbound (no GPU-local CPU available)"
+        os.sched_setaffinity(0, cpus)
+        return f"bound to the {len(cpus)} CPUs local to the GPU"
+    except Exception as exc:   # no NVML: run where the OS placed us
+        return f"unbound ({type(exc).__name__})"
+
 class ClockSampler:
     """Samples SM clock, power and clock-event reasons during a region.
 
@@ -77,16 +113,7 @@ class ClockSampler:
         self._nvml = None
         self._handle = None
         try:
-            import torch
-            props = torch.cuda.get_device_properties(torch_device_index)
-            bus = (f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:"
-                   f"{props.pci_device_id:02X}.0")
-            nv = ctypes.CDLL("libnvidia-ml.so.1")
-            if nv.nvmlInit_v2() != 0:
-                raise RuntimeError("nvmlInit failed")
-            h = ctypes.c_void_p()
-            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
-                raise RuntimeError("no NVML handle for " + bus)
+            nv, h = nvml_handle(torch_device_index)
             mx = ctypes.c_uint()
             if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
                 self.max_mhz = mx.value
@@ -453,6 +480,7 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
         nvbuild.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    host_binding = bind_to_gpu_cpus(local)   # before any pinned host buffer exists
     w = workloads.BY_NAME[args.workload]
     n = args.n or w.n
     h = Harness(w, n, dev)
@@ -525,7 +553,8 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": n * w.itemsize, "d2h_bytes_per_step": n * w.itemsize,
                 "steps": e2e_steps,
-                "path": "ps_scan_host: pinned host buffers, 32 MiB chunks in 3 device buffers, H2D/scan/D2H overlapped"},
+                "path": "ps_scan_host: pinned host buffers, 32 MiB chunks in 3 device buffers, H2D/scan/D2H overlapped",
+                "host_cpus": host_binding},
         "gpu_launches": args.steps * h.launches_per_step,
         "clocks": sampler.summary(),
         "parity_spot_check": ok,
