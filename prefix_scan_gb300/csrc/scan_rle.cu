@@ -72,6 +72,23 @@ __device__ __forceinline__ bool rle_wait(uint64_t *bar, uint32_t parity) {
     return PS_RLE_WAIT_NS ? mbar_wait_suspend(bar, parity, PS_RLE_WAIT_NS) : mbar_wait(bar, parity);
 }
 
+// k[j] for a j known only at run time, without local memory: a tree of
+// selects on the bits of j (E - 1 selects on log2(E) bit tests).
+template <typename KU, int E>
+__device__ __forceinline__ KU pick(const KU (&k)[E], int j) {
+    static_assert(E == 4 || E == 8, "four or eight keys");
+    const bool b0 = j & 1, b1 = j & 2;
+    const KU a0 = b0 ? k[1] : k[0], a1 = b0 ? k[3] : k[2];
+    const KU lo = b1 ? a1 : a0;
+    if constexpr (E == 4) {
+        return lo;
+    } else {
+        const KU a2 = b0 ? k[5] : k[4], a3 = b0 ? k[7] : k[6];
+        const KU hi = b1 ? a3 : a2;
+        return (j & 4) ? hi : lo;
+    }
+}
+
 // (heads << 32 | position of the last head); `a` is the earlier part.
 struct OpRle {
     static constexpr bool kCommutative = true;
@@ -451,9 +468,7 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                     uint32_t prev = (w >> 30) ? wbase + ((w >> 19) & 0x7ffu) : pw;
                     for (uint32_t mm = w & 0xffu; mm; mm &= mm - 1u) {
                         const int j = __ffs(mm) - 1;
-                        KU key = kk[r][0];
-#pragma unroll
-                        for (int q = 1; q < EPL; ++q) key = j == q ? kk[r][q] : key;
+                        const KU key = pick<KU, EPL>(kk[r], j);
                         ukeys[c] = key;
                         if (c > 0u) counts[c - 1u] = pos0 + (uint32_t)j - prev;
                         prev = pos0 + (uint32_t)j;
@@ -479,9 +494,7 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                     uint32_t q = rb - first;
                     for (uint32_t mm = w & 0xffu; mm; mm &= mm - 1u) {
                         const int j = __ffs(mm) - 1;
-                        KU key = kk[r][0];
-#pragma unroll
-                        for (int t = 1; t < EPL; ++t) key = j == t ? kk[r][t] : key;
+                        const KU key = pick<KU, EPL>(kk[r], j);
                         pk[rle_sw(q)] = key;
                         pp[rle_sw(q)] = (uint32_t)((r * 32 + lane) * EPL + j);
                         ++q;
