@@ -47,13 +47,13 @@ def test_scans_on_concurrent_streams():
 
 def test_different_kernels_concurrently():
     n = (1 << 23) + 5
-    s1, s2, s3, s4 = (torch.cuda.Stream(device=DEV) for _ in range(4))
+    s1, s2, s3, s4, s5 = (torch.cuda.Stream(device=DEV) for _ in range(5))
     x = inputs.full_range_i32(n, 950)
     f = inputs.bernoulli_half(n, 951).astype(np.uint8)
     k = inputs.run_keys(n, 16, 952)
     xt, ft, kt = (torch.from_numpy(a).to(DEV) for a in (x, f, k))
     ws = [torch.zeros(max(api.workspace_size(torch.int32, n), api.reduce_by_key_workspace_size(torch.int32, n)),
-                      dtype=torch.uint8, device=DEV) for _ in range(4)]
+                      dtype=torch.uint8, device=DEV) for _ in range(5)]
     torch.cuda.synchronize()
     for rep in range(4):
         with torch.cuda.stream(s1):
@@ -64,11 +64,15 @@ def test_different_kernels_concurrently():
             uk, agg, runs = api.reduce_by_key(kt, xt, workspace=ws[2], stream=s3)
         with torch.cuda.stream(s4):
             uk2, lens, runs2 = api.run_length_encode(kt, workspace=ws[3], stream=s4)
+        with torch.cuda.stream(s5):
+            part, pcnt = api.partition(xt, ft, workspace=ws[4], stream=s5)
     torch.cuda.synchronize()
     assert np.array_equal(y.cpu().numpy(), oracle.inclusive(x))
     want = oracle.select(x, f)
     m = int(cnt.item())
     assert m == want.shape[0] and np.array_equal(sel[:m].cpu().numpy(), want)
+    pw, pk = oracle.partition(x, f)
+    assert int(pcnt.item()) == pk == m and np.array_equal(part.cpu().numpy(), pw)
     ok_k, ok_v = oracle.reduce_by_key(k, x)
     r = int(runs.item())
     assert r == ok_k.shape[0]

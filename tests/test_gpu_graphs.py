@@ -63,6 +63,7 @@ def test_graph_of_several_kernels_sharing_one_workspace():
     k = torch.empty(n, dtype=torch.int32, device=DEV)
     y = torch.empty_like(x)
     sel = torch.empty_like(x)
+    part = torch.empty_like(x)
     uk = torch.empty_like(k)
     agg = torch.empty_like(k)
     uk2 = torch.empty_like(k)
@@ -75,6 +76,7 @@ def test_graph_of_several_kernels_sharing_one_workspace():
         st = torch.cuda.current_stream(DEV)
         api.scan(x, out=y, workspace=ws, stream=st)
         _, box["cnt"] = api.select(x, f, out=sel, workspace=ws, stream=st)
+        _, box["pcnt"] = api.partition(x, f, out=part, workspace=ws, stream=st)
         _, _, box["runs"] = api.reduce_by_key(k, x, unique_keys=uk, aggregates=agg, workspace=ws, stream=st)
         _, _, box["rle"] = api.run_length_encode(k, unique_keys=uk2, counts=lens, workspace=ws, stream=st)
 
@@ -92,6 +94,9 @@ def test_graph_of_several_kernels_sharing_one_workspace():
         want = oracle.select(xs, fs)
         m = int(box["cnt"].item())
         assert m == want.shape[0] and np.array_equal(sel[:m].cpu().numpy(), want)
+        pw, pk = oracle.partition(xs, fs)
+        assert int(box["pcnt"].item()) == pk == m
+        assert np.array_equal(part.cpu().numpy(), pw)
         okeys, ovals = oracle.reduce_by_key(ks, xs)
         r = int(box["runs"].item())
         assert r == okeys.shape[0]
