@@ -69,3 +69,29 @@ def test_inclusive_scan_above_2p31_elements():
         assert torch.equal(x[s:s + i.numel()], want)
     del x
     torch.cuda.empty_cache()
+
+
+def test_scans_past_2p32_elements_and_int64_past_2p31():
+    # 2^32 + 5 int32 ones in place (y[i] = i + 1 modulo 2^32: element and tile
+    # indices past 32 bits), and 2^31 + 5 int64 ones (y[i] = i + 1 exactly);
+    # each checked on the device in chunks against the closed form
+    step = 1 << 28
+    n = (1 << 32) + 5
+    x = torch.ones(n, dtype=torch.int32, device=DEV)
+    api.scan(x, inplace=True)
+    for s in range(0, n, step):
+        i = torch.arange(s, min(n, s + step), dtype=torch.int64, device=DEV) + 1
+        want = (i % (1 << 32))
+        want = (want - (want >= 2 ** 31).to(torch.int64) * 2 ** 32).to(torch.int32)
+        assert torch.equal(x[s:s + i.numel()], want), s
+    del x
+    torch.cuda.empty_cache()
+    n = (1 << 31) + 5
+    x = torch.ones(n, dtype=torch.int64, device=DEV)
+    y = api.scan_inclusive(x)
+    del x
+    for s in range(0, n, step):
+        i = torch.arange(s, min(n, s + step), dtype=torch.int64, device=DEV) + 1
+        assert torch.equal(y[s:s + i.numel()], i), s
+    del y
+    torch.cuda.empty_cache()
