@@ -197,3 +197,50 @@ def test_pair_scan_argument_errors(lib, no_device):
         assert f(0, FAKE, FAKE + (1 << 20), n, FAKE + (2 << 20), ws - 1, None) == _lib.PS_ERR_WORKSPACE_TOO_SMALL
         assert f(1, FAKE, FAKE + 800, n, FAKE + (2 << 20), ws, None) == _lib.PS_ERR_OVERLAP
         assert f(0, None, FAKE, n, FAKE + (2 << 20), ws, None) == _lib.PS_ERR_INVALID_ARG
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "prefix_scan.h"
+#include "prefix_scan_testing.h"
+
+int main(void) {
+    /* host-only calls: no device is touched */
+    size_t ws = ps_scan_workspace_size(PS_INT32, 1000000);
+    size_t rbk = ps_reduce_by_key_workspace_size(PS_INT64, 1000000);
+    size_t tile = ps_tile_elements(PS_FLOAT32);
+    ps_status bad = ps_scan_inclusive_i32(NULL, NULL, 5, NULL, 0, NULL);
+    ps_status none = ps_scan_exclusive_i64(NULL, NULL, 0, NULL, 0, NULL);
+    printf("%zu %zu %zu %d %d %zu %s\n", ws, rbk, tile, (int)bad, (int)none,
+           ps_testing_descriptor_bytes(PS_INT64), ps_status_string(PS_ERR_OVERLAP));
+    return 0;
+}
+"""
+
+
+def test_headers_serve_a_plain_c99_client(lib, tmp_path):
+    # The boundary is a C ABI: both headers compile as strict C99 and a C
+    # program links against the library and gets the same answers as the
+    # binding (host-only calls; no GPU is needed).
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = Path(nvbuild.LIBRARY).parent
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{INCLUDE}", str(src),
+                        "-o", str(exe), f"-L{libdir}", "-lprefixscan", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    ws, rbk, tile, bad, none, db, overlap = r.stdout.split(maxsplit=6)
+    assert int(ws) == lib.ps_scan_workspace_size(0, 1000000) > 0
+    assert int(rbk) == lib.ps_reduce_by_key_workspace_size(1, 1000000) > 0
+    assert int(tile) == lib.ps_tile_elements(2)
+    assert int(bad) == 1 and int(none) == 0   # PS_ERR_INVALID_ARG for NULL with n > 0; n == 0 is a no-op
+    assert overlap.strip() and int(db) == lib.ps_testing_descriptor_bytes(1)
