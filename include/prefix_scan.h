@@ -383,8 +383,12 @@ size_t ps_tile_elements(ps_dtype dtype);
  *     whose GPU work can overlap (other streams, unordered host threads)
  *     race on it and produce wrong results; calls ordered on one stream are
  *     safe.
- *   - Device-side timeouts can be read with ps_get_device_status only
- *     through the regular entry points (there is no caller workspace here).
+ *   - Every call looks the array's address up again (a host-side look-up):
+ *     cudaDeviceReset destroys the loaded copy of the array, and the next
+ *     call finds, and if it moved zero-fills, the new one.
+ *   - There is no caller workspace to pass to ps_get_device_status; the
+ *     test hook ps_testing_noalloc_scratch (prefix_scan_testing.h) gives
+ *     the array's address for that.
  */
 #define PS_NOALLOC_MAX_ELEMENTS 536870912u /* 2^29 elements */
 #define PS_NOALLOC_SCRATCH_BYTES (256u + 72u * (PS_NOALLOC_MAX_ELEMENTS / 8192u)) /* 4.5 MiB + 256 */

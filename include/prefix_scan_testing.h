@@ -58,6 +58,16 @@ ps_status ps_testing_lookback(ps_dtype dtype, const void *desc, int64_t tile, ui
 ps_status ps_testing_workspace_epoch(const void *ws, ps_stream_t stream, uint32_t *epoch);
 ps_status ps_testing_set_workspace_epoch(void *ws, uint32_t epoch, ps_stream_t stream);
 
+/*
+ * The device address (for the current device) of the fixed scratch array
+ * that ps_scan_inclusive_i32_noalloc uses in place of a workspace, written
+ * to *scratch, so that a test can read the status of the last such call
+ * with ps_get_device_status(*scratch, ...).  Does the same set-up as a
+ * first ps_scan_inclusive_i32_noalloc call on the device (the zero-fill is
+ * enqueued on `stream`).  PS_ERR_CUDA if the look-up fails.
+ */
+ps_status ps_testing_noalloc_scratch(void **scratch, ps_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,11 +20,15 @@
 //   - it keeps what the last call left there, which is exactly the state the
 //     next call needs (a workspace is zero-filled once and every call leaves
 //     it ready for the next); the first call on a device zero-fills it.
+//   - cudaDeviceReset destroys the device's context and with it the loaded
+//     copy of the array; the next call finds a fresh (zeroed) copy, possibly
+//     at another address, which is why every call looks the address up.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "prefix_scan.h"
+#include "prefix_scan_testing.h"
 #include "scan_internal.h"
 
 namespace {
@@ -42,29 +46,33 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PS_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+void *g_scratch_ptr[kMaxDevices] = {};   // address the set-up zero-filled, per device
 
-// Once per device, with that device current: look up the device address of
-// the scratch array and zero-fill it on the caller's stream.  Looking up the
-// symbol may load the library's device code onto the device, which is why
-// the first call on a device should not be made while a stream is being
-// captured.
+// With the device current: the device address of the scratch array.  The
+// look-up runs on every call, because the address belongs to the device's
+// current context: after cudaDeviceReset the library's device code is loaded
+// again and the array may sit elsewhere.  Set-up, once per device and again
+// whenever the address moved: zero-fill the array on the caller's stream.
+// The first look-up on a device may load the library's device code onto it,
+// which is why the first call on a device should not be made while a
+// stream is being captured.
 cudaError_t scratch_for_current_device(cudaStream_t stream, void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        // a workspace starts zero-filled; device globals are, but make sure
+    if (g_scratch_ptr[dev] != p) {
+        // a workspace starts zero-filled; a freshly loaded device array is,
+        // but make sure
         e = cudaMemsetAsync(p, 0, PS_NOALLOC_SCRATCH_BYTES, stream);
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -81,4 +89,16 @@ extern "C" ps_status ps_scan_inclusive_i32_noalloc(const int32_t *in, int32_t *o
         return PS_ERR_CUDA;
     }
     return ps_scan_inclusive_i32(in, out, n, scratch, PS_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// Test hook: the device address of the current device's scratch array, so
+// that a test can read its status word with ps_get_device_status.
+extern "C" ps_status ps_testing_noalloc_scratch(void **scratch, ps_stream_t stream) {
+    if (scratch == nullptr) return PS_ERR_INVALID_ARG;
+    const cudaError_t e = scratch_for_current_device((cudaStream_t)stream, scratch);
+    if (e != cudaSuccess) {
+        ps::note_cuda_error(e);
+        return PS_ERR_CUDA;
+    }
+    return PS_OK;
 }
