@@ -47,16 +47,13 @@ def is_fresh() -> bool:
     return all(p.stat().st_mtime <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> Path:
-    """Compile and link the library; returns its path (no-op when fresh)."""
-    if not force and not ptxas_info and is_fresh():
-        return LIBRARY
+def _compile_and_link(srcs: list[Path], obj_dir: Path, target: Path, extra: list[str],
+                      verbose: bool) -> Path:
     nvcc = nvcc_path()
-    BUILD_DIR.mkdir(exist_ok=True)
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    obj_dir.mkdir(parents=True, exist_ok=True)
 
     def compile_one(src: Path) -> tuple[Path, str]:
-        obj = BUILD_DIR / (src.stem + ".o")
+        obj = obj_dir / (src.stem + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", str(src), "-o", str(obj)]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,17 +61,48 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         return obj, r.stderr
 
     with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
-        results = list(ex.map(compile_one, sources()))
-    if verbose or ptxas_info:
+        results = list(ex.map(compile_one, srcs))
+    if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIBRARY.with_name(LIBRARY.name + f".{os.getpid()}.tmp")
+    tmp = target.with_name(target.name + f".{os.getpid()}.tmp")
     cmd = [nvcc, *ARCH, "-shared", "-o", str(tmp), *[str(o) for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
-    os.replace(tmp, LIBRARY)
-    return LIBRARY
+    os.replace(tmp, target)
+    return target
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> Path:
+    """Compile and link the library; returns its path (no-op when fresh)."""
+    if not force and not ptxas_info and is_fresh():
+        return LIBRARY
+    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    return _compile_and_link(sources(), BUILD_DIR, LIBRARY, extra, verbose or ptxas_info)
+
+
+# Smallest tile geometry the scan and select kernels accept: four elements
+# per thread, so tiles of 1024 elements (256 threads) for every element
+# type -- eight times as many tiles, look-backs and descriptor hand-offs per
+# byte as the product build.  The reduce-by-key and run-length kernels keep
+# their own fixed tiles.  The allocation-free entry point is left out: its
+# fixed scratch is sized for the product geometry.
+TINY_TILE_DEFINES = {"PS_ITEMS32": 4, "PS_ITEMS64": 4}
+
+
+def build_variant(name: str, defines: dict[str, int], exclude: tuple[str, ...] = ("scan_noalloc.cu",),
+                  force: bool = False) -> Path:
+    """Build a second copy of the library with other geometry macros, for
+    stress tests: ``_build/<name>/libprefixscan_<name>.so`` (not the
+    product library).  No-op when it is newer than every source."""
+    obj_dir = BUILD_DIR / name
+    target = obj_dir / f"libprefixscan_{name}.so"
+    if not force and target.exists() and all(p.stat().st_mtime <= target.stat().st_mtime for p in _deps()):
+        return target
+    srcs = [p for p in sources() if p.name not in exclude]
+    extra = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    return _compile_and_link(srcs, obj_dir, target, extra, False)
 
 
 if __name__ == "__main__":
