@@ -9,7 +9,12 @@ plus Gelem/s and the ratio to a device-to-device memcpy of the same bytes
 timed in the same run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--sweep] [--compare]
+                  [--impl ours|reference] [--no-configs] [--compare] [--compaction]
+                  [--ops] [--rbk]
+
+The line's ``configs`` key times every other workload the same way (the
+in-place workload at each of its lengths), so one default run covers them
+all; the headline stays the 2^28 int32 exclusive scan.
 
 --impl reference times the CPU oracle (the plain sequential scan) on the
 host cores on a bounded sample of the same workload.  With N > 1 (torchrun)
@@ -227,7 +232,7 @@ def replica_stats(local_seconds: float, local_units: float, world: int) -> tuple
     return max_over_ranks(local_seconds, world), sum_over_ranks(local_units, world)
 
 
-KERNEL_TRAFFIC_FILE = ROOT / "profiles" / "persistent_kernel_i32_excl_2p28_traffic.md"
+KERNEL_TRAFFIC_FILE = ROOT / "profiles" / "persistent_kernel_i32_excl_2p26_traffic.md"
 
 
 # The headline kernel's translation unit and the headers it includes: a
@@ -254,20 +259,31 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str, n: int):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    summary is for another workload or the kernel sources changed since."""
+def recorded_traffic(w: workloads.Workload, n: int):
+    """DRAM bytes per launch for ``n`` elements of workload ``w``, from the
+    committed ncu summary of a smaller launch of the same kernel instance
+    (same dtype and scan kind), scaled by the elements processed; None when
+    the summary is for another instance or the kernel sources changed since.
+    The capture runs launches back to back with ncu's cache control off, so
+    each captured launch also writes back what the previous one left dirty
+    in L2 -- its traffic per element is the steady state's, which makes the
+    linear scaling sound."""
     try:
         kv = {}
         for line in KERNEL_TRAFFIC_FILE.read_text().splitlines():
             if line.startswith("- ") and ":" in line:
                 k, _, v = line[2:].partition(":")
                 kv[k.strip()] = v.strip().strip("`")
-        if kv.get("workload") != workload or int(kv.get("n", -1)) != n:
+        kind = "exclusive" if w.exclusive else "inclusive"
+        if kv.get("dtype") != w.dtype or kv.get("kind") != kind:
             return None
         if kv.get("kernel_sources_sha256") != kernel_sources_sha256():
             return None
-        return int(kv["dram_bytes_read_per_launch"]) + int(kv["dram_bytes_write_per_launch"])
+        n_cap = int(kv["n_captured"])
+        per_launch = int(kv["dram_bytes_read_per_launch"]) + int(kv["dram_bytes_write_per_launch"])
+        return {"bytes": int(round(per_launch * n / n_cap)), "captured_n": n_cap,
+                "captured_bytes": per_launch, "source": KERNEL_TRAFFIC_FILE.name,
+                "scaling": f"x {n / n_cap:g} (elements processed)"}
     except Exception:
         return None
 
@@ -526,15 +542,20 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
             t, _ = h.timed(k, lambda: h.step(algo), 1)
             extra[algo] = {"gbs": round(bytes_step * k / t / 1e9, 2),
                            "ms_per_step": round(1000 * t / k, 4)}
-    sweep = []
-    if args.sweep and world == 1:
-        sweep = run_sweep(args)
+    configs = []
+    if not args.no_configs and world == 1:
+        configs = run_configs(w)
     compaction = run_compaction(args) if args.compaction and world == 1 else None
     ops = run_ops(args) if args.ops and world == 1 else None
     rbk = run_reduce_by_key(args) if args.rbk and world == 1 else None
 
     if rank != 0:
         return
+    if args.traffic is not None:
+        traffic = {"bytes": int(args.traffic), "source": "--traffic"}
+    else:
+        traffic = recorded_traffic(w, n)
+    tbytes = traffic["bytes"] if traffic else None
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -545,11 +566,15 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
         "memcpy_gbs": round(copy_gbs, 2), "vs_memcpy": round(gbs / copy_gbs, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": args.traffic if args.traffic is not None else recorded_traffic(w.name, n),
+                     "traffic": tbytes,
+                     "dram_frac": round(tbytes / per_launch / 1e9 / peak, 4) if tbytes else None,
+                     "traffic_source": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "per_launch_ms": round(per_launch * 1000, 4),
-                     "note": "one kernel launch per step (no workspace reset); median CUDA-event step time"},
+                     "note": "one kernel launch per step (no workspace reset); median CUDA-event step time; "
+                             "frac counts the algorithmic 2n*sizeof(T) bytes, dram_frac the DRAM bytes ncu "
+                             "counted (traffic) over the same time"},
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": n * w.itemsize, "d2h_bytes_per_step": n * w.itemsize,
                 "steps": e2e_steps,
@@ -561,8 +586,8 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
     }
     if extra:
         line["comparison_paths"] = extra
-    if sweep:
-        line["sweep"] = sweep
+    if configs:
+        line["configs"] = configs
     if compaction:
         line["compaction"] = compaction
     if ops:
@@ -574,27 +599,32 @@ def run_ours(args, rank: int, world: int, local: int) -> None:
     print(json.dumps(line), flush=True)
 
 
-def run_sweep(args) -> list[dict]:
+def run_configs(headline: workloads.Workload) -> list[dict]:
+    """Every other workload (each length of the in-place sweep), timed as
+    the headline is: warm-up, then median CUDA-event time of K calls (the L2
+    flushed before each call where the data would fit in it), beside a
+    device-to-device copy of the same bytes timed the same way, and a
+    sampled self-check of the output.  Compact: one entry per length."""
     import torch
     out = []
     for w in workloads.ALL:
-        sizes = w.sweep if w.sweep else (w.n,)
-        for n in sizes:
+        if w.name == headline.name:
+            continue
+        for n in (w.sweep if w.sweep else (w.n,)):
             h = Harness(w, n, torch.device("cuda", 0))
+            k = 40 if h.flush is not None else 20
             for _ in range(3):
                 h.step()
-            k = 20
-            t, per = h.timed(k, h.step, 1)
+            _, per = h.timed(k, h.step, 1)
             for _ in range(3):
                 h.memcpy()
-            tc, _ = h.timed(k, h.memcpy, 1)
+            _, per_c = h.timed(k, h.memcpy, 1)
             b = 2 * n * w.itemsize
-            med = statistics.median(per)
+            med, med_c = statistics.median(per), statistics.median(per_c)
             out.append({"name": w.name, "n": n, "ms": round(med * 1000, 4),
                         "gbs": round(b / med / 1e9, 2), "gelem_per_s": round(n / med / 1e9, 3),
-                        "memcpy_gbs": round(b * k / tc / 1e9, 2),
-                        "vs_memcpy": round((b / med) / (b * k / tc), 4),
-                        "l2": "flushed" if h.flush is not None else "larger than L2",
+                        "memcpy_gbs": round(b / med_c / 1e9, 2), "vs_memcpy": round(med_c / med, 4),
+                        "steps": k, "l2": "flushed before each call" if h.flush is not None else "larger than L2",
                         "spot_check": h.property_check()})
             del h
             torch.cuda.empty_cache()
@@ -698,7 +728,7 @@ def run_reduce_by_key(args, n: int = 1 << 25) -> dict:
     return res
 
 
-PROFILE_CASES = ("rbk_f32_L16", "rle_L16", "select_flagged", "partition_flagged")
+PROFILE_CASES = ("scan_i32_excl", "rbk_f32_L16", "rle_L16", "select_flagged", "partition_flagged")
 
 
 def run_profile_case(args) -> None:
@@ -709,7 +739,15 @@ def run_profile_case(args) -> None:
     from prefix_scan_gb300 import api, inputs
     dev = torch.device("cuda", 0)
     case = args.profile_case
-    if case in ("rbk_f32_L16", "rle_L16"):
+    if case == "scan_i32_excl":
+        # the headline kernel instance on the headline distribution
+        n = args.n or 1 << 26
+        w = workloads.I32_EXCL_2P28
+        x = torch.from_numpy(w.make(n)).to(dev)
+        out = torch.empty_like(x)
+        ws = api.alloc_workspace(torch.int32, n, dev)
+        fn = lambda: api.scan(x, exclusive=True, out=out, workspace=ws)[-1:]
+    elif case in ("rbk_f32_L16", "rle_L16"):
         n = args.n or 1 << 25
         kt = torch.from_numpy(inputs.run_keys(n, 16, 27)).to(dev)
         vt = torch.from_numpy(inputs.uniform_f32(n, 12)).to(dev)
@@ -803,7 +841,8 @@ def main():
     ap.add_argument("--n", type=int, default=0, help="override the workload length")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--compare", action="store_true", help="also time the comparison paths")
-    ap.add_argument("--sweep", action="store_true", help="also time every workload (extra key)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (the `configs` key of the default run)")
     ap.add_argument("--compaction", action="store_true", help="also time select / partition at 2^28")
     ap.add_argument("--ops", action="store_true", help="also time max / min and the deterministic mode at 2^28")
     ap.add_argument("--rbk", action="store_true", help="also time reduce-by-key / run-length encoding at 2^25")
