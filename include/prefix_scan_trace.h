@@ -1,0 +1,57 @@
+/*
+ * prefix_scan_trace.h -- the pipeline trace of the single-pass scan kernel.
+ *
+ * The decoupled look-back ("Single-pass Parallel Prefix Scan with Decoupled
+ * Look-back", summary page, sections 4.1 and 4.4) hides the look-back's
+ * latency only while each tile's aggregate (A) and inclusive prefix (P)
+ * appear soon enough; the trace shows where a tile's time goes.  A build of
+ * the library with PS_TRACE defined records, for each of the first
+ * ps_trace_capacity() tiles of every persistent scan launch (the last launch
+ * overwrites), the GPU's global nanosecond timer at the points below, the
+ * CTA that claimed the tile, and the windows its look-back walked and the
+ * re-polls of unpublished descriptors it made.  The product build records
+ * nothing: ps_trace_capacity() returns 0 and ps_trace_read fails.
+ */
+#ifndef PREFIX_SCAN_TRACE_H
+#define PREFIX_SCAN_TRACE_H
+
+#include "prefix_scan.h"
+
+/* Trace points, in pipeline order (index into a tile's PS_TRACE_POINTS). */
+#define PS_TRACE_CLAIM 0             /* tile id taken from the counter (a1) */
+#define PS_TRACE_DATA 1              /* tile landed in shared memory (a2) */
+#define PS_TRACE_AGGREGATE 2         /* A (tile 0: P) published (a6) */
+#define PS_TRACE_LOOKBACK_START 3    /* look-back warp starts on the tile (a7) */
+#define PS_TRACE_PREFIX 4            /* P published, prefix handed over (a8) */
+#define PS_TRACE_COMPUTE_START 5     /* compute warps start on the tile (a3) */
+#define PS_TRACE_PREFIX_RECEIVED 6   /* compute warps have the prefix (a9) */
+#define PS_TRACE_STORED 7            /* compute warp 0 issued its stores (a9) */
+#define PS_TRACE_POINTS 8
+#ifndef PS_TRACE_TILES
+#define PS_TRACE_TILES 65536
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Tiles a trace holds; 0 when this build records none. */
+size_t ps_trace_capacity(void);
+
+/*
+ * Waits for the device, then copies the trace of the first `tiles` tiles
+ * (<= ps_trace_capacity()) of the last persistent scan launch to host
+ * memory: timestamps[t * PS_TRACE_POINTS + k] (ns), lookback[t] (windows
+ * walked << 16 | re-polls, each saturating at 65535; tile 0 and tiles
+ * whose look-back did not run keep old values), cta[t].  Entries of tiles
+ * the launch did not reach keep older values.  PS_ERR_INVALID_ARG in a
+ * build without the trace or for bad arguments; PS_ERR_CUDA if a copy
+ * fails.
+ */
+ps_status ps_trace_read(uint64_t *timestamps, uint32_t *lookback, int32_t *cta, size_t tiles);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PREFIX_SCAN_TRACE_H */

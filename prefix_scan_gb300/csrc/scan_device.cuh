@@ -325,15 +325,23 @@ __device__ __forceinline__ void poll_backoff(uint32_t polls) {
 // A poll cap bounds every wait.  When it is exceeded the status word gets
 // PS_ERR_LOOKBACK_TIMEOUT and the missing tiles count as P with the
 // identity, so the warp finishes (with a wrong value) instead of hanging.
+//
+// In a trace build (PS_TRACE) lane 0 writes to *trace, when given, the
+// windows walked (high 16 bits) and the re-polls of unpublished
+// descriptors (low 16 bits), each saturating; otherwise `trace` is unused.
 template <typename U, int DW, int K, typename Op = OpSum>
 __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_t epoch,
-                                       uint32_t max_polls, unsigned long long *status) {
+                                       uint32_t max_polls, unsigned long long *status,
+                                       uint32_t *trace = nullptr) {
     const int lane = threadIdx.x & 31;
     const U ident = Op::template identity<U>();
     U excl = ident;
     long long base = tile - 1;
     uint32_t polls = 0;
     bool gave_up = false;
+#ifdef PS_TRACE
+    uint32_t windows = 1;
+#endif
     while (true) {
         uint32_t f[K];
         U v[K];
@@ -392,8 +400,16 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
         }
         if (done) break;
         base -= 32 * K;
+#ifdef PS_TRACE
+        ++windows;
+#endif
     }
     if (gave_up && lane == 0) report_error(status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+#ifdef PS_TRACE
+    if (trace && lane == 0) *trace = (min(windows, 0xffffu) << 16) | min(polls, 0xffffu);
+#else
+    (void)trace;
+#endif
     return excl;
 }
 

@@ -39,10 +39,41 @@
 // and the loop moves on (results are then unspecified, but the kernel ends).
 #include <type_traits>
 
+#include "prefix_scan_trace.h"
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
 
 namespace ps {
+
+// ---- trace build --------------------------------------------------------------
+// Built with PS_TRACE defined, the kernel records for each of the first
+// kTraceTiles tiles the %globaltimer at eight hand-offs of its pipeline
+// (claim, data landed, A published, look-back start, P published, compute
+// start, prefix received, stores issued), the CTA that took it, and the
+// look-back's windows and re-polls; ps_trace_read copies them out.  One
+// store per point by one lane; without PS_TRACE none of it is compiled.
+#ifdef PS_TRACE
+constexpr long long kTraceTiles = PS_TRACE_TILES;
+__device__ unsigned long long g_trace_ts[kTraceTiles][PS_TRACE_POINTS];
+__device__ uint32_t g_trace_lookback[kTraceTiles];
+__device__ int g_trace_cta[kTraceTiles];
+__device__ __forceinline__ void trace_point(long long tile, int k) {
+    if (tile >= 0 && tile < kTraceTiles) g_trace_ts[tile][k] = global_ns();
+}
+__device__ __forceinline__ uint32_t *trace_lookback_slot(long long tile) {
+    return (tile >= 0 && tile < kTraceTiles) ? &g_trace_lookback[tile] : nullptr;
+}
+__device__ __forceinline__ void trace_cta(long long tile) {
+    if (tile >= 0 && tile < kTraceTiles) g_trace_cta[tile] = (int)blockIdx.x;
+}
+#define PS_TRACE_POINT(tile, k) trace_point((tile), (k))
+#define PS_TRACE_CTA(tile) trace_cta(tile)
+#define PS_TRACE_LOOKBACK(tile) trace_lookback_slot(tile)
+#else
+#define PS_TRACE_POINT(tile, k) ((void)0)
+#define PS_TRACE_CTA(tile) ((void)0)
+#define PS_TRACE_LOOKBACK(tile) nullptr
+#endif
 
 constexpr int kPCW = kThreads / 32;   // compute warps per CTA
 // The compute warps hand a stage back as soon as they hold its data in
@@ -185,6 +216,10 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                     }
                 }
                 const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
+                if (t < num_tiles) {
+                    PS_TRACE_POINT(t, PS_TRACE_CLAIM);
+                    PS_TRACE_CTA(t);
+                }
                 tile_of[k % kRing] = t;
                 if (t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     mbar_arrive_expect_tx(&full[s], TILE_BYTES);
@@ -214,6 +249,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 break;
             }
             const unsigned long long tile_base = (unsigned long long)tile * TILE;
+            if (lane == 0) PS_TRACE_POINT(tile, PS_TRACE_DATA);
             U agg;
             if constexpr (Op::kCommutative) {
                 // each lane folds every 32nd vector; the order does not matter
@@ -298,6 +334,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                     Desc<U, Tr::DW>::store(desc, tile, kFlagA, agg, epoch);
                 }
                 agg_of[slot] = agg;
+                PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
                 mbar_arrive(&agg_done[slot]);
             }
         }
@@ -315,17 +352,20 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) break;
             const U agg = agg_of[slot];
+            if (lane == 0) PS_TRACE_POINT(tile, PS_TRACE_LOOKBACK_START);
             __syncwarp();
             U excl;
             if (tile == 0) {
                 excl = excl_of[slot];   // the carry the aggregator read
             } else {
-                excl = look_back<U, Tr::DW, kLookbackK, Op>(desc, tile, epoch, a.max_polls, &hdr->status);
+                excl = look_back<U, Tr::DW, kLookbackK, Op>(desc, tile, epoch, a.max_polls, &hdr->status,
+                                                            PS_TRACE_LOOKBACK(tile));
                 if (lane == 0) Desc<U, Tr::DW>::store(desc, tile, kFlagP, Op::combine(excl, agg), epoch);
             }
             if (lane == 0) {
                 if (a.carry_out && tile == num_tiles - 1) *reinterpret_cast<U *>(a.carry_out) = Op::combine(excl, agg);
                 excl_of[slot] = excl;
+                PS_TRACE_POINT(tile, PS_TRACE_PREFIX);
                 mbar_arrive(&prefix_ready[slot]);
             }
         }
@@ -344,6 +384,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         const unsigned long long tile_base = (unsigned long long)tile * TILE;
         const bool cut = tile_base + TILE > n;
         const int seg = warp * 32 * ITEMS;   // element offset of this warp in the tile
+        if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
 
         // a2: rows of 16-byte vectors from the stage (or bounded global loads)
         // With two vectors per lane, lanes 4-7 of each quarter-warp read
@@ -439,6 +480,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         if (!mbar_wait(&prefix_ready[slot], (uint32_t)((k / kRing) & 1)))   // never in a correct run
             report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
         const U tile_excl = excl_of[slot];
+        if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
 
         // a9
         const U base = Op::combine(tile_excl, warp_excl);
@@ -495,6 +537,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
+        if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_STORED);
     }
     }
 
@@ -549,3 +592,32 @@ template cudaError_t launch_persistent<int64_t>(const PassArgs &, bool, int, cud
 template cudaError_t launch_persistent<float>(const PassArgs &, bool, int, cudaStream_t);
 
 }  // namespace ps
+
+extern "C" size_t ps_trace_capacity(void) {
+#ifdef PS_TRACE
+    return (size_t)ps::kTraceTiles;
+#else
+    return 0;
+#endif
+}
+
+extern "C" ps_status ps_trace_read(uint64_t *timestamps, uint32_t *lookback, int32_t *cta, size_t tiles) {
+#ifdef PS_TRACE
+    if (timestamps == nullptr || lookback == nullptr || cta == nullptr || tiles > (size_t)ps::kTraceTiles)
+        return PS_ERR_INVALID_ARG;
+    if (tiles == 0) return PS_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpyFromSymbol(timestamps, ps::g_trace_ts, tiles * sizeof(ps::g_trace_ts[0]));
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(lookback, ps::g_trace_lookback, tiles * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(cta, ps::g_trace_cta, tiles * sizeof(int32_t));
+    if (e != cudaSuccess) {
+        ps::note_cuda_error(e);
+        return PS_ERR_CUDA;
+    }
+    return PS_OK;
+#else
+    (void)timestamps, (void)lookback, (void)cta, (void)tiles;
+    return PS_ERR_INVALID_ARG;   // this build records no trace
+#endif
+}

@@ -1,0 +1,159 @@
+"""Pipeline trace of the single-pass scan kernel.
+
+Builds the library with PS_TRACE defined (``_build/trace/``, not the
+product library), runs the persistent scan on a workload with the L2 flushed
+before each call, reads the per-tile timestamps back through
+``ps_trace_read`` (include/prefix_scan_trace.h) and prints where a tile's
+time goes, as a markdown section:
+
+  claim -> A          tile id taken until its aggregate is published
+  A -> look-back      the tile waits for its CTA's look-back warp
+  look-back           windows walked and re-polls until P is published
+  P -> compute        the prefix reached the compute warps (negative when
+                      they were still busy with earlier tiles)
+  compute -> stored   the compute warps' scan-and-store after the prefix
+
+The decoupled look-back ("Single-pass Parallel Prefix Scan with Decoupled
+Look-back", summary page, sections 4.1 and 4.4) is meant to keep the
+look-back off the critical path; these figures say whether it does.
+
+    python -m prefix_scan_gb300.trace --workload i32_excl_2p28 [--runs 5]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import sys
+from pathlib import Path
+
+import numpy as np
+
+if __package__ in (None, ""):
+    sys.path.insert(0, str(Path(__file__).resolve().parents[1]))
+
+from prefix_scan_gb300 import _lib, workloads  # noqa: E402
+from prefix_scan_gb300 import build as nvbuild  # noqa: E402
+
+POINTS = ("claim", "data", "aggregate", "lookback_start", "prefix", "compute_start",
+          "prefix_received", "stored")
+C, D, AG, LS, PR, CS, RC, ST = range(8)
+FLUSH_BYTES = 512 << 20
+
+
+def load_trace_library() -> ctypes.CDLL:
+    path = nvbuild.build_variant("trace", {"PS_TRACE": 1})
+    lib = ctypes.CDLL(str(path))
+    for name, (res, args) in _lib.SIGNATURES.items():
+        if "noalloc" in name:
+            continue
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    if lib.ps_trace_capacity() == 0:
+        raise RuntimeError("the trace build records no trace")
+    return lib
+
+
+def run(lib: ctypes.CDLL, w: workloads.Workload, n: int, runs: int):
+    """Traces of `runs` calls (L2 flushed before each): list of
+    (timestamps[tiles, 8] in us from the first claim, lookback[tiles], cta[tiles])."""
+    import torch
+    dev = torch.device("cuda", 0)
+    code = {"int32": _lib.PS_INT32, "int64": _lib.PS_INT64, "float32": _lib.PS_FLOAT32}[w.dtype]
+    x = torch.from_numpy(w.make(n)).to(dev)
+    out = x if w.inplace else torch.empty_like(x)
+    ws = torch.zeros(max(int(lib.ps_scan_workspace_size(code, n)), 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    tiles = -(-n // int(lib.ps_tile_elements(code)))
+    tiles = min(tiles, int(lib.ps_trace_capacity()))
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    traces = []
+    for r in range(runs + 1):   # the first call warms up and is dropped
+        flush.fill_(r & 0xFF)
+        st = lib.ps_scan(_lib.PS_ALGO_DECOUPLED_LOOKBACK, code, int(w.exclusive), x.data_ptr(), out.data_ptr(),
+                         n, ws.data_ptr(), ws.numel(), stream)
+        _lib.check("ps_scan", st)
+        ts = np.zeros((tiles, 8), dtype=np.uint64)
+        lb = np.zeros(tiles, dtype=np.uint32)
+        cta = np.zeros(tiles, dtype=np.int32)
+        _lib.check("ps_trace_read", lib.ps_trace_read(ts.ctypes.data, lb.ctypes.data, cta.ctypes.data, tiles))
+        if r == 0:
+            continue
+        t = ts.astype(np.int64)
+        t = (t - t[:, C].min()) / 1e3
+        traces.append((t, lb, cta))
+    return traces
+
+
+def _dist(v: np.ndarray) -> str:
+    return f"{np.median(v):.2f} ({np.percentile(v, 10):.2f} / {np.percentile(v, 90):.2f})"
+
+
+def summarize(w: workloads.Workload, n: int, traces) -> str:
+    rows = []
+    spans, lasts = [], []
+    gaps = {k: [] for k in ("claim_A", "A_lb", "lb", "P_compute", "compute_stored", "claim_stored",
+                            "claim_data", "data_A", "interval")}
+    windows, polls = [], []
+    for t, lb, cta in traces:
+        spans.append(t[:, ST].max())
+        gaps["claim_data"].append(t[:, D] - t[:, C])
+        gaps["data_A"].append(t[:, AG] - t[:, D])
+        gaps["claim_A"].append(t[:, AG] - t[:, C])
+        gaps["A_lb"].append(t[1:, LS] - t[1:, AG])
+        gaps["lb"].append(t[1:, PR] - t[1:, LS])
+        gaps["P_compute"].append(t[:, RC] - t[:, PR])
+        gaps["compute_stored"].append(t[:, ST] - t[:, RC])
+        gaps["claim_stored"].append(t[:, ST] - t[:, C])
+        for c in np.unique(cta):
+            cl = np.sort(t[cta == c, C])
+            if cl.size > 1:
+                gaps["interval"].append(np.diff(cl))
+        windows.append((lb[1:] >> 16).astype(np.int64))
+        polls.append((lb[1:] & 0xFFFF).astype(np.int64))
+        lasts.append(t[:, C].max())
+    cat = {k: np.concatenate(v) if v else np.zeros(1) for k, v in gaps.items()}
+    win = np.concatenate(windows)
+    pol = np.concatenate(polls)
+    tiles = traces[0][0].shape[0]
+    rows.append(f"### {w.name} at n = {n} ({tiles} tiles, {len(traces)} traced calls, L2 flushed before each)")
+    rows.append("")
+    rows.append(f"- span, first claim to last store: median {np.median(spans):.2f} us; "
+                f"last claim at {np.median(lasts):.2f} us")
+    rows.append(f"- CTAs that took tiles: {len(np.unique(traces[0][2]))}; per-CTA interval between claims: "
+                f"{_dist(cat['interval'])} us")
+    rows.append("")
+    rows.append("| stage | median (p10 / p90), us |")
+    rows.append("|---|---|")
+    for key, label in (("claim_data", "claim -> data landed"), ("data_A", "data landed -> A published"),
+                       ("claim_A", "claim -> A published"), ("A_lb", "A -> look-back starts (queue)"),
+                       ("lb", "look-back (start -> P published)"),
+                       ("P_compute", "P published -> compute warps have it"),
+                       ("compute_stored", "prefix received -> stores issued"),
+                       ("claim_stored", "claim -> stores issued")):
+        rows.append(f"| {label} | {_dist(cat[key])} |")
+    rows.append("")
+    hist = [(win == k).mean() for k in (1, 2, 3, 4)] + [(win >= 5).mean()]
+    rows.append(f"- look-back windows of 32 descriptors walked: 1: {hist[0]:.1%}, 2: {hist[1]:.1%}, "
+                f"3: {hist[2]:.1%}, 4: {hist[3]:.1%}, 5+: {hist[4]:.1%} (mean {win.mean():.2f})")
+    rows.append(f"- re-polls of unpublished descriptors per look-back: median {np.median(pol):.0f}, "
+                f"p90 {np.percentile(pol, 90):.0f}, none in {(pol == 0).mean():.1%}")
+    rows.append("")
+    return "\n".join(rows)
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--workload", action="append", choices=sorted(workloads.BY_NAME), required=True)
+    ap.add_argument("--n", type=int, action="append", default=None,
+                    help="length per --workload (default: the workload's own)")
+    ap.add_argument("--runs", type=int, default=5)
+    args = ap.parse_args(argv)
+    lib = load_trace_library()
+    for i, name in enumerate(args.workload):
+        w = workloads.BY_NAME[name]
+        n = args.n[i] if args.n and i < len(args.n) else w.n
+        print(summarize(w, n, run(lib, w, n, args.runs)), flush=True)
+
+
+if __name__ == "__main__":
+    main()
