@@ -30,6 +30,14 @@
 #ifndef PS_TRACE_TILES
 #define PS_TRACE_TILES 65536
 #endif
+/* Per-CTA trace points (index into a CTA's PS_TRACE_CTA_POINTS). */
+#define PS_TRACE_CTA_ENTRY 0         /* thread 0 starts */
+#define PS_TRACE_CTA_HEADER 1        /* the CTA has the workspace header's verdict */
+#define PS_TRACE_CTA_DONE 2          /* compute warp 0 leaves its loop */
+#define PS_TRACE_CTA_POINTS 3
+#ifndef PS_TRACE_CTAS
+#define PS_TRACE_CTAS 1024
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -49,6 +57,13 @@ size_t ps_trace_capacity(void);
  * fails.
  */
 ps_status ps_trace_read(uint64_t *timestamps, uint32_t *lookback, int32_t *cta, size_t tiles);
+
+/*
+ * The same for the CTAs of the last launch: timestamps[c *
+ * PS_TRACE_CTA_POINTS + k] (ns) for the first `ctas` (<= PS_TRACE_CTAS)
+ * CTAs.  Same errors as ps_trace_read.
+ */
+ps_status ps_trace_read_ctas(uint64_t *timestamps, size_t ctas);
 
 #ifdef __cplusplus
 }

@@ -57,6 +57,11 @@ constexpr long long kTraceTiles = PS_TRACE_TILES;
 __device__ unsigned long long g_trace_ts[kTraceTiles][PS_TRACE_POINTS];
 __device__ uint32_t g_trace_lookback[kTraceTiles];
 __device__ int g_trace_cta[kTraceTiles];
+constexpr int kTraceCtas = PS_TRACE_CTAS;
+__device__ unsigned long long g_trace_cta_ts[kTraceCtas][PS_TRACE_CTA_POINTS];
+__device__ __forceinline__ void trace_cta_point(int k) {
+    if (blockIdx.x < kTraceCtas) g_trace_cta_ts[blockIdx.x][k] = global_ns();
+}
 __device__ __forceinline__ void trace_point(long long tile, int k) {
     if (tile >= 0 && tile < kTraceTiles) g_trace_ts[tile][k] = global_ns();
 }
@@ -69,10 +74,12 @@ __device__ __forceinline__ void trace_cta(long long tile) {
 #define PS_TRACE_POINT(tile, k) trace_point((tile), (k))
 #define PS_TRACE_CTA(tile) trace_cta(tile)
 #define PS_TRACE_LOOKBACK(tile) trace_lookback_slot(tile)
+#define PS_TRACE_CTA_POINT(k) trace_cta_point(k)
 #else
 #define PS_TRACE_POINT(tile, k) ((void)0)
 #define PS_TRACE_CTA(tile) ((void)0)
 #define PS_TRACE_LOOKBACK(tile) nullptr
+#define PS_TRACE_CTA_POINT(k) ((void)0)
 #endif
 
 constexpr int kPCW = kThreads / 32;   // compute warps per CTA
@@ -107,6 +114,20 @@ constexpr bool kEarlyRelease = PS_PERSIST_EARLY_RELEASE != 0;
 #ifndef PS_PERSIST_AGG_SPLIT_F32
 #define PS_PERSIST_AGG_SPLIT_F32 1
 #endif
+// ... and of an int32 scan: four IADD chains of 64 rather than one chain
+// of 128 IADD3s (data landed -> A published 0.96 -> 0.74 us at 2^26 with
+// the unroll below).
+#ifndef PS_PERSIST_AGG_SPLIT32
+#define PS_PERSIST_AGG_SPLIT32 1
+#endif
+// Unroll of the aggregator's commutative loop for 4-byte and 8-byte
+// elements (shared-memory loads in flight per lane).
+#ifndef PS_PERSIST_AGG_UNROLL32
+#define PS_PERSIST_AGG_UNROLL32 16
+#endif
+#ifndef PS_PERSIST_AGG_UNROLL64
+#define PS_PERSIST_AGG_UNROLL64 8
+#endif
 constexpr int kRing = kEarlyRelease ? 2 * kPStages : kPStages;   // hand-off slots: iteration k uses k % kRing
 // per stage: full, empty; per hand-off slot: agg_done, prefix_ready, tile id, aggregate, prefix
 constexpr size_t kStageTailBytes = ((size_t)kPStages * 2 * 8 + (size_t)kRing * (2 * 8 + 8 + 8 + 8) + 127) / 128 * 128;
@@ -128,9 +149,18 @@ constexpr size_t persistent_smem_bytes() {
 static_assert(kThreads % 32 == 0 && kThreads <= 960, "compute threads per CTA");
 
 
-template <typename T, bool EXCL, typename Op>
-__global__ void __launch_bounds__((kPCW + 3) * 32, kPCtasPerSm)
+// LBW look-back warps per CTA; look-back warp j resolves the CTA's
+// iterations j, j + LBW, ...  A second one lets a CTA resolve two tiles'
+// prefixes at once: each look-back costs one or two L2 round trips of over a
+// microsecond while the memory streams, close to the time in which a CTA
+// moves a tile, so with one the tiles queue for it.  The launcher picks LBW
+// from the array's length.
+template <int LBW> constexpr int persistent_threads() { return (kPCW + 2 + LBW) * 32; }
+
+template <typename T, bool EXCL, typename Op, int LBW>
+__global__ void __launch_bounds__(persistent_threads<LBW>(), kPCtasPerSm)
 persistent_kernel(PassArgs a, long long num_tiles) {
+    static_assert(LBW >= 1 && LBW <= kPStages, "at most one look-back warp per stage");
     using Tr = Traits<T>;
     using U = typename Tr::U;
     const U ident = Op::template identity<U>();
@@ -173,6 +203,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     __shared__ uint32_t s_epoch;
     __shared__ int s_ok;
     if (tid == 0) {
+        PS_TRACE_CTA_POINT(PS_TRACE_CTA_ENTRY);
         if (PS_PERSIST_PREFETCH) {
             // The producers take up to kPStages tile ids each before any
             // stage comes back, so the first claims fall on the first
@@ -202,6 +233,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     __syncthreads();
     if (!s_ok) return;   // same verdict in every CTA: nothing runs
     const uint32_t epoch = s_epoch;
+    if (tid == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_HEADER);
 
     if (warp == kPCW) {
         // ---------------- producer warp ----------------
@@ -244,8 +276,17 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             }
             const int slot = (int)(k % kRing);
             const long long tile = tile_of[slot];
-            if (tile < 0 || tile >= num_tiles) {   // end marker: pass it on to the look-back warp
-                if (lane == 0) mbar_arrive(&agg_done[slot]);
+            if (tile < 0 || tile >= num_tiles) {
+                // end marker: pass it on to every look-back warp, on the
+                // slots of the next LBW iterations (the producer, which
+                // stopped here, writes none of them again)
+                if (lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < LBW; ++i) {
+                        if (i > 0) tile_of[(k + i) % kRing] = num_tiles;
+                        mbar_arrive(&agg_done[(k + i) % kRing]);
+                    }
+                }
                 break;
             }
             const unsigned long long tile_base = (unsigned long long)tile * TILE;
@@ -254,13 +295,15 @@ persistent_kernel(PassArgs a, long long num_tiles) {
             if constexpr (Op::kCommutative) {
                 // each lane folds every 32nd vector; the order does not matter
                 constexpr int AC = (sizeof(U) == 8 && PS_PERSIST_AGG_SPLIT64) ? VEC
-                                   : (std::is_same<U, float>::value && PS_PERSIST_AGG_SPLIT_F32) ? VEC : 1;
+                                   : (std::is_same<U, float>::value && PS_PERSIST_AGG_SPLIT_F32) ? VEC
+                                   : (std::is_same<U, uint32_t>::value && PS_PERSIST_AGG_SPLIT32) ? VEC : 1;
+                constexpr int UNROLL = sizeof(U) == 8 ? PS_PERSIST_AGG_UNROLL64 : PS_PERSIST_AGG_UNROLL32;
                 U accs[AC];
 #pragma unroll
                 for (int c = 0; c < AC; ++c) accs[c] = ident;
                 if (tile_base + TILE <= n) {
                     const V *src = reinterpret_cast<const V *>(stage_data + (size_t)s * TILE);
-#pragma unroll 8
+#pragma unroll UNROLL
                     for (int i = lane; i < (int)(TILE / VEC); i += 32) {
                         const V x = src[i];
 #pragma unroll
@@ -338,14 +381,25 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                 mbar_arrive(&agg_done[slot]);
             }
         }
-    } else if (warp == kPCW + 2) {
-        // ---------------- look-back warp ----------------
-        // Runs ahead of the compute warps: once a tile's A is out it looks
-        // back, publishes P and leaves the exclusive prefix in excl_of[slot]
-        // (steps 4-5 of section 4.1), so the compute warps rarely wait.
-        for (long long k = 0;; ++k) {
-            const int slot = (int)(k % kRing);
-            if (!mbar_wait(&agg_done[slot], (uint32_t)((k / kRing) & 1))) {   // never in a correct run
+    } else if (warp == kPCW + 2 || (LBW > 1 && warp > kPCW + 2)) {
+        // ---------------- look-back warps ----------------
+        // Run ahead of the compute warps: once a tile's A is out its
+        // look-back warp looks back, publishes P and leaves the exclusive
+        // prefix in excl_of[slot] (steps 4-5 of section 4.1), so the compute
+        // warps rarely wait.
+        // Warp j takes iterations j, j + LBW, ...; the slot and the phase
+        // parity are stepped directly (LBW divides the ring), which keeps
+        // 64-bit divisions out of the loop and the kernel within its
+        // register budget.
+        static_assert(kRing % LBW == 0, "the look-back warps step through the ring evenly");
+        int slot = LBW == 1 ? 0 : warp - (kPCW + 2);
+        uint32_t parity = 0;
+        for (;; slot += LBW) {
+            if (slot >= kRing) {
+                slot -= kRing;
+                parity ^= 1u;
+            }
+            if (!mbar_wait(&agg_done[slot], parity)) {   // never in a correct run
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
@@ -539,6 +593,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
         }
         if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_STORED);
     }
+    if (warp == 0 && lane == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_DONE);
     }
 
     // The last producer to take its last tile id readied the workspace
@@ -546,27 +601,45 @@ persistent_kernel(PassArgs a, long long num_tiles) {
     if (epoch == kEpochMask) finish_call(hdr, a.ws, a.ws_bytes, epoch);
 }
 
-template <typename T, bool EXCL, typename Op>
-cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
+// Two look-back warps per CTA for arrays of [FROM, BELOW) tiles per CTA slot
+// of a full grid, one otherwise.  Macros so that a sweep can rebuild with
+// other bounds.
+#ifndef PS_PERSIST_LBW2_FROM
+#define PS_PERSIST_LBW2_FROM 0
+#endif
+#ifndef PS_PERSIST_LBW2_BELOW
+#define PS_PERSIST_LBW2_BELOW 16
+#endif
+
+template <typename T, bool EXCL, typename Op, int LBW>
+cudaError_t launch_persistent_lbw(const PassArgs &a, long long tiles, int dev, long long grid, cudaStream_t s) {
     constexpr size_t smem = persistent_smem_bytes<T>();
-    const long long tiles = (long long)((a.n + persistent_tile_elems<T>() - 1) / persistent_tile_elems<T>());
     // the dynamic shared-memory opt-in, once per device and template instance
     // (a repeated call from a racing thread is harmless)
     static volatile int configured[64] = {};
     cudaError_t e;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(persistent_kernel<T, EXCL, Op>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(persistent_kernel<T, EXCL, Op, LBW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    long long grid = (long long)sms * kPCtasPerSm;
-    if (grid > tiles) grid = tiles;
-    persistent_kernel<T, EXCL, Op><<<(unsigned int)grid, (kPCW + 3) * 32, smem, s>>>(a, tiles);
+    persistent_kernel<T, EXCL, Op, LBW><<<(unsigned int)grid, persistent_threads<LBW>(), smem, s>>>(a, tiles);
     return cudaGetLastError();
+}
+
+template <typename T, bool EXCL, typename Op>
+cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
+    const long long tiles = (long long)((a.n + persistent_tile_elems<T>() - 1) / persistent_tile_elems<T>());
+    cudaError_t e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long long full = (long long)sms * kPCtasPerSm;
+    const long long grid = full < tiles ? full : tiles;
+    if (tiles >= (long long)PS_PERSIST_LBW2_FROM * full && tiles < (long long)PS_PERSIST_LBW2_BELOW * full)
+        return launch_persistent_lbw<T, EXCL, Op, 2>(a, tiles, dev, grid, s);
+    return launch_persistent_lbw<T, EXCL, Op, 1>(a, tiles, dev, grid, s);
 }
 
 template <typename T, typename Op>
@@ -618,6 +691,24 @@ extern "C" ps_status ps_trace_read(uint64_t *timestamps, uint32_t *lookback, int
     return PS_OK;
 #else
     (void)timestamps, (void)lookback, (void)cta, (void)tiles;
+    return PS_ERR_INVALID_ARG;   // this build records no trace
+#endif
+}
+
+extern "C" ps_status ps_trace_read_ctas(uint64_t *timestamps, size_t ctas) {
+#ifdef PS_TRACE
+    if (timestamps == nullptr || ctas > (size_t)ps::kTraceCtas) return PS_ERR_INVALID_ARG;
+    if (ctas == 0) return PS_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpyFromSymbol(timestamps, ps::g_trace_cta_ts, ctas * sizeof(ps::g_trace_cta_ts[0]));
+    if (e != cudaSuccess) {
+        ps::note_cuda_error(e);
+        return PS_ERR_CUDA;
+    }
+    return PS_OK;
+#else
+    (void)timestamps, (void)ctas;
     return PS_ERR_INVALID_ARG;   // this build records no trace
 #endif
 }

@@ -18,6 +18,12 @@ Look-back", summary page, sections 4.1 and 4.4) is meant to keep the
 look-back off the critical path; these figures say whether it does.
 
     python -m prefix_scan_gb300.trace --workload i32_excl_2p28 [--runs 5]
+
+``--define NAME=VALUE`` rebuilds the variant with other compile-time
+settings of the kernel (for example the look-back's poll back-off), and
+``--launch-only K`` only launches the scan K times after one warm-up call
+(no trace read, no summary): the command to put under a profiler when
+comparing such variants.
 """
 from __future__ import annotations
 
@@ -40,22 +46,45 @@ C, D, AG, LS, PR, CS, RC, ST = range(8)
 FLUSH_BYTES = 512 << 20
 
 
-def load_trace_library() -> ctypes.CDLL:
-    path = nvbuild.build_variant("trace", {"PS_TRACE": 1})
+def load_trace_library(defines: dict[str, int] | None = None, trace: bool = True) -> ctypes.CDLL:
+    defs = dict(defines or {})
+    if trace:
+        defs["PS_TRACE"] = 1
+    name = "trace" if defs == {"PS_TRACE": 1} else \
+        "v_" + "_".join(f"{k.lower()}{v}" for k, v in sorted(defs.items()))
+    path = nvbuild.build_variant(name, defs)
     lib = ctypes.CDLL(str(path))
     for name, (res, args) in _lib.SIGNATURES.items():
         if "noalloc" in name:
             continue
         fn = getattr(lib, name)
         fn.restype, fn.argtypes = res, args
-    if lib.ps_trace_capacity() == 0:
+    if trace and lib.ps_trace_capacity() == 0:
         raise RuntimeError("the trace build records no trace")
     return lib
 
 
+def launch_only(lib: ctypes.CDLL, w: workloads.Workload, n: int, launches: int) -> None:
+    """One warm-up call, then `launches` back-to-back calls; prints one line."""
+    import torch
+    dev = torch.device("cuda", 0)
+    code = {"int32": _lib.PS_INT32, "int64": _lib.PS_INT64, "float32": _lib.PS_FLOAT32}[w.dtype]
+    x = torch.from_numpy(w.make(n)).to(dev)
+    out = x if w.inplace else torch.empty_like(x)
+    ws = torch.zeros(max(int(lib.ps_scan_workspace_size(code, n)), 16), dtype=torch.uint8, device=dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    for _ in range(launches + 1):
+        _lib.check("ps_scan", lib.ps_scan(_lib.PS_ALGO_DECOUPLED_LOOKBACK, code, int(w.exclusive), x.data_ptr(),
+                                          out.data_ptr(), n, ws.data_ptr(), ws.numel(), stream))
+    st = ctypes.c_int(-1)
+    _lib.check("ps_get_device_status", lib.ps_get_device_status(ws.data_ptr(), stream, ctypes.byref(st)))
+    print(f"{w.name} n={n}: {launches + 1} launches, device status {st.value}", flush=True)
+
+
 def run(lib: ctypes.CDLL, w: workloads.Workload, n: int, runs: int):
     """Traces of `runs` calls (L2 flushed before each): list of
-    (timestamps[tiles, 8] in us from the first claim, lookback[tiles], cta[tiles])."""
+    (timestamps[tiles, 8] in us from the first CTA's start, lookback[tiles],
+    cta[tiles], per-CTA timestamps[ctas, 3] in us on the same base)."""
     import torch
     dev = torch.device("cuda", 0)
     code = {"int32": _lib.PS_INT32, "int64": _lib.PS_INT64, "float32": _lib.PS_FLOAT32}[w.dtype]
@@ -78,9 +107,13 @@ def run(lib: ctypes.CDLL, w: workloads.Workload, n: int, runs: int):
         _lib.check("ps_trace_read", lib.ps_trace_read(ts.ctypes.data, lb.ctypes.data, cta.ctypes.data, tiles))
         if r == 0:
             continue
-        t = ts.astype(np.int64)
-        t = (t - t[:, C].min()) / 1e3
-        traces.append((t, lb, cta))
+        ctas = int(cta.max()) + 1
+        cts = np.zeros((ctas, 3), dtype=np.uint64)
+        _lib.check("ps_trace_read_ctas", lib.ps_trace_read_ctas(cts.ctypes.data, ctas))
+        t0 = int(cts[:, 0].min())
+        t = (ts.astype(np.int64) - t0) / 1e3
+        ct = (cts.astype(np.int64) - t0) / 1e3
+        traces.append((t, lb, cta, ct))
     return traces
 
 
@@ -94,8 +127,15 @@ def summarize(w: workloads.Workload, n: int, traces) -> str:
     gaps = {k: [] for k in ("claim_A", "A_lb", "lb", "P_compute", "compute_stored", "claim_stored",
                             "claim_data", "data_A", "interval")}
     windows, polls = [], []
-    for t, lb, cta in traces:
-        spans.append(t[:, ST].max())
+    starts = {k: [] for k in ("first_claim", "last_entry", "header", "first_data", "last_store", "last_done")}
+    for t, lb, cta, ct in traces:
+        starts["first_claim"].append(t[:, C].min())
+        starts["last_entry"].append(ct[:, 0].max())
+        starts["header"].append(np.median(ct[:, 1] - ct[:, 0]))
+        starts["first_data"].append(t[:, D].min())
+        starts["last_store"].append(t[:, ST].max())
+        starts["last_done"].append(ct[:, 2].max())
+        spans.append(t[:, ST].max() - t[:, C].min())
         gaps["claim_data"].append(t[:, D] - t[:, C])
         gaps["data_A"].append(t[:, AG] - t[:, D])
         gaps["claim_A"].append(t[:, AG] - t[:, C])
@@ -108,8 +148,9 @@ def summarize(w: workloads.Workload, n: int, traces) -> str:
             cl = np.sort(t[cta == c, C])
             if cl.size > 1:
                 gaps["interval"].append(np.diff(cl))
-        windows.append((lb[1:] >> 16).astype(np.int64))
-        polls.append((lb[1:] & 0xFFFF).astype(np.int64))
+        looked = t[1:, LS] > 0   # tiles whose look-back ran and recorded
+        windows.append((lb[1:][looked] >> 16).astype(np.int64))
+        polls.append((lb[1:][looked] & 0xFFFF).astype(np.int64))
         lasts.append(t[:, C].max())
     cat = {k: np.concatenate(v) if v else np.zeros(1) for k, v in gaps.items()}
     win = np.concatenate(windows)
@@ -117,8 +158,13 @@ def summarize(w: workloads.Workload, n: int, traces) -> str:
     tiles = traces[0][0].shape[0]
     rows.append(f"### {w.name} at n = {n} ({tiles} tiles, {len(traces)} traced calls, L2 flushed before each)")
     rows.append("")
-    rows.append(f"- span, first claim to last store: median {np.median(spans):.2f} us; "
-                f"last claim at {np.median(lasts):.2f} us")
+    rows.append(f"- from the first CTA's start (medians over the calls, us): last CTA starts "
+                f"{np.median(starts['last_entry']):.2f}; a CTA has the header's verdict "
+                f"{np.median(starts['header']):.2f} after it starts; first claim "
+                f"{np.median(starts['first_claim']):.2f}; first tile landed {np.median(starts['first_data']):.2f}; "
+                f"last claim {np.median(lasts):.2f}; last store issued {np.median(starts['last_store']):.2f}; "
+                f"last CTA's compute warps done {np.median(starts['last_done']):.2f}")
+    rows.append(f"- span, first claim to last store: median {np.median(spans):.2f} us")
     rows.append(f"- CTAs that took tiles: {len(np.unique(traces[0][2]))}; per-CTA interval between claims: "
                 f"{_dist(cat['interval'])} us")
     rows.append("")
@@ -147,12 +193,23 @@ def main(argv=None) -> None:
     ap.add_argument("--n", type=int, action="append", default=None,
                     help="length per --workload (default: the workload's own)")
     ap.add_argument("--runs", type=int, default=5)
+    ap.add_argument("--define", action="append", default=[], metavar="NAME=VALUE",
+                    help="compile-time setting of the variant build (repeatable)")
+    ap.add_argument("--launch-only", type=int, default=0, metavar="K",
+                    help="only launch the scan K times (a build without the trace)")
     args = ap.parse_args(argv)
-    lib = load_trace_library()
+    defines = {}
+    for d in args.define:
+        k, _, v = d.partition("=")
+        defines[k] = int(v)
+    lib = load_trace_library(defines, trace=not args.launch_only)
     for i, name in enumerate(args.workload):
         w = workloads.BY_NAME[name]
         n = args.n[i] if args.n and i < len(args.n) else w.n
-        print(summarize(w, n, run(lib, w, n, args.runs)), flush=True)
+        if args.launch_only:
+            launch_only(lib, w, n, args.launch_only)
+        else:
+            print(summarize(w, n, run(lib, w, n, args.runs)), flush=True)
 
 
 if __name__ == "__main__":

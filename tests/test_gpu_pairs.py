@@ -24,7 +24,8 @@ from prefix_scan_gb300 import api  # noqa: E402
 
 DEV = torch.device("cuda:0")
 T = 4096   # elements per tile of 8-byte elements
-SIZES = [1, 2, 31, 33, 1000, T - 1, T, T + 1, 3 * T + 7, 40 * T + 5, (1 << 20) + 3]
+# the last: enough tiles for look-back units of two tiles, an odd count
+SIZES = [1, 2, 31, 33, 1000, T - 1, T, T + 1, 3 * T + 7, 40 * T + 5, (1 << 20) + 3, 1301 * T + 5]
 
 
 def pairs(n: int, seed: int):

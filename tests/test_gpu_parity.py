@@ -56,8 +56,10 @@ def run(x: np.ndarray, exclusive: bool, inplace: bool = False, algo: str = "deco
 def sizes_for(dtype: str) -> list[int]:
     T = api.tile_elements(DTYPES[dtype][1])
     # up to 2 tiles one CTA scans the whole array; above, the look-back kernel
+    # (with look-back units of two tiles from a few thousand tiles on: an odd
+    # tile count leaves the last unit a tile past the end)
     return [1, 2, 3, 16, 31, 32, 33, 127, 1000, T - 1, T, T + 1, 2 * T - 3, 2 * T, 2 * T + 1,
-            5 * T + 17, 33 * T + 5, 65537, (1 << 20) + 3]
+            5 * T + 17, 33 * T + 5, 65537, (1 << 20) + 3, 1301 * T + 17, 1302 * T]
 
 
 @pytest.mark.parametrize("dtype", list(DTYPES))

@@ -58,7 +58,9 @@ def assert_close(got, want, cx, exclusive, dtype):
 @pytest.mark.parametrize("exclusive", [False, True], ids=["incl", "excl"])
 def test_seeded_carries(dtype, exclusive):
     T = api.tile_elements(TT[dtype])
-    for k, n in enumerate([1, 5, T, T + 1, 3 * T + 7, (1 << 20) + 3]):
+    # the last two: enough tiles for look-back units of two tiles (an odd
+    # count leaves a unit with one tile past the end)
+    for k, n in enumerate([1, 5, T, T + 1, 3 * T + 7, (1 << 20) + 3, 1301 * T + 5, 1302 * T]):
         x = make(dtype, n, 500 + k)
         c = make(dtype, 1, 900 + k)[0]
         y_want, tot_want, cx = expected(x, c, exclusive)
