@@ -728,7 +728,7 @@ def run_reduce_by_key(args, n: int = 1 << 25) -> dict:
     return res
 
 
-PROFILE_CASES = ("scan_i32_excl", "rbk_f32_L16", "rle_L16", "select_flagged", "partition_flagged")
+PROFILE_CASES = ("scan", "rbk_f32_L16", "rle_L16", "select_flagged", "partition_flagged")
 
 
 def run_profile_case(args) -> None:
@@ -739,14 +739,15 @@ def run_profile_case(args) -> None:
     from prefix_scan_gb300 import api, inputs
     dev = torch.device("cuda", 0)
     case = args.profile_case
-    if case == "scan_i32_excl":
-        # the headline kernel instance on the headline distribution
+    if case == "scan":
+        # the scan of --workload (its kind, placement and distribution) at
+        # --n elements (default 2^26)
         n = args.n or 1 << 26
-        w = workloads.I32_EXCL_2P28
+        w = workloads.BY_NAME[args.workload]
         x = torch.from_numpy(w.make(n)).to(dev)
-        out = torch.empty_like(x)
-        ws = api.alloc_workspace(torch.int32, n, dev)
-        fn = lambda: api.scan(x, exclusive=True, out=out, workspace=ws)[-1:]
+        out = x if w.inplace else torch.empty_like(x)
+        ws = api.alloc_workspace(x.dtype, n, dev)
+        fn = lambda: api.scan(x, exclusive=w.exclusive, out=out, workspace=ws)[-1:].view(torch.uint8)[:1]
     elif case in ("rbk_f32_L16", "rle_L16"):
         n = args.n or 1 << 25
         kt = torch.from_numpy(inputs.run_keys(n, 16, 27)).to(dev)
@@ -769,8 +770,9 @@ def run_profile_case(args) -> None:
     for _ in range(args.steps):
         cnt = fn()
     torch.cuda.synchronize()
-    print(json.dumps({"profile_case": case, "n": n, "launches": args.steps + 1, "count": int(cnt.item()),
-                      "status": api.device_status(ws)}), flush=True)
+    print(json.dumps({"profile_case": case, "workload": args.workload if case == "scan" else None, "n": n,
+                      "launches": args.steps + 1, "count": int(cnt.item()), "status": api.device_status(ws)}),
+          flush=True)
 
 
 def run_ops(args, n: int = 1 << 28) -> dict:
