@@ -608,7 +608,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
 #define PS_PERSIST_LBW2_FROM 0
 #endif
 #ifndef PS_PERSIST_LBW2_BELOW
-#define PS_PERSIST_LBW2_BELOW 16
+#define PS_PERSIST_LBW2_BELOW 12
 #endif
 
 template <typename T, bool EXCL, typename Op, int LBW>
