@@ -8,6 +8,7 @@
 #include <cstdint>
 
 #include "scan_internal.h"
+#include "scan_pipeline.cuh"
 
 namespace ps {
 
@@ -169,6 +170,23 @@ template <> struct Desc<unsigned long long, 2> {
         v = (w0 & 0xffffffffull) | (w1 << 32);
     }
 };
+
+// The producer that takes a tile id fetches that tile's descriptor line into
+// L2 at once.  The line was last touched by an earlier call (or never), so
+// without this the first look-back poll of it -- and, after an 8-byte
+// publish into a line that is not cached, the first read of that partly
+// written sector -- goes to DRAM, a round trip of a microsecond or more
+// while the memory streams.  By the time the tile publishes A (its data has
+// landed) and its successors poll it, the line is in L2.
+#ifndef PS_DESC_PREFETCH
+#define PS_DESC_PREFETCH 1
+#endif
+template <int DW>
+__device__ __forceinline__ void prefetch_descriptor(const void *desc, long long tile) {
+    if (PS_DESC_PREFETCH)
+        prefetch_line_l2_last(reinterpret_cast<const unsigned char *>(desc) +
+                              tile * (DW == 1 ? kDescStride32 : kDescStride64));
+}
 
 // A device-side error of call `epoch` (ps_get_device_status reads it).
 __device__ __forceinline__ void report_error(unsigned long long *status, uint32_t epoch,

@@ -253,6 +253,7 @@ persistent_kernel(PassArgs a, long long num_tiles) {
                     PS_TRACE_CTA(t);
                 }
                 tile_of[k % kRing] = t;
+                if (t < num_tiles) prefetch_descriptor<Tr::DW>(desc, t);
                 if (t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     mbar_arrive_expect_tx(&full[s], TILE_BYTES);
                     bulk_load(stage_data + (size_t)s * TILE, in + t * TILE, TILE_BYTES, &full[s]);
@@ -611,8 +612,12 @@ persistent_kernel(PassArgs a, long long num_tiles) {
 #define PS_PERSIST_LBW2_BELOW 12
 #endif
 
+// Internal linkage (static) for the launchers that keep a function-local
+// static: an external template instance's local static is a process-wide
+// (GNU-unique) symbol, so a second copy of this library loaded into the same
+// process would share the first one's record and skip its own opt-in.
 template <typename T, bool EXCL, typename Op, int LBW>
-cudaError_t launch_persistent_lbw(const PassArgs &a, long long tiles, int dev, long long grid, cudaStream_t s) {
+static cudaError_t launch_persistent_lbw(const PassArgs &a, long long tiles, int dev, long long grid, cudaStream_t s) {
     constexpr size_t smem = persistent_smem_bytes<T>();
     // the dynamic shared-memory opt-in, once per device and template instance
     // (a repeated call from a racing thread is harmless)
@@ -629,7 +634,7 @@ cudaError_t launch_persistent_lbw(const PassArgs &a, long long tiles, int dev, l
 }
 
 template <typename T, bool EXCL, typename Op>
-cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
+static cudaError_t launch_persistent_kind(const PassArgs &a, cudaStream_t s) {
     const long long tiles = (long long)((a.n + persistent_tile_elems<T>() - 1) / persistent_tile_elems<T>());
     cudaError_t e;
     int dev = 0, sms = 0;

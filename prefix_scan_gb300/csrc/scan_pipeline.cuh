@@ -91,6 +91,10 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, 
 __device__ __forceinline__ void prefetch_l2(const void *src_gmem, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src_gmem), "r"(bytes) : "memory");
 }
+// A hint: fetch the line holding p into L2, to be evicted last.
+__device__ __forceinline__ void prefetch_line_l2_last(const void *p) {
+    asm volatile("prefetch.global.L2::evict_last [%0];" :: "l"(p) : "memory");
+}
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }

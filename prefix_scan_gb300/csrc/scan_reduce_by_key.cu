@@ -220,6 +220,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 }
                 const long long t = ends ? num_tiles : (long long)atomicAdd(&hdr->tile_counter, 1ull);
                 tile_of[s] = t;
+                if (t < num_tiles) prefetch_descriptor<2>(desc, t);
                 if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     const uint32_t kb = t == 0 ? KEY_BYTES - 16u : KEY_BYTES;
                     mbar_arrive_expect_tx(&full[s], kb + VAL_BYTES);

@@ -199,6 +199,7 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 }
                 const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
                 tile_of[k % R] = t;
+                if (t < num_tiles) prefetch_descriptor<2>(desc, t);
                 if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     if (t == 0) {
                         mbar_arrive_expect_tx(&full[s], KEY_BYTES);

@@ -182,6 +182,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 }
                 const long long t = ends ? num_tiles : (long long)atomicAdd(&hdr->tile_counter, 1ull);
                 tile_of[k % R] = t;
+                if (t < num_tiles) prefetch_descriptor<1>(desc, t);
                 if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     mbar_arrive_expect_tx(&full[s], VAL_BYTES + FLAG_BYTES);
                     bulk_load(vals + (size_t)s * TILE, in + t * TILE, VAL_BYTES, &full[s]);

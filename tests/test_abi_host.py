@@ -44,6 +44,22 @@ def test_every_declared_symbol_is_exported(lib):
     assert names == set(_lib.SIGNATURES), names ^ set(_lib.SIGNATURES)
 
 
+def test_no_process_wide_symbols(lib):
+    """A function-local static of an externally visible template instance is
+    a GNU-unique symbol, which the dynamic linker binds once per process: a
+    second copy of the library (a variant build, another plug-in bundling
+    it) would then share the first one's per-device launch records and skip
+    its own shared-memory opt-in.  The library must export none."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    syms = subprocess.run([nm, "-D", str(nvbuild.LIBRARY)], capture_output=True, text=True, check=True).stdout
+    unique = [line for line in syms.splitlines() if " u " in line]
+    assert not unique, unique[:5]
+
+
 def test_workspace_size(lib):
     assert lib.ps_scan_workspace_size(0, 0) == 0
     for code in (0, 1, 2):
