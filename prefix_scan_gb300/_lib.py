@@ -44,8 +44,8 @@ SIGNATURES = {
 SIGNATURES["ps_scan_inclusive_i32_noalloc"] = (_int, [_vp, _vp, _sz, _vp])
 SIGNATURES["ps_testing_noalloc_scratch"] = (_int, [ctypes.POINTER(_vp), _vp])
 SIGNATURES["ps_trace_capacity"] = (_sz, [])
-SIGNATURES["ps_trace_read"] = (_int, [_vp, _vp, _vp, _sz])
-SIGNATURES["ps_trace_read_ctas"] = (_int, [_vp, _sz])
+SIGNATURES["ps_trace_read"] = (_int, [_int, _vp, _vp, _vp, _sz])
+SIGNATURES["ps_trace_read_ctas"] = (_int, [_int, _vp, _sz])
 SIGNATURES["ps_scan_seeded"] = (_int, [_int, _int, _vp, _vp, _sz, _vp, _vp, _vp, _sz, _vp])
 SIGNATURES["ps_scan_host_staging_size"] = (_sz, [_int, _sz])
 SIGNATURES["ps_scan_host"] = (_int, [_int, _int, _vp, _vp, _sz, _vp, _sz, _vp, _sz, _vp])

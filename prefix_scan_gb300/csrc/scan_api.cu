@@ -8,6 +8,7 @@
 
 #include "prefix_scan.h"
 #include "prefix_scan_testing.h"
+#include "prefix_scan_trace.h"
 #include "scan_internal.h"
 
 namespace {
@@ -415,3 +416,60 @@ ps_status ps_testing_set_workspace_epoch(void *ws, uint32_t epoch, ps_stream_t s
 }
 
 }  // extern "C"
+
+// ---- pipeline trace (include/prefix_scan_trace.h) ----------------------------
+extern "C" size_t ps_trace_capacity(void) {
+#ifdef PS_TRACE
+    return (size_t)PS_TRACE_TILES;
+#else
+    return 0;
+#endif
+}
+
+extern "C" ps_status ps_trace_read(int kernel, uint64_t *timestamps, uint32_t *lookback, int32_t *cta,
+                                   size_t tiles) {
+#ifdef PS_TRACE
+    if (timestamps == nullptr || lookback == nullptr || cta == nullptr || tiles > (size_t)PS_TRACE_TILES)
+        return PS_ERR_INVALID_ARG;
+    if (tiles == 0) return PS_OK;
+    cudaError_t e;
+    switch (kernel) {
+    case PS_TRACE_KERNEL_SCAN: e = ps::trace_copy_scan(timestamps, lookback, cta, tiles); break;
+    case PS_TRACE_KERNEL_SELECT: e = ps::trace_copy_select(timestamps, lookback, cta, tiles); break;
+    case PS_TRACE_KERNEL_RBK: e = ps::trace_copy_rbk(timestamps, lookback, cta, tiles); break;
+    case PS_TRACE_KERNEL_RLE: e = ps::trace_copy_rle(timestamps, lookback, cta, tiles); break;
+    default: return PS_ERR_INVALID_ARG;
+    }
+    if (e != cudaSuccess) {
+        ps::note_cuda_error(e);
+        return PS_ERR_CUDA;
+    }
+    return PS_OK;
+#else
+    (void)kernel, (void)timestamps, (void)lookback, (void)cta, (void)tiles;
+    return PS_ERR_INVALID_ARG;   // this build records no trace
+#endif
+}
+
+extern "C" ps_status ps_trace_read_ctas(int kernel, uint64_t *timestamps, size_t ctas) {
+#ifdef PS_TRACE
+    if (timestamps == nullptr || ctas > (size_t)PS_TRACE_CTAS) return PS_ERR_INVALID_ARG;
+    if (ctas == 0) return PS_OK;
+    cudaError_t e;
+    switch (kernel) {
+    case PS_TRACE_KERNEL_SCAN: e = ps::trace_copy_scan_ctas(timestamps, ctas); break;
+    case PS_TRACE_KERNEL_SELECT: e = ps::trace_copy_select_ctas(timestamps, ctas); break;
+    case PS_TRACE_KERNEL_RBK: e = ps::trace_copy_rbk_ctas(timestamps, ctas); break;
+    case PS_TRACE_KERNEL_RLE: e = ps::trace_copy_rle_ctas(timestamps, ctas); break;
+    default: return PS_ERR_INVALID_ARG;
+    }
+    if (e != cudaSuccess) {
+        ps::note_cuda_error(e);
+        return PS_ERR_CUDA;
+    }
+    return PS_OK;
+#else
+    (void)kernel, (void)timestamps, (void)ctas;
+    return PS_ERR_INVALID_ARG;   // this build records no trace
+#endif
+}

@@ -410,8 +410,8 @@ __device__ __forceinline__ U look_back(const void *desc, long long tile, uint32_
             const int limit = mp ? pos_p : 0x7fffffff;
             U part = ident;
 #pragma unroll
-            for (int j = K - 1; j >= 0; --j)   // farther tiles on the left
-                if (lane * K + j <= limit) part = Op::combine(v[j], part);
+            for (int j = K - 1; j >= 0; --j)   // from the farthest tile on: earlier parts on the left
+                if (lane * K + j <= limit) part = Op::combine(part, v[j]);
             excl = Op::combine(warp_reduce_window<U, Op>(part), excl);
             done = (mp != 0u);
             break;

@@ -232,6 +232,17 @@ cudaError_t launch_reduce_by_key(const RbkArgs &a, ps_dtype key_dt, ps_dtype val
 // of keys, so the reduce-by-key workspace size covers it.
 cudaError_t launch_run_length_encode(const RbkArgs &a, ps_dtype key_dt, cudaStream_t s);
 
+// Trace build (PS_TRACE): each kernel's translation unit copies the trace of
+// its own last launch (cudaErrorNotSupported in the product build).
+cudaError_t trace_copy_scan(uint64_t *ts, uint32_t *lookback, int32_t *cta, size_t tiles);
+cudaError_t trace_copy_scan_ctas(uint64_t *ts, size_t ctas);
+cudaError_t trace_copy_select(uint64_t *ts, uint32_t *lookback, int32_t *cta, size_t tiles);
+cudaError_t trace_copy_select_ctas(uint64_t *ts, size_t ctas);
+cudaError_t trace_copy_rbk(uint64_t *ts, uint32_t *lookback, int32_t *cta, size_t tiles);
+cudaError_t trace_copy_rbk_ctas(uint64_t *ts, size_t ctas);
+cudaError_t trace_copy_rle(uint64_t *ts, uint32_t *lookback, int32_t *cta, size_t tiles);
+cudaError_t trace_copy_rle_ctas(uint64_t *ts, size_t ctas);
+
 // Records `e` as the calling thread's last CUDA error (ps_last_cuda_error).
 void note_cuda_error(cudaError_t e);
 

@@ -39,48 +39,11 @@
 // and the loop moves on (results are then unspecified, but the kernel ends).
 #include <type_traits>
 
-#include "prefix_scan_trace.h"
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
+#include "scan_trace.cuh"
 
 namespace ps {
-
-// ---- trace build --------------------------------------------------------------
-// Built with PS_TRACE defined, the kernel records for each of the first
-// kTraceTiles tiles the %globaltimer at eight hand-offs of its pipeline
-// (claim, data landed, A published, look-back start, P published, compute
-// start, prefix received, stores issued), the CTA that took it, and the
-// look-back's windows and re-polls; ps_trace_read copies them out.  One
-// store per point by one lane; without PS_TRACE none of it is compiled.
-#ifdef PS_TRACE
-constexpr long long kTraceTiles = PS_TRACE_TILES;
-__device__ unsigned long long g_trace_ts[kTraceTiles][PS_TRACE_POINTS];
-__device__ uint32_t g_trace_lookback[kTraceTiles];
-__device__ int g_trace_cta[kTraceTiles];
-constexpr int kTraceCtas = PS_TRACE_CTAS;
-__device__ unsigned long long g_trace_cta_ts[kTraceCtas][PS_TRACE_CTA_POINTS];
-__device__ __forceinline__ void trace_cta_point(int k) {
-    if (blockIdx.x < kTraceCtas) g_trace_cta_ts[blockIdx.x][k] = global_ns();
-}
-__device__ __forceinline__ void trace_point(long long tile, int k) {
-    if (tile >= 0 && tile < kTraceTiles) g_trace_ts[tile][k] = global_ns();
-}
-__device__ __forceinline__ uint32_t *trace_lookback_slot(long long tile) {
-    return (tile >= 0 && tile < kTraceTiles) ? &g_trace_lookback[tile] : nullptr;
-}
-__device__ __forceinline__ void trace_cta(long long tile) {
-    if (tile >= 0 && tile < kTraceTiles) g_trace_cta[tile] = (int)blockIdx.x;
-}
-#define PS_TRACE_POINT(tile, k) trace_point((tile), (k))
-#define PS_TRACE_CTA(tile) trace_cta(tile)
-#define PS_TRACE_LOOKBACK(tile) trace_lookback_slot(tile)
-#define PS_TRACE_CTA_POINT(k) trace_cta_point(k)
-#else
-#define PS_TRACE_POINT(tile, k) ((void)0)
-#define PS_TRACE_CTA(tile) ((void)0)
-#define PS_TRACE_LOOKBACK(tile) nullptr
-#define PS_TRACE_CTA_POINT(k) ((void)0)
-#endif
 
 constexpr int kPCW = kThreads / 32;   // compute warps per CTA
 // The compute warps hand a stage back as soon as they hold its data in
@@ -671,49 +634,6 @@ template cudaError_t launch_persistent<float>(const PassArgs &, bool, int, cudaS
 
 }  // namespace ps
 
-extern "C" size_t ps_trace_capacity(void) {
-#ifdef PS_TRACE
-    return (size_t)ps::kTraceTiles;
-#else
-    return 0;
-#endif
-}
-
-extern "C" ps_status ps_trace_read(uint64_t *timestamps, uint32_t *lookback, int32_t *cta, size_t tiles) {
-#ifdef PS_TRACE
-    if (timestamps == nullptr || lookback == nullptr || cta == nullptr || tiles > (size_t)ps::kTraceTiles)
-        return PS_ERR_INVALID_ARG;
-    if (tiles == 0) return PS_OK;
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e == cudaSuccess)
-        e = cudaMemcpyFromSymbol(timestamps, ps::g_trace_ts, tiles * sizeof(ps::g_trace_ts[0]));
-    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(lookback, ps::g_trace_lookback, tiles * sizeof(uint32_t));
-    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(cta, ps::g_trace_cta, tiles * sizeof(int32_t));
-    if (e != cudaSuccess) {
-        ps::note_cuda_error(e);
-        return PS_ERR_CUDA;
-    }
-    return PS_OK;
-#else
-    (void)timestamps, (void)lookback, (void)cta, (void)tiles;
-    return PS_ERR_INVALID_ARG;   // this build records no trace
-#endif
-}
-
-extern "C" ps_status ps_trace_read_ctas(uint64_t *timestamps, size_t ctas) {
-#ifdef PS_TRACE
-    if (timestamps == nullptr || ctas > (size_t)ps::kTraceCtas) return PS_ERR_INVALID_ARG;
-    if (ctas == 0) return PS_OK;
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e == cudaSuccess)
-        e = cudaMemcpyFromSymbol(timestamps, ps::g_trace_cta_ts, ctas * sizeof(ps::g_trace_cta_ts[0]));
-    if (e != cudaSuccess) {
-        ps::note_cuda_error(e);
-        return PS_ERR_CUDA;
-    }
-    return PS_OK;
-#else
-    (void)timestamps, (void)ctas;
-    return PS_ERR_INVALID_ARG;   // this build records no trace
-#endif
-}
+namespace ps {
+TRACE_COPY_FUNCTIONS(trace_copy_scan, trace_copy_scan_ctas)
+}  // namespace ps

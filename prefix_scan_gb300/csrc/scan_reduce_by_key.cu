@@ -30,6 +30,7 @@
 // when it has none), found with a maximum.
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
+#include "scan_trace.cuh"
 
 namespace ps {
 
@@ -122,7 +123,12 @@ template <> struct KeyVec<unsigned long long> {
     static __device__ __forceinline__ uint32_t val(const W &w, int j) { return j == 0 ? w.x : w.y; }
 };
 
-template <typename KU> constexpr long long rbk_tile() { return sizeof(KU) == 4 ? 4096 : 2048; }
+// Keys per tile for 32-bit keys (half as many for 64-bit ones); a macro so
+// that a tuning sweep can rebuild (the workspace is sized for 4096).
+#ifndef PS_RBK_TILE32
+#define PS_RBK_TILE32 4096
+#endif
+template <typename KU> constexpr long long rbk_tile() { return sizeof(KU) == 4 ? PS_RBK_TILE32 : PS_RBK_TILE32 / 2; }
 template <typename KU> constexpr uint32_t rbk_key_bytes() {   // the tile's keys and the halo vector
     return (uint32_t)(rbk_tile<KU>() * sizeof(KU) + 16);
 }
@@ -190,6 +196,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     __shared__ uint32_t s_epoch;
     __shared__ int s_ok;
     if (tid == 0) {
+        PS_TRACE_CTA_POINT(PS_TRACE_CTA_ENTRY);
         uint32_t e;
         s_ok = begin_call(hdr, &e) ? 1 : 0;
         s_epoch = e;
@@ -207,6 +214,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     __syncthreads();
     if (!s_ok) return;   // same verdict in every CTA
     const uint32_t epoch = s_epoch;
+    if (tid == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_HEADER);
 
     if (warp == kRCW) {
         // ---------------- producer ----------------
@@ -220,7 +228,11 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 }
                 const long long t = ends ? num_tiles : (long long)atomicAdd(&hdr->tile_counter, 1ull);
                 tile_of[s] = t;
-                if (t < num_tiles) prefetch_descriptor<2>(desc, t);
+                if (t < num_tiles) {
+                    prefetch_descriptor<2>(desc, t);
+                    PS_TRACE_POINT(t, PS_TRACE_CLAIM);
+                    PS_TRACE_CTA(t);
+                }
                 if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     const uint32_t kb = t == 0 ? KEY_BYTES - 16u : KEY_BYTES;
                     mbar_arrive_expect_tx(&full[s], kb + VAL_BYTES);
@@ -247,10 +259,12 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             const long long tile = tile_of[s];
             if (tile < 0 || tile >= num_tiles) break;
             const P agg = agg_of[s];
+            if (lane == 0) PS_TRACE_POINT(tile, PS_TRACE_LOOKBACK_START);
             __syncwarp();
             P excl = 0;
             if (tile != 0) {
-                excl = look_back<P, 2, PS_RBK_LOOKBACK_K, Op>(desc, tile, epoch, a.max_polls, &hdr->status);
+                excl = look_back<P, 2, PS_RBK_LOOKBACK_K, Op>(desc, tile, epoch, a.max_polls, &hdr->status,
+                                                              PS_TRACE_LOOKBACK(tile));
                 if (lane == 0) Desc<P, 2>::store(desc, tile, kFlagP, Op::combine(excl, agg), epoch);
             }
             if (lane == 0) {
@@ -262,6 +276,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                     if (a.num_runs) *a.num_runs = runs;
                 }
                 excl_of[s] = excl;
+                PS_TRACE_POINT(tile, PS_TRACE_PREFIX);
                 mbar_arrive(&prefix_ready[s]);
             }
         }
@@ -295,6 +310,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 if (++ends == kLB) break;
                 continue;
             }
+            if (ag == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_DATA);
             const unsigned long long base = (unsigned long long)tile * TILE;
             const bool staged = a.use_bulk && base + TILE <= n;
             const int len = staged ? (int)TILE : (int)(n - base < (unsigned long long)TILE ? n - base : TILE);
@@ -370,6 +386,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 if (ag == 0) {
                     const P agg = pair_of(C, val);
                     Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
+                    PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
                     agg_of[s] = agg;
                     mbar_arrive(&agg_done[s]);
                 }
@@ -389,6 +406,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             const unsigned long long base = (unsigned long long)tile * TILE;
             const bool staged = a.use_bulk && base + TILE <= n;
             const int seg = warp * 32 * ITEMS;
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
 
             KU kk[ROWS][EPL];
             uint32_t vv[ROWS][EPL];
@@ -507,6 +525,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             if (!role_wait(&prefix_ready[s], (uint32_t)((k / S) & 1)))
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
             const P pre = Op::combine(excl_of[s], warp_excl);
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
             // Pack this warp's runs in its own slice of the stage -- free now:
             // every compute warp has read the stage (named barrier above) and
             // the aggregator finished with it before the prefix was handed
@@ -542,7 +561,9 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_STORED);
         }
+        if (warp == 0 && lane == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_DONE);
     }
 
     // the last producer readied the workspace; before an epoch wrap the
@@ -578,11 +599,13 @@ static cudaError_t launch_rbk_keys(const RbkArgs &a, ps_dtype val_dt, cudaStream
 }
 
 cudaError_t launch_reduce_by_key(const RbkArgs &a, ps_dtype key_dt, ps_dtype val_dt, cudaStream_t s) {
-    static_assert(rbk_tile<uint32_t>() == (long long)rbk_tile_elems(PS_INT32) &&
-                  rbk_tile<unsigned long long>() == (long long)rbk_tile_elems(PS_INT64),
-                  "tile sizes of the kernel and of the workspace sizing must agree");
+    static_assert(rbk_tile<uint32_t>() >= (long long)rbk_tile_elems(PS_INT32) &&
+                  rbk_tile<unsigned long long>() >= (long long)rbk_tile_elems(PS_INT64),
+                  "the workspace must hold a descriptor per tile of the kernel");
     return key_dt == PS_INT64 ? launch_rbk_keys<unsigned long long>(a, val_dt, s)
                               : launch_rbk_keys<uint32_t>(a, val_dt, s);
 }
+
+TRACE_COPY_FUNCTIONS(trace_copy_rbk, trace_copy_rbk_ctas)
 
 }  // namespace ps

@@ -35,6 +35,7 @@
 // as contiguous ranges.  Counts and positions are 32-bit (n < 2^32).
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
+#include "scan_trace.cuh"
 
 namespace ps {
 
@@ -50,7 +51,14 @@ constexpr int kLRing = 2 * kLStages;  // hand-off slots: iteration k uses k % kL
 #define PS_RLE_AGG_WARPS 2
 #endif
 constexpr int kLAgg = PS_RLE_AGG_WARPS;
-constexpr int kLThreads = (kLCW + 2 + kLAgg) * 32;   // compute, producer, look-back, aggregators
+// Look-back warps; warp j resolves iterations j, j + LB, ...  (a macro so
+// that a tuning sweep can rebuild).
+#ifndef PS_RLE_LOOKBACK_WARPS
+#define PS_RLE_LOOKBACK_WARPS 1
+#endif
+constexpr int kLLB = PS_RLE_LOOKBACK_WARPS;
+static_assert(kLRing % kLLB == 0, "the look-back warps step through the ring evenly");
+constexpr int kLThreads = (kLCW + 1 + kLLB + kLAgg) * 32;   // compute, producer, look-back, aggregators
 
 // Role waits suspend in the barrier for up to this many nanoseconds per try
 // (0: poll), so that waiting warps leave the issue slots to working ones; a
@@ -113,7 +121,11 @@ template <> struct RleVec<unsigned long long> {
 };
 
 // 32 KiB of keys per tile, plus the halo vector in front of them.
-template <typename KU> constexpr long long rle_tile() { return 32768 / (long long)sizeof(KU); }
+// Bytes of keys per tile (a macro so that a tuning sweep can rebuild).
+#ifndef PS_RLE_TILE_BYTES
+#define PS_RLE_TILE_BYTES 32768
+#endif
+template <typename KU> constexpr long long rle_tile() { return PS_RLE_TILE_BYTES / (long long)sizeof(KU); }
 template <typename KU> constexpr uint32_t rle_stage_bytes() { return (uint32_t)(rle_tile<KU>() * sizeof(KU) + 16); }
 template <typename KU> constexpr size_t rle_smem_bytes() {
     return (size_t)kLStages * rle_stage_bytes<KU>() +
@@ -168,6 +180,7 @@ rle_kernel(RbkArgs a, long long num_tiles) {
     __shared__ uint32_t s_epoch;
     __shared__ int s_ok;
     if (tid == 0) {
+        PS_TRACE_CTA_POINT(PS_TRACE_CTA_ENTRY);
         uint32_t e;
         s_ok = begin_call(hdr, &e) ? 1 : 0;
         s_epoch = e;
@@ -187,19 +200,25 @@ rle_kernel(RbkArgs a, long long num_tiles) {
     __syncthreads();
     if (!s_ok) return;   // same verdict in every CTA
     const uint32_t epoch = s_epoch;
+    if (tid == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_HEADER);
 
     if (warp == kLCW) {
         // ---------------- producer ----------------
         if (lane == 0) {
+            int ends = 0;   // end markers sent: one per look-back warp
             for (long long k = 0;; ++k) {
                 const int s = (int)(k % S);
                 if (k >= S && !rle_wait(&empty[s], (uint32_t)((k / S - 1) & 1))) {
                     report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                     break;
                 }
-                const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
+                const long long t = ends ? num_tiles : (long long)atomicAdd(&hdr->tile_counter, 1ull);
                 tile_of[k % R] = t;
-                if (t < num_tiles) prefetch_descriptor<2>(desc, t);
+                if (t < num_tiles) {
+                    prefetch_descriptor<2>(desc, t);
+                    PS_TRACE_POINT(t, PS_TRACE_CLAIM);
+                    PS_TRACE_CTA(t);
+                }
                 if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     if (t == 0) {
                         mbar_arrive_expect_tx(&full[s], KEY_BYTES);
@@ -211,13 +230,13 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 } else {
                     mbar_arrive(&full[s]);   // end marker, or a tile read from global
                 }
-                if (t >= num_tiles) break;
+                if (t >= num_tiles && ++ends == kLLB) break;
             }
             if (epoch != kEpochMask) claims_done(hdr, a.ws_bytes, epoch);
         }
-    } else if (warp == kLCW + 1) {
-        // ---------------- look-back: the tile's exclusive pair ----------------
-        for (long long k = 0;; ++k) {
+    } else if (warp > kLCW && warp <= kLCW + kLLB) {
+        // ---------------- look-back warps: the tile's exclusive pair ----------------
+        for (long long k = warp - (kLCW + 1);; k += kLLB) {
             const int slot = (int)(k % R);
             if (!rle_wait(&agg_done[slot], (uint32_t)((k / R) & 1))) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
@@ -226,10 +245,12 @@ rle_kernel(RbkArgs a, long long num_tiles) {
             const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) break;
             const P agg = agg_of[slot];
+            if (lane == 0) PS_TRACE_POINT(tile, PS_TRACE_LOOKBACK_START);
             __syncwarp();
             P excl = 0;
             if (tile != 0) {
-                excl = look_back<P, 2, kLookbackK, OpRle>(desc, tile, epoch, a.max_polls, &hdr->status);
+                excl = look_back<P, 2, kLookbackK, OpRle>(desc, tile, epoch, a.max_polls, &hdr->status,
+                                                          PS_TRACE_LOOKBACK(tile));
                 if (lane == 0) Desc<P, 2>::store(desc, tile, kFlagP, OpRle::combine(excl, agg), epoch);
             }
             if (lane == 0) {
@@ -242,14 +263,16 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                     if (a.num_runs) *a.num_runs = runs;
                 }
                 excl_of[slot] = excl;
+                PS_TRACE_POINT(tile, PS_TRACE_PREFIX);
                 mbar_arrive(&prefix_ready[slot]);
             }
         }
-    } else if (warp >= kLCW + 2) {
+    } else if (warp > kLCW + kLLB) {
         // ---------------- aggregators: the tile's pair, published at once ----------------
         // kLAgg warps, each over an equal part of the tile; the last to
         // finish combines the parts and publishes the pair.
-        const int g = warp - (kLCW + 2);
+        const int g = warp - (kLCW + 1 + kLLB);
+        int ends = 0;   // end markers passed on: one per look-back warp
         for (long long k = 0;; ++k) {
             const int s = (int)(k % S);
             if (!rle_wait(&full[s], (uint32_t)((k / S) & 1))) {
@@ -258,10 +281,12 @@ rle_kernel(RbkArgs a, long long num_tiles) {
             }
             const int slot = (int)(k % R);
             const long long tile = tile_of[slot];
-            if (tile < 0 || tile >= num_tiles) {   // end marker: pass it on to the look-back warp
+            if (tile < 0 || tile >= num_tiles) {   // end marker: pass it on to a look-back warp
                 if (g == 0 && lane == 0) mbar_arrive(&agg_done[slot]);
-                break;
+                if (++ends == kLLB) break;
+                continue;
             }
+            if (g == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_DATA);
             const unsigned long long base = (unsigned long long)tile * TILE;
             uint32_t heads = 0;
             uint32_t last = 0;   // position of the part's last head (0: none)
@@ -337,6 +362,7 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                     for (int gg = 0; gg < kLAgg; ++gg) agg = OpRle::combine(agg, (P)part[gg]);
                     s_parts_done[slot] = 0;   // the slot's next use is kLRing iterations on
                     Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
+                    PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
                     agg_of[slot] = agg;
                     mbar_arrive(&agg_done[slot]);
                 }
@@ -357,6 +383,7 @@ rle_kernel(RbkArgs a, long long num_tiles) {
             const unsigned long long base = (unsigned long long)tile * TILE;
             const bool staged = a.use_bulk && base + TILE <= n;
             const int seg = warp * 32 * ITEMS;   // the warp's first key in the tile
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
 
             // Rows of two 16-byte vectors per lane (EPL keys); lanes 4-7 of
             // each quarter-warp read their pair in swapped order, so that
@@ -456,6 +483,7 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
             const P pre = OpRle::combine(excl_of[slot], warp_excl);
             const uint32_t cw = (uint32_t)(pre >> 32), pw = (uint32_t)pre;
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
 
             if (!dense) {
                 // each head: its key to unique_keys[c], and the length of run
@@ -513,7 +541,9 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 }
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_STORED);
         }
+        if (warp == 0 && lane == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_DONE);
     }
 
     // the last producer readied the workspace; before an epoch wrap the
@@ -548,5 +578,7 @@ cudaError_t launch_run_length_encode(const RbkArgs &a, ps_dtype key_dt, cudaStre
                   "run-length encoding must need no more descriptors than reduce-by-key");
     return key_dt == PS_INT64 ? launch_rle_keys<unsigned long long>(a, s) : launch_rle_keys<uint32_t>(a, s);
 }
+
+TRACE_COPY_FUNCTIONS(trace_copy_rle, trace_copy_rle_ctas)
 
 }  // namespace ps

@@ -27,6 +27,7 @@
 // aligned values and flags.
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
+#include "scan_trace.cuh"
 
 namespace ps {
 
@@ -151,6 +152,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
     __shared__ uint32_t s_epoch;
     __shared__ int s_ok;
     if (tid == 0) {
+        PS_TRACE_CTA_POINT(PS_TRACE_CTA_ENTRY);
         uint32_t e;
         s_ok = begin_call(hdr, &e) ? 1 : 0;
         s_epoch = e;
@@ -169,6 +171,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
     __syncthreads();
     if (!s_ok) return;   // same verdict in every CTA
     const uint32_t epoch = s_epoch;
+    if (tid == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_HEADER);
 
     if (warp == kSCW) {
         // ---------------- producer ----------------
@@ -182,7 +185,11 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 }
                 const long long t = ends ? num_tiles : (long long)atomicAdd(&hdr->tile_counter, 1ull);
                 tile_of[k % R] = t;
-                if (t < num_tiles) prefetch_descriptor<1>(desc, t);
+                if (t < num_tiles) {
+                    prefetch_descriptor<1>(desc, t);
+                    PS_TRACE_POINT(t, PS_TRACE_CLAIM);
+                    PS_TRACE_CTA(t);
+                }
                 if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
                     mbar_arrive_expect_tx(&full[s], VAL_BYTES + FLAG_BYTES);
                     bulk_load(vals + (size_t)s * TILE, in + t * TILE, VAL_BYTES, &full[s]);
@@ -210,6 +217,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 if (++ends == LB) break;
                 continue;
             }
+            if (lane == 0) PS_TRACE_POINT(tile, PS_TRACE_DATA);
             const unsigned long long base = (unsigned long long)tile * TILE;
             U cnt = 0;
             if (a.use_bulk && base + TILE <= n) {
@@ -243,6 +251,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
             const U agg = __reduce_add_sync(kFull, cnt);
             if (lane == 0) {
                 Desc<U, 1>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
+                PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
                 agg_of[slot] = agg;
                 mbar_arrive(&agg_done[slot]);
             }
@@ -259,15 +268,18 @@ select_kernel(SelectArgs a, long long num_tiles) {
             const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) break;
             const U agg = agg_of[slot];
+            if (lane == 0) PS_TRACE_POINT(tile, PS_TRACE_LOOKBACK_START);
             __syncwarp();
             U excl = 0;
             if (tile != 0) {
-                excl = look_back<U, 1, kLookbackK>(desc, tile, epoch, a.max_polls, &hdr->status);
+                excl = look_back<U, 1, kLookbackK>(desc, tile, epoch, a.max_polls, &hdr->status,
+                                                   PS_TRACE_LOOKBACK(tile));
                 if (lane == 0) Desc<U, 1>::store(desc, tile, kFlagP, excl + agg, epoch);
             }
             if (lane == 0) {
                 if (a.num_selected && tile == num_tiles - 1) *a.num_selected = (unsigned long long)(excl + agg);
                 excl_of[slot] = excl;
+                PS_TRACE_POINT(tile, PS_TRACE_PREFIX);
                 mbar_arrive(&prefix_ready[slot]);
             }
         }
@@ -286,6 +298,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
             const unsigned long long base = (unsigned long long)tile * TILE;
             const bool staged = a.use_bulk && base + TILE <= n;
             const int seg = warp * 32 * ITEMS;
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
 
             T v[ROWS][VEC];
             uint32_t sel[ROWS];   // bit j: element j of this lane's row chunk is kept
@@ -349,6 +362,7 @@ select_kernel(SelectArgs a, long long num_tiles) {
             if (!mbar_wait(&prefix_ready[slot], (uint32_t)((k / R) & 1)))
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
             const U tile_excl = excl_of[slot];
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
 
             if (!PARTITION) {
                 // select: kept elements straight to their places; within a
@@ -396,7 +410,9 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 for (U q = lane; q < w_rej; q += 32) out[n - 1 - (rej_before + q)] = wbuf[w_sel + q];
                 __syncwarp();   // the slice is packed again next iteration
             }
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_STORED);
         }
+        if (warp == 0 && lane == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_DONE);
     }
 
     // the last producer readied the workspace; before an epoch wrap the
@@ -443,5 +459,7 @@ cudaError_t launch_select(const SelectArgs &a, int op, bool partition, cudaStrea
 template cudaError_t launch_select<int32_t>(const SelectArgs &, int, bool, cudaStream_t);
 template cudaError_t launch_select<int64_t>(const SelectArgs &, int, bool, cudaStream_t);
 template cudaError_t launch_select<float>(const SelectArgs &, int, bool, cudaStream_t);
+
+TRACE_COPY_FUNCTIONS(trace_copy_select, trace_copy_select_ctas)
 
 }  // namespace ps

@@ -18,6 +18,7 @@ Look-back", summary page, sections 4.1 and 4.4) is meant to keep the
 look-back off the critical path; these figures say whether it does.
 
     python -m prefix_scan_gb300.trace --workload i32_excl_2p28 [--runs 5]
+    python -m prefix_scan_gb300.trace --kernel rle --n 33554432 [--mean-run 16]
 
 ``--define NAME=VALUE`` rebuilds the variant with other compile-time
 settings of the kernel (for example the look-back's poll back-off), and
@@ -81,35 +82,85 @@ def launch_only(lib: ctypes.CDLL, w: workloads.Workload, n: int, launches: int) 
     print(f"{w.name} n={n}: {launches + 1} launches, device status {st.value}", flush=True)
 
 
-def run(lib: ctypes.CDLL, w: workloads.Workload, n: int, runs: int):
+# Kernels the trace covers: the record each keeps (include/prefix_scan_trace.h)
+# and the elements of one of its tiles (32-bit keys / elements).
+KERNELS = {"scan": 0, "select": 1, "partition": 1, "rbk": 2, "rle": 3}
+RBK_TILE, RLE_TILE = 4096, 8192
+
+
+def make_call(lib: ctypes.CDLL, kernel: str, w: workloads.Workload | None, n: int, mean_run: int, dev):
+    """(call(stream) -> status, tiles, keep-alive tensors) for one launch of
+    `kernel` on seeded inputs of length n: the scan workload `w`; select and
+    partition of full-range int32 values by Bernoulli(1/2) flags; reduce-by-key
+    ({int32 key, fp32 value}) and run-length encoding of int32 keys in runs of
+    mean length `mean_run`."""
+    import torch
+    from prefix_scan_gb300 import inputs
+    if kernel == "scan":
+        code = {"int32": _lib.PS_INT32, "int64": _lib.PS_INT64, "float32": _lib.PS_FLOAT32}[w.dtype]
+        x = torch.from_numpy(w.make(n)).to(dev)
+        out = x if w.inplace else torch.empty_like(x)
+        ws = torch.zeros(max(int(lib.ps_scan_workspace_size(code, n)), 16), dtype=torch.uint8, device=dev)
+
+        def call(stream):
+            return lib.ps_scan(_lib.PS_ALGO_DECOUPLED_LOOKBACK, code, int(w.exclusive), x.data_ptr(),
+                               out.data_ptr(), n, ws.data_ptr(), ws.numel(), stream)
+        return call, -(-n // int(lib.ps_tile_elements(code))), (x, out, ws)
+    if kernel in ("select", "partition"):
+        x = torch.from_numpy(inputs.full_range_i32(n, 8)).to(dev)
+        flags = torch.from_numpy(inputs.bernoulli_half(n, 3).astype(np.uint8)).to(dev)
+        out = torch.empty_like(x)
+        cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+        ws = torch.zeros(max(int(lib.ps_scan_workspace_size(_lib.PS_INT32, n)), 16), dtype=torch.uint8, device=dev)
+        fn = lib.ps_partition if kernel == "partition" else lib.ps_select
+
+        def call(stream):
+            return fn(_lib.PS_INT32, 0, x.data_ptr(), flags.data_ptr(), None, out.data_ptr(), cnt.data_ptr(), n,
+                      ws.data_ptr(), ws.numel(), stream)
+        return call, -(-n // int(lib.ps_tile_elements(_lib.PS_INT32))), (x, flags, out, cnt, ws)
+    keys = torch.from_numpy(inputs.run_keys(n, mean_run, 11)).to(dev)
+    vals = torch.from_numpy(inputs.uniform_f32(n, 12)).to(dev)
+    uk = torch.empty_like(keys)
+    ag = torch.empty(n, dtype=torch.int32 if kernel == "rle" else torch.float32, device=dev)
+    nr = torch.zeros(1, dtype=torch.int64, device=dev)
+    ws = torch.zeros(max(int(lib.ps_reduce_by_key_workspace_size(_lib.PS_INT32, n)), 16), dtype=torch.uint8,
+                     device=dev)
+
+    def call(stream):
+        if kernel == "rle":
+            return lib.ps_run_length_encode(_lib.PS_INT32, keys.data_ptr(), uk.data_ptr(), ag.data_ptr(),
+                                            nr.data_ptr(), n, ws.data_ptr(), ws.numel(), stream)
+        return lib.ps_reduce_by_key(_lib.PS_INT32, _lib.PS_FLOAT32, keys.data_ptr(), vals.data_ptr(), uk.data_ptr(),
+                                    ag.data_ptr(), nr.data_ptr(), n, ws.data_ptr(), ws.numel(), stream)
+    return call, -(-n // (RLE_TILE if kernel == "rle" else RBK_TILE)), (keys, vals, uk, ag, nr, ws)
+
+
+def run(lib: ctypes.CDLL, w: workloads.Workload | None, n: int, runs: int, kernel: str = "scan",
+        mean_run: int = 16):
     """Traces of `runs` calls (L2 flushed before each): list of
     (timestamps[tiles, 8] in us from the first CTA's start, lookback[tiles],
     cta[tiles], per-CTA timestamps[ctas, 3] in us on the same base)."""
     import torch
     dev = torch.device("cuda", 0)
-    code = {"int32": _lib.PS_INT32, "int64": _lib.PS_INT64, "float32": _lib.PS_FLOAT32}[w.dtype]
-    x = torch.from_numpy(w.make(n)).to(dev)
-    out = x if w.inplace else torch.empty_like(x)
-    ws = torch.zeros(max(int(lib.ps_scan_workspace_size(code, n)), 16), dtype=torch.uint8, device=dev)
+    call, tiles, keep = make_call(lib, kernel, w, n, mean_run, dev)
+    which = KERNELS[kernel]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    tiles = -(-n // int(lib.ps_tile_elements(code)))
     tiles = min(tiles, int(lib.ps_trace_capacity()))
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     traces = []
     for r in range(runs + 1):   # the first call warms up and is dropped
         flush.fill_(r & 0xFF)
-        st = lib.ps_scan(_lib.PS_ALGO_DECOUPLED_LOOKBACK, code, int(w.exclusive), x.data_ptr(), out.data_ptr(),
-                         n, ws.data_ptr(), ws.numel(), stream)
-        _lib.check("ps_scan", st)
+        _lib.check(kernel, call(stream))
         ts = np.zeros((tiles, 8), dtype=np.uint64)
         lb = np.zeros(tiles, dtype=np.uint32)
         cta = np.zeros(tiles, dtype=np.int32)
-        _lib.check("ps_trace_read", lib.ps_trace_read(ts.ctypes.data, lb.ctypes.data, cta.ctypes.data, tiles))
+        _lib.check("ps_trace_read", lib.ps_trace_read(which, ts.ctypes.data, lb.ctypes.data, cta.ctypes.data,
+                                                      tiles))
         if r == 0:
             continue
         ctas = int(cta.max()) + 1
         cts = np.zeros((ctas, 3), dtype=np.uint64)
-        _lib.check("ps_trace_read_ctas", lib.ps_trace_read_ctas(cts.ctypes.data, ctas))
+        _lib.check("ps_trace_read_ctas", lib.ps_trace_read_ctas(which, cts.ctypes.data, ctas))
         t0 = int(cts[:, 0].min())
         t = (ts.astype(np.int64) - t0) / 1e3
         ct = (cts.astype(np.int64) - t0) / 1e3
@@ -121,7 +172,7 @@ def _dist(v: np.ndarray) -> str:
     return f"{np.median(v):.2f} ({np.percentile(v, 10):.2f} / {np.percentile(v, 90):.2f})"
 
 
-def summarize(w: workloads.Workload, n: int, traces) -> str:
+def summarize(name: str, n: int, traces) -> str:
     rows = []
     spans, lasts = [], []
     gaps = {k: [] for k in ("claim_A", "A_lb", "lb", "P_compute", "compute_stored", "claim_stored",
@@ -156,7 +207,7 @@ def summarize(w: workloads.Workload, n: int, traces) -> str:
     win = np.concatenate(windows)
     pol = np.concatenate(polls)
     tiles = traces[0][0].shape[0]
-    rows.append(f"### {w.name} at n = {n} ({tiles} tiles, {len(traces)} traced calls, L2 flushed before each)")
+    rows.append(f"### {name} at n = {n} ({tiles} tiles, {len(traces)} traced calls, L2 flushed before each)")
     rows.append("")
     rows.append(f"- from the first CTA's start (medians over the calls, us): last CTA starts "
                 f"{np.median(starts['last_entry']):.2f}; a CTA has the header's verdict "
@@ -189,7 +240,11 @@ def summarize(w: workloads.Workload, n: int, traces) -> str:
 
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--workload", action="append", choices=sorted(workloads.BY_NAME), required=True)
+    ap.add_argument("--workload", action="append", choices=sorted(workloads.BY_NAME), default=[],
+                    help="scan workload (repeatable)")
+    ap.add_argument("--kernel", action="append", choices=[k for k in KERNELS if k != "scan"], default=[],
+                    help="another persistent kernel, on its seeded inputs (repeatable; length from --n)")
+    ap.add_argument("--mean-run", type=int, default=16, help="mean run length of the rbk / rle keys")
     ap.add_argument("--n", type=int, action="append", default=None,
                     help="length per --workload (default: the workload's own)")
     ap.add_argument("--runs", type=int, default=5)
@@ -209,7 +264,13 @@ def main(argv=None) -> None:
         if args.launch_only:
             launch_only(lib, w, n, args.launch_only)
         else:
-            print(summarize(w, n, run(lib, w, n, args.runs)), flush=True)
+            print(summarize(w.name, n, run(lib, w, n, args.runs)), flush=True)
+    for j, kernel in enumerate(args.kernel):
+        i = len(args.workload) + j
+        n = args.n[i] if args.n and i < len(args.n) else 1 << 25
+        label = kernel + (f" (int32 keys, mean run {args.mean_run})" if kernel in ("rbk", "rle")
+                          else " (int32 values, flag array, Bernoulli(1/2))")
+        print(summarize(label, n, run(lib, None, n, args.runs, kernel, args.mean_run)), flush=True)
 
 
 if __name__ == "__main__":

@@ -1,4 +1,5 @@
-"""Scans, pair scans and select from a tiny-tile build of the library.
+"""Scans, pair scans, select and reduce-by-key from a tiny-tile build of the
+library.
 
 A second copy of the library is built with the smallest tile geometry the
 scan and select kernels accept (four elements per thread: tiles of 1024
@@ -8,6 +9,9 @@ role hand-offs per byte.  That is where a wrong ordering of a descriptor's
 words (or of a hand-off) would show as a rare mismatch, so each case runs
 100 times over thousands of tiles, every run against the oracle: integers
 bit for bit, fp32 within FP32_REL * sum|x| + FP32_ABS of the fp64 result.
+The build's look-back also reads two descriptors per lane, so the affine
+maps and the segmented sum of reduce-by-key (operators that are not
+commutative) check that a window is folded in sequence order.
 """
 from __future__ import annotations
 
@@ -163,4 +167,27 @@ def test_select_and_partition_repeated(tiny):
             assert st == _lib.PS_OK
             assert int(cnt.item()) == m, (fname, k)
             assert torch.equal(o[:m], rs) if fname == "ps_select" else torch.equal(o, rp), (fname, k)
+    assert _status(tiny, ws) == _lib.PS_OK
+
+
+def test_reduce_by_key_repeated(tiny):
+    # reduce-by-key keeps its own tiles (4096 keys) but this build's
+    # two-descriptor look-back window: its segmented sum is not commutative
+    keys = inputs.run_keys(N, 16, 48)
+    vals = inputs.full_range_i32(N, 49)
+    want_keys, want_sums = oracle.reduce_by_key(keys, vals)
+    m = want_keys.shape[0]
+    kt, vt = torch.from_numpy(keys).to(DEV), torch.from_numpy(vals).to(DEV)
+    uk, ag = torch.empty_like(kt), torch.empty_like(vt)
+    nr = torch.zeros(1, dtype=torch.int64, device=DEV)
+    ws = torch.zeros(max(int(tiny.ps_reduce_by_key_workspace_size(_lib.PS_INT32, N)), 16), dtype=torch.uint8,
+                     device=DEV)
+    rk = torch.from_numpy(want_keys.view(np.int32)).to(DEV)
+    rs = torch.from_numpy(want_sums.view(np.int32)).to(DEV)
+    for k in range(REPEATS):
+        st = tiny.ps_reduce_by_key(_lib.PS_INT32, _lib.PS_INT32, kt.data_ptr(), vt.data_ptr(), uk.data_ptr(),
+                                   ag.data_ptr(), nr.data_ptr(), N, ws.data_ptr(), ws.numel(), _stream())
+        assert st == _lib.PS_OK
+        assert int(nr.item()) == m, k
+        assert torch.equal(uk[:m], rk) and torch.equal(ag[:m], rs), k
     assert _status(tiny, ws) == _lib.PS_OK
