@@ -21,18 +21,29 @@
 // kernel (scan_reduce_by_key.cu); lengths need none: a length is a
 // difference of two head positions.
 //
-// Structure as in the persistent scan and the select kernel: a producer warp
-// takes tile ids and bulk-copies the tile's keys -- starting one 16-byte
-// vector early, so the key before the tile (the "halo") is in shared memory
-// too -- into a 3-stage ring; two aggregator warps count the heads of half
-// the tile each and find the last one, and the second to finish publishes
-// the tile's pair; a look-back warp resolves the tile's exclusive pair;
-// eight compute warps find the heads of their rows, count them with warp
-// scans and write each head's key and the length of the run it closes.  A
-// warp with few heads writes them straight from registers and hands the
-// stage back as soon as the keys are in registers; a warp dense in heads
-// packs each row's runs in its slice of the stage first, so that they go out
-// as contiguous ranges.  Counts and positions are 32-bit (n < 2^32).
+// Roles.  A producer warp takes tile ids and bulk-copies each tile's keys --
+// starting one 16-byte vector early, so the key before the tile (the "halo")
+// is in shared memory too -- into a ring of stages.  Eight compute warps
+// take the tiles in order and never wait for a tile's prefix: they find the
+// heads, count them (warp scans, then the warps' totals), publish the tile's
+// pair (A; P for tile 0) themselves, and pack the tile's runs into an output
+// buffer -- each head's key and 16-bit position within the tile, in order --
+// after which the stage goes straight back to the producer.  Look-back
+// warps resolve each tile's exclusive pair; a writer warp waits for it and
+// writes the buffer out as contiguous ranges (keys, and lengths as
+// differences of consecutive head positions), then frees the buffer.  So a stage is held only from its copy
+// to the compute warps' pass, and the look-back's latency stays off both the
+// stages and the compute warps: it is covered by the output buffers, which
+// hold a few bytes per head.  A tile with more heads than a buffer holds
+// (a dense tile) is written by the compute warps themselves -- eight warps
+// instead of one for a tile that writes as much as it reads -- one
+// iteration late: they publish its pair, keep its stage, do the next tile's
+// pass (so that tile's pair is published too), and only then wait for the
+// dense tile's prefix, re-read its keys from the stage, pack each row's runs
+// in their slice of the stage and write them as contiguous ranges.  Waiting
+// for a tile's prefix before publishing the next tile's pair would chain
+// every CTA's tiles behind the look-backs of its earlier ones.  Counts and
+// positions are 32-bit (n < 2^32).
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
 #include "scan_trace.cuh"
@@ -42,23 +53,52 @@ namespace ps {
 namespace {
 
 constexpr int kLCW = kThreads / 32;   // compute warps per CTA
-constexpr int kLStages = 3;
-constexpr int kLRing = 2 * kLStages;  // hand-off slots: iteration k uses k % kLRing
-// Aggregator warps: each reduces an equal part of a tile.  One warp took
-// about 2 us per 32 KiB tile, which capped each CTA at one tile per
-// aggregation; twelve warps of 80 registers still fit two CTAs per SM.
-#ifndef PS_RLE_AGG_WARPS
-#define PS_RLE_AGG_WARPS 2
+// Stages of keys (32 KiB each) and output buffers (a macro each, so that a
+// tuning sweep can rebuild).
+#ifndef PS_RLE_STAGES
+#define PS_RLE_STAGES 2
 #endif
-constexpr int kLAgg = PS_RLE_AGG_WARPS;
-// Look-back warps; warp j resolves iterations j, j + LB, ...  (a macro so
-// that a tuning sweep can rebuild).
+#ifndef PS_RLE_OUT_BUFFERS
+#define PS_RLE_OUT_BUFFERS 4
+#endif
+#ifndef PS_RLE_OUT_BYTES
+#define PS_RLE_OUT_BYTES 8192
+#endif
+// Descriptors per lane in the look-back window (the operator is commutative).
+#ifndef PS_RLE_LOOKBACK_K
+#define PS_RLE_LOOKBACK_K PS_LOOKBACK_K
+#endif
+// Look-back warps (warp j resolves iterations j, j + LB, ...) and writer
+// warps (the same, for the write-out).
 #ifndef PS_RLE_LOOKBACK_WARPS
-#define PS_RLE_LOOKBACK_WARPS 1
+#define PS_RLE_LOOKBACK_WARPS 2
 #endif
+#ifndef PS_RLE_WRITER_WARPS
+#define PS_RLE_WRITER_WARPS 1
+#endif
+constexpr int kLStages = PS_RLE_STAGES;
+constexpr int kLOut = PS_RLE_OUT_BUFFERS;
+constexpr int kLOutBytes = PS_RLE_OUT_BYTES;
 constexpr int kLLB = PS_RLE_LOOKBACK_WARPS;
-static_assert(kLRing % kLLB == 0, "the look-back warps step through the ring evenly");
-constexpr int kLThreads = (kLCW + 1 + kLLB + kLAgg) * 32;   // compute, producer, look-back, aggregators
+constexpr int kLW = PS_RLE_WRITER_WARPS;
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+// Iterations past the end that the compute warps mark: every look-back and
+// writer warp waits on its next iteration.
+constexpr int kLEnds = cmax(kLLB, kLW);
+// Hand-off slots (tile id, pair, exclusive pair, buffer kind and the
+// agg_done / prefix_ready / packed mbarriers): iteration k uses slot k % R.
+// A slot is reused only after every role is done with it: the writer is at
+// most kLOut iterations behind the compute warps (each waits for its buffer
+// before a sparse tile), the producer at most kLStages + 1 ahead of their
+// pass, and the compute warps write the end markers of up to kLEnds
+// iterations ahead.
+constexpr int ring_slots() {
+    const int need = cmax(kLStages + kLOut + 1, kLEnds + kLOut);
+    return (need + 1) / 2 * 2;
+}
+constexpr int kLRing = ring_slots();
+constexpr int kLThreads = (kLCW + 1 + kLLB + kLW) * 32;   // compute, producer, look-back, writer
+static_assert(kLStages >= 2, "a dense tile keeps its stage while the next one is scanned");
 
 // Role waits suspend in the barrier for up to this many nanoseconds per try
 // (0: poll), so that waiting warps leave the issue slots to working ones; a
@@ -66,13 +106,7 @@ constexpr int kLThreads = (kLCW + 1 + kLLB + kLAgg) * 32;   // compute, producer
 #ifndef PS_RLE_WAIT_NS
 #define PS_RLE_WAIT_NS 2000
 #endif
-// A warp whose 32 x ITEMS keys hold more heads than this packs each row's
-// runs in its slice of the stage and writes them out as contiguous ranges;
-// below it, each head is written straight from registers.
-#ifndef PS_RLE_DENSE_HEADS
-#define PS_RLE_DENSE_HEADS 128
-#endif
-// Position of packed entry q in a warp's slice: XOR-swizzled within each 32
+// Position of packed entry q in an output buffer: XOR-swizzled within each 32
 // entries, so that lanes packing entries 8 apart (every key a head) and
 // lanes reading 32 consecutive entries hit distinct banks.
 __device__ __forceinline__ uint32_t rle_sw(uint32_t q) { return q ^ ((q >> 5) & 7u); }
@@ -120,16 +154,21 @@ template <> struct RleVec<unsigned long long> {
     static __device__ __forceinline__ unsigned long long key(const V &v, int j) { return vget(v, j); }
 };
 
-// 32 KiB of keys per tile, plus the halo vector in front of them.
 // Bytes of keys per tile (a macro so that a tuning sweep can rebuild).
 #ifndef PS_RLE_TILE_BYTES
 #define PS_RLE_TILE_BYTES 32768
 #endif
 template <typename KU> constexpr long long rle_tile() { return PS_RLE_TILE_BYTES / (long long)sizeof(KU); }
 template <typename KU> constexpr uint32_t rle_stage_bytes() { return (uint32_t)(rle_tile<KU>() * sizeof(KU) + 16); }
+// Runs an output buffer holds: a key and a 16-bit position within the tile
+// each, a multiple of 32 entries (the swizzle stays within each 32).
+template <typename KU> constexpr int rle_out_cap() {
+    return (int)((kLOutBytes / (sizeof(KU) + 2)) / 32 * 32);
+}
 template <typename KU> constexpr size_t rle_smem_bytes() {
-    return (size_t)kLStages * rle_stage_bytes<KU>() +
-           ((size_t)kLStages * 2 * 8 + (size_t)kLRing * (2 * 8 + 8 + 8 + 8) + 127) / 128 * 128;
+    return (size_t)kLStages * rle_stage_bytes<KU>() + (size_t)kLOut * kLOutBytes +
+           ((size_t)kLStages * 2 * 8 + (size_t)kLOut * 8 + (size_t)kLRing * (3 * 8 + 8 + 8 + 8 + 8) + 127) / 128 *
+               128;
 }
 
 }  // namespace
@@ -146,27 +185,38 @@ rle_kernel(RbkArgs a, long long num_tiles) {
     constexpr int ITEMS = (int)(TILE / kThreads);   // keys per compute lane
     constexpr int EPL = 2 * VK;                     // keys per lane per row: two vectors
     constexpr int ROWS = ITEMS / EPL;
-    constexpr int S = kLStages, R = kLRing;
+    constexpr int S = kLStages, R = kLRing, NOB = kLOut;
     constexpr uint32_t KEY_BYTES = (uint32_t)(TILE * sizeof(KU));
     constexpr uint32_t STAGE = rle_stage_bytes<KU>();
-    constexpr int NV = (int)(TILE / VK);   // vectors per tile
     constexpr int CT = kLCW * 32;
-    static_assert(ITEMS % EPL == 0 && NV % 32 == 0 && STAGE % 16 == 0, "tile geometry");
+    constexpr int CAP = rle_out_cap<KU>();
+    static_assert(ITEMS % EPL == 0 && STAGE % 16 == 0 && TILE <= 65536, "tile geometry (16-bit positions)");
+    static_assert(CAP >= 32, "output buffer geometry");
+    // a dense tile's runs of one row, packed in the warp's slice of the stage
+    static_assert(32 * EPL * (sizeof(KU) + 4) <= 32 * ITEMS * sizeof(KU), "a row's runs fit the slice");
 
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * STAGE);
+    unsigned char *outbuf = smem + (size_t)S * STAGE;
+    uint64_t *full = reinterpret_cast<uint64_t *>(outbuf + (size_t)NOB * kLOutBytes);
     uint64_t *empty = full + S;
-    uint64_t *agg_done = empty + S;   // the rest: R slots, slot k % R
+    uint64_t *ob_empty = empty + S;
+    uint64_t *agg_done = ob_empty + NOB;   // the rest: R slots, slot k % R
     uint64_t *prefix_ready = agg_done + R;
-    long long *tile_of = reinterpret_cast<long long *>(prefix_ready + R);
+    uint64_t *packed = prefix_ready + R;
+    long long *tile_of = reinterpret_cast<long long *>(packed + R);
     P *agg_of = reinterpret_cast<P *>(tile_of + R);
     P *excl_of = agg_of + R;
+    int *sparse_of = reinterpret_cast<int *>(excl_of + R);
     __shared__ P s_warp[2][kLCW];
     __shared__ int s_abort;   // a compute warp's wait ran out: all of them leave
-    __shared__ P s_part[kLRing][kLAgg];   // the aggregators' parts of a tile's pair
-    __shared__ int s_parts_done[kLRing];  // parts in: the last one publishes
     // stage s: [halo vector][TILE keys]
     auto stage_keys = [&](int s) { return reinterpret_cast<KU *>(smem + (size_t)s * STAGE + 16); };
+    // output buffer o: a sparse tile's runs, CAP keys then CAP positions
+    // (within the tile), entry q at rle_sw(q)
+    auto out_keys = [&](int o) { return reinterpret_cast<KU *>(outbuf + (size_t)o * kLOutBytes); };
+    auto out_pos = [&](int o) {
+        return reinterpret_cast<uint16_t *>(outbuf + (size_t)o * kLOutBytes + (size_t)CAP * sizeof(KU));
+    };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     Header *hdr = reinterpret_cast<Header *>(a.ws);
@@ -181,19 +231,26 @@ rle_kernel(RbkArgs a, long long num_tiles) {
     __shared__ int s_ok;
     if (tid == 0) {
         PS_TRACE_CTA_POINT(PS_TRACE_CTA_ENTRY);
+        if (PS_PREFETCH_FIRST_TILES && a.use_bulk) {
+            for (int j = 0; j < S; ++j) {
+                const unsigned long long t = blockIdx.x + (unsigned long long)j * gridDim.x;
+                if ((t + 1) * (unsigned long long)TILE <= n) prefetch_l2(keys + t * TILE, KEY_BYTES);
+            }
+        }
         uint32_t e;
         s_ok = begin_call(hdr, &e) ? 1 : 0;
         s_epoch = e;
         s_abort = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kLCW + kLAgg);   // compute warps + aggregators
+            mbar_init(&empty[s], 1);     // the compute warps, or the writer of a dense tile
         }
+        for (int o = 0; o < NOB; ++o) mbar_init(&ob_empty[o], 1);   // the writer
         for (int slot = 0; slot < R; ++slot) {
             mbar_init(&agg_done[slot], 1);
             mbar_init(&prefix_ready[slot], 1);
+            mbar_init(&packed[slot], kLCW);
             tile_of[slot] = num_tiles;   // end marker until the producer fills it
-            s_parts_done[slot] = 0;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -205,14 +262,13 @@ rle_kernel(RbkArgs a, long long num_tiles) {
     if (warp == kLCW) {
         // ---------------- producer ----------------
         if (lane == 0) {
-            int ends = 0;   // end markers sent: one per look-back warp
             for (long long k = 0;; ++k) {
                 const int s = (int)(k % S);
                 if (k >= S && !rle_wait(&empty[s], (uint32_t)((k / S - 1) & 1))) {
                     report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                     break;
                 }
-                const long long t = ends ? num_tiles : (long long)atomicAdd(&hdr->tile_counter, 1ull);
+                const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
                 tile_of[k % R] = t;
                 if (t < num_tiles) {
                     prefetch_descriptor<2>(desc, t);
@@ -230,7 +286,7 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 } else {
                     mbar_arrive(&full[s]);   // end marker, or a tile read from global
                 }
-                if (t >= num_tiles && ++ends == kLLB) break;
+                if (t >= num_tiles) break;   // the compute warps pass the end marker on
             }
             if (epoch != kEpochMask) claims_done(hdr, a.ws_bytes, epoch);
         }
@@ -249,8 +305,8 @@ rle_kernel(RbkArgs a, long long num_tiles) {
             __syncwarp();
             P excl = 0;
             if (tile != 0) {
-                excl = look_back<P, 2, kLookbackK, OpRle>(desc, tile, epoch, a.max_polls, &hdr->status,
-                                                          PS_TRACE_LOOKBACK(tile));
+                excl = look_back<P, 2, PS_RLE_LOOKBACK_K, OpRle>(desc, tile, epoch, a.max_polls, &hdr->status,
+                                                                 PS_TRACE_LOOKBACK(tile));
                 if (lane == 0) Desc<P, 2>::store(desc, tile, kFlagP, OpRle::combine(excl, agg), epoch);
             }
             if (lane == 0) {
@@ -268,122 +324,167 @@ rle_kernel(RbkArgs a, long long num_tiles) {
             }
         }
     } else if (warp > kLCW + kLLB) {
-        // ---------------- aggregators: the tile's pair, published at once ----------------
-        // kLAgg warps, each over an equal part of the tile; the last to
-        // finish combines the parts and publishes the pair.
-        const int g = warp - (kLCW + 1 + kLLB);
-        int ends = 0;   // end markers passed on: one per look-back warp
-        for (long long k = 0;; ++k) {
-            const int s = (int)(k % S);
-            if (!rle_wait(&full[s], (uint32_t)((k / S) & 1))) {
+        // ---------------- writer warps: a tile's runs, once its pair is known ----------------
+        for (long long k = warp - (kLCW + 1 + kLLB);; k += kLW) {
+            const int slot = (int)(k % R);
+            const uint32_t par = (uint32_t)((k / R) & 1);
+            if (!rle_wait(&packed[slot], par)) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
-            const int slot = (int)(k % R);
             const long long tile = tile_of[slot];
-            if (tile < 0 || tile >= num_tiles) {   // end marker: pass it on to a look-back warp
-                if (g == 0 && lane == 0) mbar_arrive(&agg_done[slot]);
-                if (++ends == kLLB) break;
-                continue;
+            if (tile < 0 || tile >= num_tiles) break;
+            if (!rle_wait(&prefix_ready[slot], par)) {
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                break;
             }
-            if (g == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_DATA);
+            const int o = (int)(k % NOB);
             const unsigned long long base = (unsigned long long)tile * TILE;
-            uint32_t heads = 0;
-            uint32_t last = 0;   // position of the part's last head (0: none)
-            if (a.use_bulk && base + TILE <= n) {
-                // lane l takes the C consecutive vectors of its chunk, so
-                // the key before a vector is the last key of the one it read
-                // before (a register); it visits them from vector r = l mod 8
-                // on and wraps round, so that the 8 lanes one 16-byte load
-                // serves hit distinct bank groups.  Only two keys come from
-                // elsewhere: the one before the chunk (the halo for the
-                // tile's first chunk; tile 0 starts with a value that differs
-                // from element 0) and the one before vector r, which comes
-                // round last.
-                constexpr int PV = NV / kLAgg;   // vectors per part
-                constexpr int C = PV / 32;
-                static_assert(PV % 32 == 0 && C >= 8 && (C & (C - 1)) == 0, "chunk of a power-of-two size >= 8");
-                const KU *ks = stage_keys(s);
-                const int v_chunk = g * PV + lane * C;   // the chunk's first vector
-                const V *kv = reinterpret_cast<const V *>(ks) + v_chunk;
-                const int r0 = lane & 7;
-                const int e_chunk = v_chunk * VK;   // tile index of the chunk's first key
-                const KU before_chunk = (tile == 0 && e_chunk == 0) ? (KU)~ks[0] : ks[e_chunk - 1];
-                KU carry = r0 == 0 ? before_chunk : ks[e_chunk + r0 * VK - 1];
-                int last_vec = -1;   // highest vector of the chunk that holds a head
-#pragma unroll 8
-                for (int q = 0; q < C; ++q) {
-                    const int vi = (q + r0) & (C - 1);
-                    const V x = kv[vi];
-                    const KU prev = vi == 0 ? before_chunk : carry;
-                    carry = KV::key(x, VK - 1);
-                    uint32_t h = 0;
-#pragma unroll
-                    for (int j = 0; j < VK; ++j) h += (uint32_t)(KV::key(x, j) != (j ? KV::key(x, j - 1) : prev));
-                    heads += h;
-                    last_vec = (h && vi > last_vec) ? vi : last_vec;
+            const bool sparse = sparse_of[slot] != 0;
+            if (sparse && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
+            const P excl = excl_of[slot];
+            const uint32_t c0 = (uint32_t)(excl >> 32), p0 = (uint32_t)excl;
+            const uint32_t tbase = (uint32_t)base;
+            if (sparse) {
+                // the runs in order: keys to unique_keys[c0 + t], and the
+                // length of the run each head closes to counts[c0 + t - 1]
+                const uint32_t h = (uint32_t)(agg_of[slot] >> 32);
+                const KU *ok = out_keys(o);
+                const uint16_t *op = out_pos(o);
+                for (uint32_t t = lane; t < h; t += 32) {
+                    const uint32_t pos = tbase + op[rle_sw(t)];
+                    const uint32_t pv = t ? tbase + op[rle_sw(t - 1u)] : p0;
+                    ukeys[c0 + t] = ok[rle_sw(t)];
+                    if (c0 + t > 0u) counts[c0 + t - 1u] = pos - pv;
                 }
-                // the part's last head: in the highest lane that has one, in
-                // that lane's highest vector with one (same in every lane)
-                const int lv_lane = __reduce_max_sync(kFull, last_vec >= 0 ? lane : -1);
-                if (lv_lane >= 0) {
-                    const int lv = g * PV + lv_lane * C + __shfl_sync(kFull, last_vec, lv_lane);
-                    const V x = reinterpret_cast<const V *>(ks)[lv];
-                    const KU prev = lv > 0 ? ks[lv * VK - 1] : tile == 0 ? (KU)~KV::key(x, 0) : ks[-1];
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int j = 0; j < VK; ++j) m |= (uint32_t)(KV::key(x, j) != (j ? KV::key(x, j - 1) : prev)) << j;
-                    last = (uint32_t)(base + (unsigned long long)(lv * VK + 31 - __clz(m)));
-                }
-            } else {
-                constexpr long long PART = TILE / kLAgg;
-                const unsigned long long lo = base + (unsigned long long)(g * PART);
-                const unsigned long long hi = base + (unsigned long long)((g + 1) * PART);
-                const unsigned long long end = hi < n ? hi : n;
-                long long le = -1;
-                for (unsigned long long i = lo + lane; i < end; i += 32)
-                    if (i == 0 || keys[i] != keys[i - 1]) { ++heads; le = (long long)(i - base); }
-                const int lmax = __reduce_max_sync(kFull, (int)le);
-                last = lmax >= 0 ? (uint32_t)(base + (unsigned long long)lmax) : 0u;
-            }
+            }   // a dense tile: the compute warps write it
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            heads = __reduce_add_sync(kFull, heads);
             if (lane == 0) {
-                // parts later in the tile have larger positions, so the
-                // parts combine in any order
-                volatile P *part = s_part[slot];
-                part[g] = ((P)heads << 32) | last;
-                __threadfence_block();
-                if (atomicAdd(&s_parts_done[slot], 1) == kLAgg - 1) {
-                    __threadfence_block();
-                    P agg = 0;
-#pragma unroll
-                    for (int gg = 0; gg < kLAgg; ++gg) agg = OpRle::combine(agg, (P)part[gg]);
-                    s_parts_done[slot] = 0;   // the slot's next use is kLRing iterations on
-                    Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
-                    PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
-                    agg_of[slot] = agg;
-                    mbar_arrive(&agg_done[slot]);
-                }
+                if (sparse) PS_TRACE_POINT(tile, PS_TRACE_STORED);
+                mbar_arrive(&ob_empty[o]);
             }
         }
     } else {
-        // ---------------- compute warps: find the heads, write the runs ----------------
+        // ---------------- compute warps: find the heads, pack the runs ----------------
+        const int seg = warp * 32 * ITEMS;   // the warp's first key in a tile
+        // A dense tile waiting for the next iteration's pass: its stage, slot
+        // and the slot's phase parity (pend_at: stage | slot << 8 | parity <<
+        // 16), its tile (n < 2^32, so tile ids fit 32 bits), the pair of its
+        // keys before this warp's, and per row the lane's head mask (bits
+        // 0-7) and heads before it in the warp.
+        bool pend = false;
+        uint32_t pend_at = 0, pend_tile = 0;
+        P pend_wex = 0;
+        uint32_t pend_info[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) pend_info[r] = 0;
+        // Writes the pending dense tile once its pair is known: per row the
+        // row's runs -- run indices [cw + first, cw + first + nh) -- packed in
+        // this warp's slice of the stage, then keys and lengths written with
+        // consecutive lanes on consecutive runs; the stage goes back after.
+        auto write_dense = [&]() {
+            const int ps = (int)(pend_at & 0xffu), pslot = (int)((pend_at >> 8) & 0xffu);
+            const unsigned long long pbase = (unsigned long long)pend_tile * TILE;
+            const bool pstaged = a.use_bulk && pbase + TILE <= n;
+            if (!rle_wait(&prefix_ready[pslot], pend_at >> 16))
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(pend_tile, PS_TRACE_PREFIX_RECEIVED);
+            const P pre = OpRle::combine(excl_of[pslot], pend_wex);
+            const uint32_t cw = (uint32_t)(pre >> 32);
+            const uint32_t wbase = (uint32_t)(pbase + (unsigned long long)seg);
+            // the warp's keys again, all of them before the slice is reused
+            KU kp[ROWS][EPL];
+            if (pstaged) {
+                const V *kv = reinterpret_cast<const V *>(stage_keys(ps));
+                const int rot = (lane >> 2) & 1;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const int e0 = seg + (r * 32 + lane) * EPL;
+                    const V x0 = kv[e0 / VK + rot], x1 = kv[e0 / VK + (rot ^ 1)];
+                    const V lo = rot ? x1 : x0, hi = rot ? x0 : x1;
+#pragma unroll
+                    for (int j = 0; j < VK; ++j) {
+                        kp[r][j] = KV::key(lo, j);
+                        kp[r][VK + j] = KV::key(hi, j);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                    for (int j = 0; j < EPL; ++j) {
+                        const unsigned long long i = pbase + seg + (unsigned long long)((r * 32 + lane) * EPL + j);
+                        kp[r][j] = i < n ? keys[i] : KU(0);
+                    }
+            }
+            __syncwarp();
+            KU *pk = stage_keys(ps) + seg;                                 // 32 * EPL keys
+            uint32_t *pp = reinterpret_cast<uint32_t *>(pk + 32 * EPL);   // 32 * EPL offsets
+            uint32_t row_prev = (uint32_t)pre;   // position of the last head before the row
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const uint32_t mr = pend_info[r] & 0xffu, rb = pend_info[r] >> 8;
+                const uint32_t first = __shfl_sync(kFull, rb, 0);
+                const uint32_t nh = __shfl_sync(kFull, rb + (uint32_t)__popc(mr), 31) - first;
+                uint32_t q = rb - first;
+                for (uint32_t mm = mr; mm; mm &= mm - 1u) {
+                    const int j = __ffs(mm) - 1;
+                    pk[rle_sw(q)] = pick<KU, EPL>(kp[r], j);
+                    pp[rle_sw(q)] = (uint32_t)((r * 32 + lane) * EPL + j);
+                    ++q;
+                }
+                __syncwarp();
+                const uint32_t c0 = cw + first;
+                for (uint32_t t = lane; t < nh; t += 32) {
+                    const uint32_t pos = wbase + pp[rle_sw(t)];
+                    const uint32_t pv = t ? wbase + pp[rle_sw(t - 1u)] : row_prev;
+                    ukeys[c0 + t] = pk[rle_sw(t)];
+                    if (c0 + t > 0u) counts[c0 + t - 1u] = pos - pv;
+                }
+                if (nh) row_prev = wbase + pp[rle_sw(nh - 1u)];
+                __syncwarp();
+            }
+            // the stage goes back once every warp has written from its slice
+            named_barrier(2, CT);
+            if (warp == 0 && lane == 0) {
+                PS_TRACE_POINT(pend_tile, PS_TRACE_STORED);
+                mbar_arrive(&empty[ps]);
+            }
+            pend = false;
+        };
         for (long long k = 0;; ++k) {
             const int s = (int)(k % S);
+            const int slot = (int)(k % R);
             if (!rle_wait(&full[s], (uint32_t)((k / S) & 1))) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 abort_meet(&s_abort, 1, CT);
                 break;
             }
-            const int slot = (int)(k % R);
             const long long tile = tile_of[slot];
-            if (tile < 0 || tile >= num_tiles) break;
+            if (tile < 0 || tile >= num_tiles) {
+                if (pend) write_dense();
+                // end marker: pass it on to every look-back and writer warp,
+                // on the slots of the next iterations (the producer, which
+                // stopped here, writes none of them again)
+                if (warp == 0 && lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < kLEnds; ++i) {
+                        if (i > 0) tile_of[(k + i) % R] = num_tiles;
+                        if (i < kLLB) mbar_arrive(&agg_done[(k + i) % R]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+#pragma unroll
+                    for (int i = 0; i < kLW; ++i) mbar_arrive(&packed[(k + i) % R]);
+                break;
+            }
             const unsigned long long base = (unsigned long long)tile * TILE;
             const bool staged = a.use_bulk && base + TILE <= n;
-            const int seg = warp * 32 * ITEMS;   // the warp's first key in the tile
-            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
+            if (warp == 0 && lane == 0) {
+                PS_TRACE_POINT(tile, PS_TRACE_DATA);
+                PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
+            }
 
             // Rows of two 16-byte vectors per lane (EPL keys); lanes 4-7 of
             // each quarter-warp read their pair in swapped order, so that
@@ -427,121 +528,88 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                     m[r] = mm;
                 }
             }
-            // The keys are in registers.  A sparse warp does not touch the
-            // stage again and hands it back before the tile's pair arrives
-            // (the hand-off ring keeps the slots apart); a dense one packs
-            // its runs in its slice of the stage -- free once the pair has
-            // arrived, since the aggregator finished reading the stage before
-            // the look-back began -- and hands it back after writing them.
-            uint32_t wh = 0;
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) wh += (uint32_t)__popc(m[r]);
-            const bool dense = __reduce_add_sync(kFull, wh) > (uint32_t)PS_RLE_DENSE_HEADS;
-            __syncwarp();
-            if (!dense && lane == 0) mbar_arrive(&empty[s]);
 
-            // Per row: heads before each lane's chunk (warp scan of the
-            // chunk counts), and the position of the last head before it --
-            // in the nearest lower lane that has one (ballot + one shuffle),
-            // else in an earlier row of this warp.  Both are below the warp's
-            // 32 * ITEMS keys, so a row's mask, count and previous head share
-            // one word (registers are at the cap that two CTAs per SM allow):
-            //   bits 0-7 mask, 8-18 heads before, 19-29 previous head (offset
-            //   from the warp's first key), bit 30 set if that head exists.
-            static_assert(32 * ITEMS <= 2048 && EPL <= 8, "row words hold 8 mask bits and two 11-bit fields");
-            const uint32_t lt_mask = (1u << lane) - 1u;
-            const uint32_t wbase = (uint32_t)(base + (unsigned long long)seg);   // position of the warp's first key
-            uint32_t info[ROWS];
-            uint32_t run_c = 0, run_p = 0, run_has = 0;   // heads so far in this warp, the last one
+            // Per row: heads before each lane's chunk within the warp (warp
+            // scan of the chunk counts); the warp's heads and its last one.
+            uint32_t before[ROWS];
+            uint32_t run_c = 0;
+            int run_last = -1;   // the warp's last head, from the warp's first key
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
                 const uint32_t t = (uint32_t)__popc(m[r]);
                 const uint32_t sc = warp_inclusive<uint32_t>(t, lane);
-                const uint32_t before = run_c + (sc - t);
+                before[r] = run_c + (sc - t);
                 run_c += __shfl_sync(kFull, sc, 31);
-                const uint32_t lp = m[r] ? (uint32_t)((r * 32 + lane) * EPL + 31 - __clz(m[r])) : 0u;
-                const uint32_t hb = __ballot_sync(kFull, m[r] != 0u);
-                const uint32_t below = hb & lt_mask;
-                const uint32_t from = __shfl_sync(kFull, lp, below ? 31 - __clz(below) : 0);
-                const uint32_t pp = below ? from : run_p;
-                const uint32_t has = below ? 1u : run_has;
-                info[r] = m[r] | (before << 8) | (pp << 19) | (has << 30);
-                const uint32_t row_last = __shfl_sync(kFull, lp, hb ? 31 - __clz(hb) : 0);
-                run_p = hb ? row_last : run_p;
-                run_has = hb ? 1u : run_has;
+                const int lp = m[r] ? (r * 32 + lane) * EPL + 31 - __clz(m[r]) : -1;
+                const int row_last = __reduce_max_sync(kFull, lp);
+                run_last = row_last > run_last ? row_last : run_last;
             }
-            run_p = run_has ? wbase + run_p : 0u;   // as a position, 0 for none
             P *sw = s_warp[k & 1];
-            if (lane == 0) sw[warp] = ((P)run_c << 32) | run_p;
-            named_barrier(1, CT);
+            if (lane == 0)
+                sw[warp] = ((P)run_c << 32) |
+                           (run_last >= 0 ? (uint32_t)(base + (unsigned long long)(seg + run_last)) : 0u);
+            named_barrier(1, CT);   // every warp has read the stage and posted its pair
             if (aborted(&s_abort)) break;
-            P warp_excl = 0;
+            P wex = 0;   // the pair of the tile's keys before this warp's
+            P agg = 0;
 #pragma unroll
-            for (int w = 0; w < kLCW; ++w)
-                if (w < warp) warp_excl = OpRle::combine(warp_excl, sw[w]);
-            if (!rle_wait(&prefix_ready[slot], (uint32_t)((k / R) & 1)))
-                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
-            const P pre = OpRle::combine(excl_of[slot], warp_excl);
-            const uint32_t cw = (uint32_t)(pre >> 32), pw = (uint32_t)pre;
-            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
-
-            if (!dense) {
-                // each head: its key to unique_keys[c], and the length of run
-                // c - 1 (which it closes) to counts[c - 1]; only the set bits
-                // of the mask are visited
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    const uint32_t w = info[r];
-                    const uint32_t pos0 = wbase + (uint32_t)((r * 32 + lane) * EPL);
-                    uint32_t c = cw + ((w >> 8) & 0x7ffu);
-                    uint32_t prev = (w >> 30) ? wbase + ((w >> 19) & 0x7ffu) : pw;
-                    for (uint32_t mm = w & 0xffu; mm; mm &= mm - 1u) {
-                        const int j = __ffs(mm) - 1;
-                        const KU key = pick<KU, EPL>(kk[r], j);
-                        ukeys[c] = key;
-                        if (c > 0u) counts[c - 1u] = pos0 + (uint32_t)j - prev;
-                        prev = pos0 + (uint32_t)j;
-                        ++c;
-                    }
+            for (int w = 0; w < kLCW; ++w) {
+                const P pw = sw[w];
+                if (w < warp) wex = OpRle::combine(wex, pw);
+                agg = OpRle::combine(agg, pw);
+            }
+            const bool sparse = (agg >> 32) <= (P)CAP;
+            if (warp == 0 && lane == 0) {
+                // A at once (P for tile 0, whose exclusive pair is empty); a
+                // sparse tile's keys are all in registers, so its stage goes
+                // back now, before the pair of the tile is known
+                Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
+                PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
+                agg_of[slot] = agg;
+                sparse_of[slot] = sparse ? 1 : 0;
+                mbar_arrive(&agg_done[slot]);
+                if (sparse) mbar_arrive(&empty[s]);
+            }
+            if (sparse) {
+                // pack the runs in the iteration's output buffer, once the
+                // writer is done with its previous tile
+                const int o = (int)(k % NOB);
+                if (k >= NOB && !rle_wait(&ob_empty[o], (uint32_t)((k / NOB - 1) & 1))) {
+                    report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                    abort_meet(&s_abort, 1, CT);
+                    break;
                 }
-            } else {
-                // per row: the row's runs are the contiguous run indices
-                // [cw + first, cw + first + nh); pack each head's key and
-                // offset in order, then write keys and lengths (differences
-                // of consecutive head offsets) with consecutive lanes on
-                // consecutive entries
-                KU *pk = stage_keys(s) + seg;                                      // 32 * EPL keys
-                uint32_t *pp = reinterpret_cast<uint32_t *>(pk + 32 * EPL);        // 32 * EPL offsets
-                static_assert(32 * EPL * (sizeof(KU) + 4) <= 32 * ITEMS * sizeof(KU), "a row's runs fit the slice");
-                uint32_t row_prev = pw;   // position of the last head before the row
+                KU *ok = out_keys(o);
+                uint16_t *op = out_pos(o);
+                const uint32_t wq0 = (uint32_t)(wex >> 32);   // heads before this warp in the tile
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
-                    const uint32_t w = info[r];
-                    const uint32_t rb = (w >> 8) & 0x7ffu;
-                    const uint32_t first = __shfl_sync(kFull, rb, 0);
-                    const uint32_t nh = __shfl_sync(kFull, rb + (uint32_t)__popc(w & 0xffu), 31) - first;
-                    uint32_t q = rb - first;
-                    for (uint32_t mm = w & 0xffu; mm; mm &= mm - 1u) {
+                    const uint32_t pos0 = (uint32_t)(seg + (r * 32 + lane) * EPL);
+                    uint32_t q = wq0 + before[r];
+                    for (uint32_t mm = m[r]; mm; mm &= mm - 1u) {
                         const int j = __ffs(mm) - 1;
-                        const KU key = pick<KU, EPL>(kk[r], j);
-                        pk[rle_sw(q)] = key;
-                        pp[rle_sw(q)] = (uint32_t)((r * 32 + lane) * EPL + j);
+                        ok[rle_sw(q)] = pick<KU, EPL>(kk[r], j);
+                        op[rle_sw(q)] = (uint16_t)(pos0 + (uint32_t)j);
                         ++q;
                     }
-                    __syncwarp();
-                    const uint32_t c0 = cw + first;
-                    for (uint32_t t = lane; t < nh; t += 32) {
-                        const uint32_t pos = wbase + pp[rle_sw(t)];
-                        const uint32_t pv = t ? wbase + pp[rle_sw(t - 1u)] : row_prev;
-                        ukeys[c0 + t] = pk[rle_sw(t)];
-                        if (c0 + t > 0u) counts[c0 + t - 1u] = pos - pv;
-                    }
-                    if (nh) row_prev = wbase + pp[rle_sw(nh - 1u)];
-                    __syncwarp();
                 }
-                if (lane == 0) mbar_arrive(&empty[s]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&packed[slot]);
+            } else {
+                // a dense tile: nothing for the writer (it only frees the
+                // buffer); the compute warps write it after the next tile's
+                // pass, and hand its stage back then
+                if (lane == 0) mbar_arrive(&packed[slot]);
             }
-            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_STORED);
+            if (pend) write_dense();   // the previous dense tile, now that this tile's pair is out
+            if (!sparse) {
+                pend = true;
+                pend_at = (uint32_t)s | ((uint32_t)slot << 8) | ((uint32_t)((k / R) & 1) << 16);
+                pend_tile = (uint32_t)tile;
+                pend_wex = wex;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) pend_info[r] = m[r] | (before[r] << 8);
+            }
         }
         if (warp == 0 && lane == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_DONE);
     }
