@@ -188,15 +188,6 @@ __device__ __forceinline__ void prefetch_descriptor(const void *desc, long long 
                               tile * (DW == 1 ? kDescStride32 : kDescStride64));
 }
 
-// At the start of a call thread 0 of each CTA of the select, reduce-by-key
-// and run-length kernels prefetches into L2 the tiles the first round of
-// claims will take (CTA b: tiles b, b + grid, ... one per stage), so that
-// their reads from memory overlap the header read and the first tile-id
-// atomics, as the scan kernel does; 0 turns it off.
-#ifndef PS_PREFETCH_FIRST_TILES
-#define PS_PREFETCH_FIRST_TILES 1
-#endif
-
 // A device-side error of call `epoch` (ps_get_device_status reads it).
 __device__ __forceinline__ void report_error(unsigned long long *status, uint32_t epoch,
                                              ps_status code) {

@@ -19,15 +19,25 @@
 // The pair travels as one 64-bit word, count << 32 | value bits, and a tile
 // descriptor is the two-word form the int64 scan uses.
 //
-// Structure as in the persistent scan and the compaction kernels: a producer
-// warp takes tile ids and bulk-copies the tile's keys -- starting one
-// 16-byte vector early, so the key before the tile (the "halo") is in shared
-// memory too -- and values into a 3-stage ring; an aggregator warp computes
-// the tile's pair and publishes it at once; a look-back warp resolves the
-// tile's exclusive pair; eight compute warps scan the tile and scatter.  The
-// aggregator needs no ordered reduction: the count is a plain sum, and the
-// value is the sum of the values from the tile's last head on (all of them
-// when it has none), found with a maximum.
+// Roles (as in scan_rle.cu).  A producer warp takes tile ids and bulk-copies
+// each tile's keys -- starting one 16-byte vector early, so the key before
+// the tile (the "halo") is in shared memory too -- and values into a ring
+// of stages.  Eight compute warps take the tiles in order and never wait
+// for a tile's prefix: they scan the tile's pairs (a segmented shuffle scan
+// of all rows side by side), combine the warps' pairs into the tile's pair
+// and publish it (A; P for tile 0) themselves, and pack the tile's runs in
+// order into an output buffer -- each head's key and the value of the run it
+// closes, summed within the tile -- after which the stage goes back to the
+// producer.  Only the run closed by the tile's first head reaches back
+// before the tile; its packed value lacks the value the tile's exclusive
+// pair carries.  Look-back warps resolve that pair; a writer warp adds its
+// value to the first run and writes the buffer out as contiguous ranges,
+// then frees the buffer.  A tile with more runs than a buffer holds (a
+// dense tile) is written by the compute warps themselves, one iteration
+// late: they publish its pair, keep its stage, do the next tile's pass (so
+// that tile's pair is out too), then wait for the dense tile's prefix,
+// re-read its keys and values and pack and write each warp's runs from its
+// slice of the stage.
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
 #include "scan_trace.cuh"
@@ -37,21 +47,39 @@ namespace ps {
 namespace {
 
 constexpr int kRCW = kThreads / 32;   // compute warps per CTA
-constexpr int kRStages = 3;
-// Aggregator warps per CTA (a macro so that a tuning sweep can rebuild).
-#ifndef PS_RBK_AGG_WARPS
-#define PS_RBK_AGG_WARPS 4
+// Stages, output buffers and their bytes, look-back and writer warps (macros
+// so that a tuning sweep can rebuild).
+#ifndef PS_RBK_STAGES
+#define PS_RBK_STAGES 3
 #endif
-constexpr int kAgg = PS_RBK_AGG_WARPS;
-// Look-back warps per CTA: each resolves every kLB-th tile of the CTA, so
-// that one CTA has several look-backs in flight (a single look-back warp
-// caps a CTA at one tile per look-back latency).
+#ifndef PS_RBK_OUT_BUFFERS
+#define PS_RBK_OUT_BUFFERS 4
+#endif
+#ifndef PS_RBK_OUT_BYTES
+#define PS_RBK_OUT_BYTES 4096
+#endif
 #ifndef PS_RBK_LOOKBACK_WARPS
-#define PS_RBK_LOOKBACK_WARPS 1
+#define PS_RBK_LOOKBACK_WARPS 2
 #endif
+#ifndef PS_RBK_WRITER_WARPS
+#define PS_RBK_WRITER_WARPS 1
+#endif
+constexpr int kRStages = PS_RBK_STAGES;
+constexpr int kROut = PS_RBK_OUT_BUFFERS;
+constexpr int kROutBytes = PS_RBK_OUT_BYTES;
 constexpr int kLB = PS_RBK_LOOKBACK_WARPS;
-static_assert(kLB >= 1 && kLB <= kRStages, "at most one look-back warp per stage");
-constexpr int kRbkThreads = (kRCW + 1 + kLB + kAgg) * 32;   // compute, producer, look-back, aggregators
+constexpr int kRW = PS_RBK_WRITER_WARPS;
+constexpr int rmax(int a, int b) { return a > b ? a : b; }
+// Iterations past the end the compute warps mark (every look-back and
+// writer warp waits on its next iteration), and the hand-off slots: a slot
+// is reused only after every role is done with it -- the writer is at most
+// kROut iterations behind the compute warps, the producer at most
+// kRStages + 1 ahead of their pass.
+constexpr int kREnds = rmax(kLB, kRW);
+constexpr int rbk_ring_slots() { return (rmax(kRStages + kROut + 1, kREnds + kROut) + 1) / 2 * 2; }
+constexpr int kRRing = rbk_ring_slots();
+constexpr int kRbkThreads = (kRCW + 1 + kLB + kRW) * 32;   // compute, producer, look-back, writer
+static_assert(kRStages >= 2, "a dense tile keeps its stage while the next one is scanned");
 // Every barrier wait suspends the warp in the barrier for up to this many
 // nanoseconds per try (0: poll), so that waiting warps leave the issue slots
 // to the ones that work; a macro so that a tuning sweep can rebuild.
@@ -135,8 +163,12 @@ template <typename KU> constexpr uint32_t rbk_key_bytes() {   // the tile's keys
 template <typename KU> constexpr uint32_t rbk_stage_bytes() {
     return rbk_key_bytes<KU>() + (uint32_t)(rbk_tile<KU>() * 4);
 }
+// Runs an output buffer holds: a key and a 32-bit value each, a multiple of
+// 32 entries (the swizzle stays within each 32).
+template <typename KU> constexpr int rbk_out_cap() { return (int)((kROutBytes / (sizeof(KU) + 4)) / 32 * 32); }
 template <typename KU> constexpr size_t rbk_smem_bytes() {
-    return (size_t)kRStages * rbk_stage_bytes<KU>() + ((size_t)kRStages * (4 * 8 + 8 * 3) + 8 + 127) / 128 * 128;
+    return (size_t)kRStages * rbk_stage_bytes<KU>() + (size_t)kROut * kROutBytes +
+           ((size_t)kRStages * 2 * 8 + (size_t)kROut * 8 + (size_t)kRRing * (3 * 8 + 4 * 8) + 127) / 128 * 128;
 }
 
 }  // namespace
@@ -147,7 +179,6 @@ __global__ void __launch_bounds__(kRbkThreads, kPCtasPerSm)
 reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     using KV = KeyVec<KU>;
     using V = typename KV::V;
-    using W = typename KV::W;
     using Op = OpSeg<VU>;
     using P = unsigned long long;
     constexpr int VK = KV::N;
@@ -159,29 +190,38 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     constexpr int EPL = 2 * VK;
     constexpr int ROWS = ITEMS / EPL;
     constexpr int WV = EPL / 4;   // 16-byte value vectors per lane per row
-    constexpr int S = kRStages;
+    constexpr int S = kRStages, R = kRRing, NOB = kROut;
     constexpr uint32_t KEY_BYTES = rbk_key_bytes<KU>();
     constexpr uint32_t STAGE = rbk_stage_bytes<KU>();
     constexpr uint32_t VAL_BYTES = (uint32_t)(TILE * 4);
     constexpr int CT = kRCW * 32;
+    constexpr int CAP = rbk_out_cap<KU>();
     static_assert(ITEMS % EPL == 0 && (WV == 1 || WV == 2) && STAGE % 16 == 0, "tile geometry");
+    static_assert(CAP >= 32 && 32 * ITEMS < (1 << 23), "output buffer geometry, packed row words");
 
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * STAGE);
+    unsigned char *outbuf = smem + (size_t)S * STAGE;
+    uint64_t *full = reinterpret_cast<uint64_t *>(outbuf + (size_t)NOB * kROutBytes);
     uint64_t *empty = full + S;
-    uint64_t *agg_done = empty + S;
-    uint64_t *prefix_ready = agg_done + S;
-    uint64_t *agg_bar = prefix_ready + S;   // the aggregator warps meet here (bounded waits)
-    long long *tile_of = reinterpret_cast<long long *>(agg_bar + 1);
-    P *agg_of = reinterpret_cast<P *>(tile_of + S);
-    P *excl_of = agg_of + S;
+    uint64_t *ob_empty = empty + S;
+    uint64_t *agg_done = ob_empty + NOB;   // the rest: R slots, slot k % R
+    uint64_t *prefix_ready = agg_done + R;
+    uint64_t *packed = prefix_ready + R;
+    long long *tile_of = reinterpret_cast<long long *>(packed + R);
+    P *agg_of = reinterpret_cast<P *>(tile_of + R);
+    P *excl_of = agg_of + R;
+    int *sparse_of = reinterpret_cast<int *>(excl_of + R);
     __shared__ P s_warp[2][kRCW];
     __shared__ int s_abort;   // a compute warp's wait ran out: all of them leave
-    __shared__ uint32_t s_ah[2][kAgg], s_av[2][kAgg];   // aggregator shares: heads, values
-    __shared__ int s_al[2][kAgg];                       // and last head
     // stage s: [halo vector][TILE keys][TILE values]
     auto stage_keys = [&](int s) { return reinterpret_cast<KU *>(smem + (size_t)s * STAGE) + VK; };
     auto stage_vals = [&](int s) { return reinterpret_cast<uint32_t *>(smem + (size_t)s * STAGE + KEY_BYTES); };
+    // output buffer o: a sparse tile's runs, CAP keys then CAP values, entry
+    // q at rbk_sw(q)
+    auto out_keys = [&](int o) { return reinterpret_cast<KU *>(outbuf + (size_t)o * kROutBytes); };
+    auto out_vals = [&](int o) {
+        return reinterpret_cast<uint32_t *>(outbuf + (size_t)o * kROutBytes + (size_t)CAP * sizeof(KU));
+    };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     Header *hdr = reinterpret_cast<Header *>(a.ws);
@@ -197,27 +237,21 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     __shared__ int s_ok;
     if (tid == 0) {
         PS_TRACE_CTA_POINT(PS_TRACE_CTA_ENTRY);
-        if (PS_PREFETCH_FIRST_TILES && a.use_bulk) {
-            for (int j = 0; j < S; ++j) {
-                const unsigned long long t = blockIdx.x + (unsigned long long)j * gridDim.x;
-                if ((t + 1) * (unsigned long long)TILE <= n) {
-                    prefetch_l2(keys + t * TILE, (uint32_t)(TILE * sizeof(KU)));   // the tile, no halo
-                    prefetch_l2(vals + t * TILE, VAL_BYTES);
-                }
-            }
-        }
         uint32_t e;
         s_ok = begin_call(hdr, &e) ? 1 : 0;
         s_epoch = e;
         s_abort = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kRCW + kAgg);
-            mbar_init(&agg_done[s], 1);
-            mbar_init(&prefix_ready[s], 1);
-            tile_of[s] = num_tiles;
+            mbar_init(&empty[s], 1);   // the compute warps, once the tile needs the stage no more
         }
-        mbar_init(agg_bar, kAgg);
+        for (int o = 0; o < NOB; ++o) mbar_init(&ob_empty[o], 1);   // the writer
+        for (int slot = 0; slot < R; ++slot) {
+            mbar_init(&agg_done[slot], 1);
+            mbar_init(&prefix_ready[slot], 1);
+            mbar_init(&packed[slot], kRCW);
+            tile_of[slot] = num_tiles;   // end marker until the producer fills it
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -228,15 +262,14 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     if (warp == kRCW) {
         // ---------------- producer ----------------
         if (lane == 0) {
-            int ends = 0;   // end markers sent: one per look-back warp
             for (long long k = 0;; ++k) {
                 const int s = (int)(k % S);
                 if (k >= S && !role_wait(&empty[s], (uint32_t)((k / S - 1) & 1))) {
                     report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                     break;
                 }
-                const long long t = ends ? num_tiles : (long long)atomicAdd(&hdr->tile_counter, 1ull);
-                tile_of[s] = t;
+                const long long t = (long long)atomicAdd(&hdr->tile_counter, 1ull);
+                tile_of[k % R] = t;
                 if (t < num_tiles) {
                     prefetch_descriptor<2>(desc, t);
                     PS_TRACE_POINT(t, PS_TRACE_CLAIM);
@@ -253,21 +286,21 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 } else {
                     mbar_arrive(&full[s]);   // end marker, or a tile read from global
                 }
-                if (t >= num_tiles && ++ends == kLB) break;
+                if (t >= num_tiles) break;   // the compute warps pass the end marker on
             }
             if (epoch != kEpochMask) claims_done(hdr, a.ws_bytes, epoch);
         }
     } else if (warp > kRCW && warp <= kRCW + kLB) {
         // ---------------- look-back warps: the tile's exclusive pair ----------------
         for (long long k = warp - (kRCW + 1);; k += kLB) {
-            const int s = (int)(k % S);
-            if (!role_wait(&agg_done[s], (uint32_t)((k / S) & 1))) {
+            const int slot = (int)(k % R);
+            if (!role_wait(&agg_done[slot], (uint32_t)((k / R) & 1))) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
-            const long long tile = tile_of[s];
+            const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) break;
-            const P agg = agg_of[s];
+            const P agg = agg_of[slot];
             if (lane == 0) PS_TRACE_POINT(tile, PS_TRACE_LOOKBACK_START);
             __syncwarp();
             P excl = 0;
@@ -284,155 +317,68 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                     if (runs > 0) aggs[runs - 1] = pair_value(incl);
                     if (a.num_runs) *a.num_runs = runs;
                 }
-                excl_of[s] = excl;
+                excl_of[slot] = excl;
                 PS_TRACE_POINT(tile, PS_TRACE_PREFIX);
-                mbar_arrive(&prefix_ready[s]);
+                mbar_arrive(&prefix_ready[slot]);
             }
         }
     } else if (warp > kRCW + kLB) {
-        // ---------------- aggregators: the tile's pair, published at once ----------------
-        // kAgg warps, each over its share of the tile: count the heads and
-        // find the last one, combine through shared memory, then sum the
-        // values from the tile's last head on, again in shares.
-        const int ag = warp - (kRCW + 1 + kLB);
-        int ends = 0;   // end markers passed on: one per look-back warp
-        constexpr int PART = (int)(TILE / VK / kAgg);   // vectors per aggregator warp
-        static_assert(PART % 32 == 0, "aggregator shares must be whole warp rows");
-        uint32_t meets = 0;   // completed phases of agg_bar
-        auto meet = [&]() {   // all aggregator warps here; false if the wait ran out
-            __syncwarp();
-            if (lane == 0) mbar_arrive(agg_bar);
-            const bool ok = role_wait(agg_bar, meets & 1u);
-            ++meets;
-            if (!ok) report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
-            return ok;
-        };
-        for (long long k = 0;; ++k) {
-            const int s = (int)(k % S);
-            if (!role_wait(&full[s], (uint32_t)((k / S) & 1))) {
+        // ---------------- writer warps: a tile's runs, once its pair is known ----------------
+        for (long long k = warp - (kRCW + 1 + kLB);; k += kRW) {
+            const int slot = (int)(k % R);
+            const uint32_t par = (uint32_t)((k / R) & 1);
+            if (!role_wait(&packed[slot], par)) {
                 report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
                 break;
             }
-            const long long tile = tile_of[s];
-            if (tile < 0 || tile >= num_tiles) {
-                if (ag == 0 && lane == 0) mbar_arrive(&agg_done[s]);
-                if (++ends == kLB) break;
-                continue;
+            const long long tile = tile_of[slot];
+            if (tile < 0 || tile >= num_tiles) break;
+            if (!role_wait(&prefix_ready[slot], par)) {
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                break;
             }
-            if (ag == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_DATA);
-            const unsigned long long base = (unsigned long long)tile * TILE;
-            const bool staged = a.use_bulk && base + TILE <= n;
-            const int len = staged ? (int)TILE : (int)(n - base < (unsigned long long)TILE ? n - base : TILE);
-            const KU *ks = stage_keys(s);
-            uint32_t heads = 0;
-            int last = -1;   // tile-local index of the last head in this warp's share
-            if (staged) {
-                const V *kv = reinterpret_cast<const V *>(ks);
-                // the key before the share: the halo (or, for tile 0, a value
-                // that differs from element 0, which opens a run), or the
-                // previous share's last key
-                const KU before = ag > 0 ? ks[ag * PART * VK - 1] : tile == 0 ? (KU)~ks[0] : ks[-1];
-                int last_vec = -1;
-#pragma unroll 4
-                for (int it = 0; it < PART / 32; ++it) {
-                    const int vi = ag * PART + it * 32 + lane;
-                    const V x = kv[vi];
-                    KU prev = __shfl_up_sync(kFull, KV::key(x, VK - 1), 1);
-                    if (lane == 0) prev = it == 0 ? before : ks[vi * VK - 1];
-                    uint32_t h = 0;
-#pragma unroll
-                    for (int j = 0; j < VK; ++j) h += (uint32_t)(KV::key(x, j) != (j ? KV::key(x, j - 1) : prev));
-                    heads += h;
-                    last_vec = h ? vi : last_vec;
+            const int o = (int)(k % NOB);
+            const bool sparse = sparse_of[slot] != 0;
+            if (sparse) {
+                // the runs in order: keys to unique_keys[c0 + t], and the value
+                // of the run each head closes to aggregates[c0 + t - 1]; the
+                // first of them began before the tile, so the exclusive pair's
+                // value (that run's sum so far) is added to its packed part
+                if (lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
+                const P excl = excl_of[slot];
+                const uint32_t c0 = pair_count(excl), pv = pair_value(excl);
+                const uint32_t h = pair_count(agg_of[slot]);
+                const KU *ok = out_keys(o);
+                const uint32_t *ov = out_vals(o);
+                for (uint32_t t = lane; t < h; t += 32) {
+                    ukeys[c0 + t] = ok[rbk_sw(t)];
+                    if (c0 + t > 0u) aggs[c0 + t - 1u] = t ? ov[rbk_sw(t)] : RunValue<VU>::add(pv, ov[rbk_sw(t)]);
                 }
-                const int lv = __reduce_max_sync(kFull, last_vec);
-                if (lv >= 0) {   // the last head within that vector (same in every lane)
-                    const V x = kv[lv];
-                    const KU prev = lv == ag * PART ? before : ks[lv * VK - 1];
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int j = 0; j < VK; ++j) m |= (uint32_t)(KV::key(x, j) != (j ? KV::key(x, j - 1) : prev)) << j;
-                    last = lv * VK + 31 - __clz(m);
-                }
-            } else if (ag == 0) {   // a tile read from global memory: the first warp alone
-                for (int e = lane; e < len; e += 32) {
-                    const unsigned long long i = base + e;
-                    if (i == 0 || keys[i] != keys[i - 1]) { ++heads; last = e; }
-                }
-            }
-            heads = __reduce_add_sync(kFull, heads);
-            last = __reduce_max_sync(kFull, last);
-            const int b = (int)(k & 1);
-            if (lane == 0) { s_ah[b][ag] = heads; s_al[b][ag] = last; }
-            if (!meet()) break;
-            uint32_t C = 0;
-            int L = -1;
-#pragma unroll
-            for (int g = 0; g < kAgg; ++g) { C += s_ah[b][g]; L = s_al[b][g] > L ? s_al[b][g] : L; }
-            const int from = L < 0 ? 0 : L;   // the tile's trailing run starts here
-            uint32_t val = 0u;   // +0.0f for fp32
-            uint32_t acc = 0u;
-            if (staged) {
-                const W *wv = reinterpret_cast<const W *>(stage_vals(s));
-                const int v0 = ag * PART, v1 = v0 + PART;
-                for (int vi = (from / VK > v0 ? from / VK : v0) + lane; vi < v1; vi += 32) {
-                    const W w = wv[vi];
-#pragma unroll
-                    for (int j = 0; j < VK; ++j)
-                        if (vi * VK + j >= from) acc = RunValue<VU>::add(acc, KV::val(w, j));
-                }
-            } else if (ag == 0) {
-                for (int e = from + lane; e < len; e += 32) acc = RunValue<VU>::add(acc, vals[base + e]);
-            }
-            acc = RunValue<VU>::warp_total(acc);
-            if (lane == 0) s_av[b][ag] = acc;
-            if (!meet()) break;
-#pragma unroll
-            for (int g = 0; g < kAgg; ++g) val = RunValue<VU>::add(val, s_av[b][g]);
+            }   // a dense tile: the compute warps write it
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&empty[s]);
-                if (ag == 0) {
-                    const P agg = pair_of(C, val);
-                    Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
-                    PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
-                    agg_of[s] = agg;
-                    mbar_arrive(&agg_done[s]);
-                }
+                if (sparse) PS_TRACE_POINT(tile, PS_TRACE_STORED);
+                mbar_arrive(&ob_empty[o]);
             }
         }
     } else {
-        // ---------------- compute warps: scan the pairs, scatter at heads ----------------
-        for (long long k = 0;; ++k) {
-            const int s = (int)(k % S);
-            if (!role_wait(&full[s], (uint32_t)((k / S) & 1))) {
-                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
-                abort_meet(&s_abort, 1, CT);
-                break;
-            }
-            const long long tile = tile_of[s];
-            if (tile < 0 || tile >= num_tiles) break;
-            const unsigned long long base = (unsigned long long)tile * TILE;
-            const bool staged = a.use_bulk && base + TILE <= n;
-            const int seg = warp * 32 * ITEMS;
-            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
-
-            KU kk[ROWS][EPL];
-            uint32_t vv[ROWS][EPL];
-            uint32_t hm[ROWS];              // bit j: element j of this lane's chunk opens a run
-            uint32_t offc[ROWS], offv[ROWS];   // exclusive pair of the chunk within the warp
-            uint32_t rc = 0u, rv = 0u;      // pair of the warp's rows so far
-            const uint32_t lt_mask = (1u << lane) - 1u;
-            // lanes 4-7 of each quarter-warp read a pair of 16-byte vectors
-            // in swapped order, so that the quarter-warp's reads fall in
-            // distinct bank groups; the pair is put back in order in registers
-            const int rot = (lane >> 2) & 1;
+        // ---------------- compute warps: scan the pairs, pack the runs ----------------
+        const int seg = warp * 32 * ITEMS;   // the warp's first element in a tile
+        const uint32_t lt_mask = (1u << lane) - 1u;
+        // lanes 4-7 of each quarter-warp read a pair of 16-byte vectors in
+        // swapped order, so that the quarter-warp's reads fall in distinct
+        // bank groups; the pair is put back in order in registers
+        const int rot = (lane >> 2) & 1;
+        // This warp's keys and values of a tile, and each lane-chunk's head
+        // mask (bit j: element j of the chunk opens a run).
+        auto load_rows = [&](int s_, long long tile_, unsigned long long base_, bool staged_, KU (&kk)[ROWS][EPL],
+                             uint32_t (&vv)[ROWS][EPL], uint32_t (&hm)[ROWS]) {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
                 const int e0 = seg + (r * 32 + lane) * EPL;   // tile-local index of the chunk
                 uint32_t m = 0;
-                if (staged) {
-                    const KU *ks = stage_keys(s);
+                if (staged_) {
+                    const KU *ks = stage_keys(s_);
                     const V *kv = reinterpret_cast<const V *>(ks) + e0 / VK;
                     const V x0 = kv[rot], x1 = kv[rot ^ 1];
                     const V klo = rot ? x1 : x0, khi = rot ? x0 : x1;
@@ -445,8 +391,8 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                     if (lane == 0) prev = ks[e0 - 1];   // e0 == 0 reads the halo
 #pragma unroll
                     for (int j = 0; j < EPL; ++j) m |= (uint32_t)(kk[r][j] != (j ? kk[r][j - 1] : prev)) << j;
-                    if (tile == 0 && e0 == 0) m |= 1u;
-                    const uint4 *wv = reinterpret_cast<const uint4 *>(stage_vals(s)) + e0 / 4;
+                    if (tile_ == 0 && e0 == 0) m |= 1u;
+                    const uint4 *wv = reinterpret_cast<const uint4 *>(stage_vals(s_)) + e0 / 4;
                     if constexpr (WV == 2) {
                         const uint4 w0 = wv[rot], w1 = wv[rot ^ 1];
                         const uint4 vlo = rot ? w1 : w0, vhi = rot ? w0 : w1;
@@ -463,7 +409,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 } else {
 #pragma unroll
                     for (int j = 0; j < EPL; ++j) {
-                        const unsigned long long i = base + (unsigned long long)(e0 + j);
+                        const unsigned long long i = base_ + (unsigned long long)(e0 + j);
                         if (i < n) {
                             kk[r][j] = keys[i];
                             m |= (uint32_t)(i == 0 || kk[r][j] != keys[i - 1]) << j;
@@ -476,101 +422,235 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 }
                 hm[r] = m;
             }
+        };
+        // A dense tile waiting for the next iteration's pass: its stage, slot
+        // and the slot's phase parity (stage | slot << 8 | parity << 16), its
+        // tile (tile ids of a call with 32-bit run counts fit 32 bits), the
+        // pair of its elements before this warp's, this warp's runs, and per
+        // row the lane-chunk's head mask (bits 0-7) and runs before it in the
+        // warp (bits 8 up), and its exclusive value within the warp.
+        bool pend = false;
+        uint32_t pend_at = 0, pend_tile = 0, pend_rc = 0;
+        P pend_wex = 0;
+        uint32_t pend_info[ROWS], pend_offv[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) pend_info[r] = pend_offv[r] = 0;
+        // Writes the pending dense tile once its pair is known: this warp's
+        // runs packed in its slice of the stage -- keys of runs cw .. cw+rc-1
+        // and values of runs cw-1 .. cw+rc-2 (each head closes the run before
+        // it) -- then written as two contiguous ranges; the stage goes back
+        // after.  Entries are XOR-swizzled within each 32 (rbk_sw), so lanes
+        // packing entries EPL apart and lanes reading 32 consecutive ones hit
+        // distinct banks.
+        auto write_dense = [&]() {
+            const int ps = (int)(pend_at & 0xffu), pslot = (int)((pend_at >> 8) & 0xffu);
+            const unsigned long long pbase = (unsigned long long)pend_tile * TILE;
+            const bool pstaged = a.use_bulk && pbase + TILE <= n;
+            if (!role_wait(&prefix_ready[pslot], pend_at >> 16))
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+            if (warp == 0 && lane == 0) PS_TRACE_POINT(pend_tile, PS_TRACE_PREFIX_RECEIVED);
+            const P pre = Op::combine(excl_of[pslot], pend_wex);
+            const uint32_t cw = pair_count(pre), pv = pair_value(pre);
+            // the warp's keys and values again, all of them before the slice is reused
+            KU kp[ROWS][EPL];
+            uint32_t vp[ROWS][EPL], hp[ROWS];
+            load_rows(ps, pend_tile, pbase, pstaged, kp, vp, hp);
+            __syncwarp();
+            KU *pk = stage_keys(ps) + seg;
+            uint32_t *pvals = stage_vals(ps) + seg;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const uint32_t m = pend_info[r] & 0xffu, offc = pend_info[r] >> 8;
+                uint32_t q = offc;   // run index - cw of this chunk's first head
+                uint32_t v = offc ? pend_offv[r] : RunValue<VU>::add(pv, pend_offv[r]);
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) {
+                    const bool h = (m >> j) & 1u;
+                    if (h) {
+                        pk[rbk_sw(q)] = kp[r][j];
+                        pvals[rbk_sw(q)] = v;
+                    }
+                    const uint32_t sum = RunValue<VU>::add(v, vp[r][j]);
+                    v = h ? vp[r][j] : sum;
+                    q += h ? 1u : 0u;
+                }
+            }
+            __syncwarp();
+            for (uint32_t q = lane; q < pend_rc; q += 32) {
+                ukeys[cw + q] = pk[rbk_sw(q)];
+                if (cw + q > 0u) aggs[cw + q - 1u] = pvals[rbk_sw(q)];
+            }
+            // the stage goes back once every warp has written from its slice
+            named_barrier(2, CT);
+            if (warp == 0 && lane == 0) {
+                PS_TRACE_POINT(pend_tile, PS_TRACE_STORED);
+                mbar_arrive(&empty[ps]);
+            }
+            pend = false;
+        };
+        for (long long k = 0;; ++k) {
+            const int s = (int)(k % S);
+            const int slot = (int)(k % R);
+            if (!role_wait(&full[s], (uint32_t)((k / S) & 1))) {
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                abort_meet(&s_abort, 1, CT);
+                break;
+            }
+            const long long tile = tile_of[slot];
+            if (tile < 0 || tile >= num_tiles) {
+                if (pend) write_dense();
+                // end marker: pass it on to every look-back and writer warp,
+                // on the slots of the next iterations (the producer, which
+                // stopped here, writes none of them again)
+                if (warp == 0 && lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < kREnds; ++i) {
+                        if (i > 0) tile_of[(k + i) % R] = num_tiles;
+                        if (i < kLB) mbar_arrive(&agg_done[(k + i) % R]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+#pragma unroll
+                    for (int i = 0; i < kRW; ++i) mbar_arrive(&packed[(k + i) % R]);
+                break;
+            }
+            const unsigned long long base = (unsigned long long)tile * TILE;
+            const bool staged = a.use_bulk && base + TILE <= n;
+            if (warp == 0 && lane == 0) {
+                PS_TRACE_POINT(tile, PS_TRACE_DATA);
+                PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
+            }
+            KU kk[ROWS][EPL];
+            uint32_t vv[ROWS][EPL];
+            uint32_t hm[ROWS];
+            load_rows(s, tile, base, staged, kk, vv, hm);
             // Segmented inclusive scan of the chunk pairs over the lanes, the
             // rows side by side so that their shuffle chains overlap.  A
             // chunk's pair is (its heads, its value from its last head on);
             // the segment of lane l starts at the nearest lane <= l whose
             // chunk holds a head (none: it reaches back past lane 0), and a
             // partial from lane l-d joins only while l-d lies in it.
-            uint32_t cc[ROWS], cv[ROWS], cnt[ROWS];
-            int seg_lo[ROWS];
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                uint32_t v = 0u;
-#pragma unroll
-                for (int j = 0; j < EPL; ++j) {
-                    const bool h = (hm[r] >> j) & 1u;
-                    const uint32_t sum = RunValue<VU>::add(v, vv[r][j]);
-                    v = h ? vv[r][j] : sum;
-                }
-                cv[r] = v;
-                cnt[r] = (uint32_t)__popc(hm[r]);
-                cc[r] = cnt[r];
-                const uint32_t with_head = __ballot_sync(kFull, hm[r] != 0u);
-                const uint32_t le = with_head & (lt_mask | (1u << lane));
-                seg_lo[r] = le ? 31 - __clz(le) : -1;
-            }
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
+            uint32_t offc[ROWS], offv[ROWS];   // exclusive pair of the chunk within the warp
+            uint32_t rc = 0u, rv = 0u;         // pair of the warp's rows so far
+            {
+                uint32_t cc[ROWS], cv[ROWS], cnt[ROWS];
+                int seg_lo[ROWS];
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
-                    const uint32_t oc = __shfl_up_sync(kFull, cc[r], d);
-                    const uint32_t ov = __shfl_up_sync(kFull, cv[r], d);
-                    const uint32_t sum = RunValue<VU>::add(ov, cv[r]);
-                    cc[r] += lane >= d ? oc : 0u;
-                    cv[r] = (lane >= d && lane - d >= seg_lo[r]) ? sum : cv[r];
-                }
-            }
+                    uint32_t v = 0u;
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                // exclusive pair of the chunk: lane l-1's inclusive pair
-                const uint32_t ec = cc[r] - cnt[r];
-                uint32_t ev = __shfl_up_sync(kFull, cv[r], 1);
-                if (lane == 0) ev = 0u;
-                offc[r] = rc + ec;
-                offv[r] = ec ? ev : RunValue<VU>::add(rv, ev);
-                const uint32_t tc = __shfl_sync(kFull, cc[r], 31), tv = __shfl_sync(kFull, cv[r], 31);
-                rv = tc ? tv : RunValue<VU>::add(rv, tv);
-                rc += tc;
+                    for (int j = 0; j < EPL; ++j) {
+                        const bool h = (hm[r] >> j) & 1u;
+                        const uint32_t sum = RunValue<VU>::add(v, vv[r][j]);
+                        v = h ? vv[r][j] : sum;
+                    }
+                    cv[r] = v;
+                    cnt[r] = (uint32_t)__popc(hm[r]);
+                    cc[r] = cnt[r];
+                    const uint32_t with_head = __ballot_sync(kFull, hm[r] != 0u);
+                    const uint32_t le = with_head & (lt_mask | (1u << lane));
+                    seg_lo[r] = le ? 31 - __clz(le) : -1;
+                }
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+                    for (int r = 0; r < ROWS; ++r) {
+                        const uint32_t oc = __shfl_up_sync(kFull, cc[r], d);
+                        const uint32_t ov = __shfl_up_sync(kFull, cv[r], d);
+                        const uint32_t sum = RunValue<VU>::add(ov, cv[r]);
+                        cc[r] += lane >= d ? oc : 0u;
+                        cv[r] = (lane >= d && lane - d >= seg_lo[r]) ? sum : cv[r];
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    // exclusive pair of the chunk: lane l-1's inclusive pair
+                    const uint32_t ec = cc[r] - cnt[r];
+                    uint32_t ev = __shfl_up_sync(kFull, cv[r], 1);
+                    if (lane == 0) ev = 0u;
+                    offc[r] = rc + ec;
+                    offv[r] = ec ? ev : RunValue<VU>::add(rv, ev);
+                    const uint32_t tc = __shfl_sync(kFull, cc[r], 31), tv = __shfl_sync(kFull, cv[r], 31);
+                    rv = tc ? tv : RunValue<VU>::add(rv, tv);
+                    rc += tc;
+                }
             }
             P *sw = s_warp[k & 1];
             if (lane == 0) sw[warp] = pair_of(rc, rv);
-            named_barrier(1, CT);
+            named_barrier(1, CT);   // every warp has read the stage and posted its pair
             if (aborted(&s_abort)) break;
-            P warp_excl = 0;
+            P wex = 0;   // the pair of the tile's elements before this warp's
+            P agg = 0;
 #pragma unroll
-            for (int w = 0; w < kRCW; ++w)
-                if (w < warp) warp_excl = Op::combine(warp_excl, sw[w]);
-            if (!role_wait(&prefix_ready[s], (uint32_t)((k / S) & 1)))
-                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
-            const P pre = Op::combine(excl_of[s], warp_excl);
-            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
-            // Pack this warp's runs in its own slice of the stage -- free now:
-            // every compute warp has read the stage (named barrier above) and
-            // the aggregator finished with it before the prefix was handed
-            // over -- keyed by run index relative to the warp's first run,
-            // then write them out as two contiguous ranges: keys of runs
-            // cw .. cw+rc-1 and values of runs cw-1 .. cw+rc-2 (each head
-            // closes the run before it).  Entries are XOR-swizzled within
-            // each 32 (rbk_sw), so lanes packing entries EPL apart (every key
-            // a head) and lanes reading 32 consecutive ones hit distinct banks.
-            const uint32_t cw = pair_count(pre), pv = pair_value(pre);
-            KU *pk = stage_keys(s) + seg;
-            uint32_t *pvals = stage_vals(s) + seg;
+            for (int w = 0; w < kRCW; ++w) {
+                const P pw = sw[w];
+                if (w < warp) wex = Op::combine(wex, pw);
+                agg = Op::combine(agg, pw);
+            }
+            const bool sparse = pair_count(agg) <= (uint32_t)CAP;
+            if (warp == 0 && lane == 0) {
+                // A at once (P for tile 0, whose exclusive pair is empty); a
+                // sparse tile's elements are all in registers, so its stage
+                // goes back now, before the pair of the tile is known
+                Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
+                PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
+                agg_of[slot] = agg;
+                sparse_of[slot] = sparse ? 1 : 0;
+                mbar_arrive(&agg_done[slot]);
+                if (sparse) mbar_arrive(&empty[s]);
+            }
+            if (sparse) {
+                // pack the runs in the iteration's output buffer, once the
+                // writer is done with its previous tile; run q of the tile
+                // gets its key and the value of the run its head closes,
+                // summed from the tile's start at most
+                const int o = (int)(k % NOB);
+                if (k >= NOB && !role_wait(&ob_empty[o], (uint32_t)((k / NOB - 1) & 1))) {
+                    report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                    abort_meet(&s_abort, 1, CT);
+                    break;
+                }
+                KU *ok = out_keys(o);
+                uint32_t *ov = out_vals(o);
+                const uint32_t wq0 = pair_count(wex), wv0 = pair_value(wex);
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                uint32_t q = offc[r];   // run index - cw of this chunk's first head
-                uint32_t v = offc[r] ? offv[r] : RunValue<VU>::add(pv, offv[r]);
+                for (int r = 0; r < ROWS; ++r) {
+                    uint32_t q = wq0 + offc[r];
+                    uint32_t v = offc[r] ? offv[r] : RunValue<VU>::add(wv0, offv[r]);
 #pragma unroll
-                for (int j = 0; j < EPL; ++j) {
-                    const bool h = (hm[r] >> j) & 1u;
-                    if (h) {
-                        pk[rbk_sw(q)] = kk[r][j];
-                        pvals[rbk_sw(q)] = v;
+                    for (int j = 0; j < EPL; ++j) {
+                        const bool h = (hm[r] >> j) & 1u;
+                        if (h) {
+                            ok[rbk_sw(q)] = kk[r][j];
+                            ov[rbk_sw(q)] = v;
+                        }
+                        const uint32_t sum = RunValue<VU>::add(v, vv[r][j]);
+                        v = h ? vv[r][j] : sum;
+                        q += h ? 1u : 0u;
                     }
-                    const uint32_t sum = RunValue<VU>::add(v, vv[r][j]);
-                    v = h ? vv[r][j] : sum;
-                    q += h ? 1u : 0u;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&packed[slot]);
+            } else {
+                // a dense tile: nothing for the writer (it only frees the
+                // buffer); the compute warps write it after the next tile's
+                // pass, and hand its stage back then
+                if (lane == 0) mbar_arrive(&packed[slot]);
+            }
+            if (pend) write_dense();   // the previous dense tile, now that this tile's pair is out
+            if (!sparse) {
+                pend = true;
+                pend_at = (uint32_t)s | ((uint32_t)slot << 8) | ((uint32_t)((k / R) & 1) << 16);
+                pend_tile = (uint32_t)tile;
+                pend_wex = wex;
+                pend_rc = rc;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    pend_info[r] = hm[r] | (offc[r] << 8);
+                    pend_offv[r] = offv[r];
                 }
             }
-            __syncwarp();
-            for (uint32_t q = lane; q < rc; q += 32) {
-                ukeys[cw + q] = pk[rbk_sw(q)];
-                if (cw + q > 0u) aggs[cw + q - 1u] = pvals[rbk_sw(q)];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_STORED);
         }
         if (warp == 0 && lane == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_DONE);
     }

@@ -231,12 +231,6 @@ rle_kernel(RbkArgs a, long long num_tiles) {
     __shared__ int s_ok;
     if (tid == 0) {
         PS_TRACE_CTA_POINT(PS_TRACE_CTA_ENTRY);
-        if (PS_PREFETCH_FIRST_TILES && a.use_bulk) {
-            for (int j = 0; j < S; ++j) {
-                const unsigned long long t = blockIdx.x + (unsigned long long)j * gridDim.x;
-                if ((t + 1) * (unsigned long long)TILE <= n) prefetch_l2(keys + t * TILE, KEY_BYTES);
-            }
-        }
         uint32_t e;
         s_ok = begin_call(hdr, &e) ? 1 : 0;
         s_epoch = e;

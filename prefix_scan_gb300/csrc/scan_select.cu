@@ -153,15 +153,6 @@ select_kernel(SelectArgs a, long long num_tiles) {
     __shared__ int s_ok;
     if (tid == 0) {
         PS_TRACE_CTA_POINT(PS_TRACE_CTA_ENTRY);
-        if (PS_PREFETCH_FIRST_TILES && a.use_bulk) {
-            for (int j = 0; j < S; ++j) {
-                const unsigned long long t = blockIdx.x + (unsigned long long)j * gridDim.x;
-                if ((t + 1) * (unsigned long long)TILE <= n) {
-                    prefetch_l2(in + t * TILE, VAL_BYTES);
-                    if (OP == 0) prefetch_l2(a.flags + t * TILE, FLAG_BYTES);
-                }
-            }
-        }
         uint32_t e;
         s_ok = begin_call(hdr, &e) ? 1 : 0;
         s_epoch = e;

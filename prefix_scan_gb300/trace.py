@@ -177,7 +177,7 @@ def summarize(name: str, n: int, traces) -> str:
     spans, lasts = [], []
     gaps = {k: [] for k in ("claim_A", "A_lb", "lb", "P_compute", "compute_stored", "claim_stored",
                             "claim_data", "data_A", "interval")}
-    windows, polls = [], []
+    windows, polls, lbt = [], [], []
     starts = {k: [] for k in ("first_claim", "last_entry", "header", "first_data", "last_store", "last_done")}
     for t, lb, cta, ct in traces:
         starts["first_claim"].append(t[:, C].min())
@@ -202,6 +202,7 @@ def summarize(name: str, n: int, traces) -> str:
         looked = t[1:, LS] > 0   # tiles whose look-back ran and recorded
         windows.append((lb[1:][looked] >> 16).astype(np.int64))
         polls.append((lb[1:][looked] & 0xFFFF).astype(np.int64))
+        lbt.append((t[1:, PR] - t[1:, LS])[looked])
         lasts.append(t[:, C].max())
     cat = {k: np.concatenate(v) if v else np.zeros(1) for k, v in gaps.items()}
     win = np.concatenate(windows)
@@ -234,6 +235,16 @@ def summarize(name: str, n: int, traces) -> str:
                 f"3: {hist[2]:.1%}, 4: {hist[3]:.1%}, 5+: {hist[4]:.1%} (mean {win.mean():.2f})")
     rows.append(f"- re-polls of unpublished descriptors per look-back: median {np.median(pol):.0f}, "
                 f"p90 {np.percentile(pol, 90):.0f}, none in {(pol == 0).mean():.1%}")
+    # a look-back's time against the windows it walked, among those that never
+    # re-polled: the slope is the cost of one more window, the rest is fixed
+    lt = np.concatenate(lbt)
+    cells = []
+    for k in (1, 2, 3, 4, 5):
+        sel = (win == k) & (pol == 0)
+        if sel.sum() >= 20:
+            cells.append(f"{k}: {np.median(lt[sel]):.2f} us ({int(sel.sum())})")
+    if cells:
+        rows.append("- look-back time by windows walked, no re-polls (median, count): " + "; ".join(cells))
     rows.append("")
     return "\n".join(rows)
 
