@@ -249,6 +249,17 @@ def summarize(name: str, n: int, traces) -> str:
     return "\n".join(rows)
 
 
+def run_l2_probe() -> None:
+    """Builds (under _build/) and runs the probe of one look-back window's
+    L2 round trip, idle and under a full-rate copy; prints its lines."""
+    import subprocess
+    src = Path(__file__).resolve().parent / "probes" / "l2_window_latency.cu"
+    exe = nvbuild.BUILD_DIR / "l2_window_latency"
+    exe.parent.mkdir(parents=True, exist_ok=True)
+    subprocess.run([nvbuild.nvcc_path(), *nvbuild.ARCH, "-O3", "-o", str(exe), str(src)], check=True)
+    subprocess.run([str(exe)], check=True)
+
+
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--workload", action="append", choices=sorted(workloads.BY_NAME), default=[],
@@ -261,9 +272,14 @@ def main(argv=None) -> None:
     ap.add_argument("--runs", type=int, default=5)
     ap.add_argument("--define", action="append", default=[], metavar="NAME=VALUE",
                     help="compile-time setting of the variant build (repeatable)")
+    ap.add_argument("--l2-probe", action="store_true",
+                    help="build and run the L2 window-latency probe (probes/l2_window_latency.cu)")
     ap.add_argument("--launch-only", type=int, default=0, metavar="K",
                     help="only launch the scan K times (a build without the trace)")
     args = ap.parse_args(argv)
+    if args.l2_probe:
+        run_l2_probe()
+        return
     defines = {}
     for d in args.define:
         k, _, v = d.partition("=")
