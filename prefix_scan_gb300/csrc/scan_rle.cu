@@ -56,13 +56,13 @@ constexpr int kLCW = kThreads / 32;   // compute warps per CTA
 // Stages of keys (32 KiB each) and output buffers (a macro each, so that a
 // tuning sweep can rebuild).
 #ifndef PS_RLE_STAGES
-#define PS_RLE_STAGES 2
+#define PS_RLE_STAGES 3
 #endif
 #ifndef PS_RLE_OUT_BUFFERS
 #define PS_RLE_OUT_BUFFERS 4
 #endif
 #ifndef PS_RLE_OUT_BYTES
-#define PS_RLE_OUT_BYTES 8192
+#define PS_RLE_OUT_BYTES 4096
 #endif
 // Descriptors per lane in the look-back window (the operator is commutative).
 #ifndef PS_RLE_LOOKBACK_K

@@ -240,3 +240,40 @@ def test_positions_above_2p31():
     assert bool((sums[:m - 1] == L).all()) and int(sums[m - 1].item()) == n - (m - 1) * L
     del keys, ones, uk, sums, want
     torch.cuda.empty_cache()
+
+
+def _tiles_with_run_counts(T: int, counts, dtype, tail: int = 0) -> np.ndarray:
+    """Keys made tile by tile (T keys each): tile t holds counts[t] runs of
+    near-equal length, with keys no other tile uses, so every tile opens
+    with a head and has exactly counts[t] of them; then `tail` distinct keys
+    (a last, partial tile full of heads)."""
+    parts = []
+    for t, r in enumerate(counts):
+        r = max(1, min(r, T))
+        bounds = (np.arange(T) * r) // T          # run index of each key
+        parts.append(t * 65536 + bounds)
+    parts.append(len(counts) * 65536 + np.arange(tail))
+    return np.concatenate(parts).astype(dtype)
+
+
+@pytest.mark.parametrize("kdt", list(KEYS))
+@pytest.mark.parametrize("vkind", ["int32", "float32", "rle"])
+def test_sparse_and_dense_tiles_in_one_call(kdt, vkind):
+    # The kernels pack a tile's runs into an output buffer that a writer warp
+    # writes once the tile's prefix is known, unless the tile has more runs
+    # than a buffer holds; those are written by the compute warps one tile
+    # late.  Per-tile run counts around every buffer size of the two kernels
+    # and key widths, in shuffled order -- so dense tiles follow sparse ones
+    # and the reverse, dense tiles come in a row, and one is still pending
+    # when the input ends (the partial last tile is all heads).
+    T = RLE_TILE[kdt] if vkind == "rle" else TILE[kdt]
+    edges = [256, 319, 320, 321, 340, 341, 342, 383, 384, 385, 511, 512, 513, 671, 672, 673, 799, 800, 801,
+             1343, 1344, 1345]
+    counts = [c for c in edges if c <= T] + [1, 2, 31, T // 2, T - 1, T, T, T]
+    rng = np.random.default_rng(17)
+    for rep in range(2):
+        order = rng.permutation(len(counts))
+        keys = _tiles_with_run_counts(T, [counts[i] for i in order], KEYS[kdt], tail=T // 3 + 5)
+        vals = make_values(vkind, keys.shape[0], 40 + rep)
+        uk, agg, runs = run(keys, vals)
+        check(keys, vals, uk, agg, runs)
