@@ -24,11 +24,13 @@
 // Roles.  A producer warp takes tile ids and bulk-copies each tile's keys --
 // starting one 16-byte vector early, so the key before the tile (the "halo")
 // is in shared memory too -- into a ring of stages.  Eight compute warps
-// take the tiles in order and never wait for a tile's prefix: they find the
-// heads, count them (warp scans, then the warps' totals), publish the tile's
-// pair (A; P for tile 0) themselves, and pack the tile's runs into an output
-// buffer -- each head's key and 16-bit position within the tile, in order --
-// after which the stage goes straight back to the producer.  Look-back
+// take the tiles in order and never wait for a tile's prefix: each lane
+// finds the heads among 128 consecutive bytes of keys (one 32-bit mask), a
+// warp scan and a scan of the eight warps' totals count them, the warps
+// publish the tile's pair (A; P for tile 0) themselves and pack the tile's
+// runs into an output buffer -- each head's key, read back from the stage,
+// and its 16-bit position within the tile, in order -- after which the
+// stage goes straight back to the producer.  Look-back
 // warps resolve each tile's exclusive pair; a writer warp waits for it and
 // writes the buffer out as contiguous ranges (keys, and lengths as
 // differences of consecutive head positions), then frees the buffer.  So a stage is held only from its copy
@@ -40,7 +42,8 @@
 // iteration late: they publish its pair, keep its stage, do the next tile's
 // pass (so that tile's pair is published too), and only then wait for the
 // dense tile's prefix, re-read its keys from the stage, pack each row's runs
-// in their slice of the stage and write them as contiguous ranges.  Waiting
+// in their slice of the stage (the head masks kept from the pass) and write
+// them as contiguous ranges.  Waiting
 // for a tile's prefix before publishing the next tile's pair would chain
 // every CTA's tiles behind the look-backs of its earlier ones.  Counts and
 // positions are 32-bit (n < 2^32).
@@ -114,20 +117,26 @@ __device__ __forceinline__ bool rle_wait(uint64_t *bar, uint32_t parity) {
     return PS_RLE_WAIT_NS ? mbar_wait_suspend(bar, parity, PS_RLE_WAIT_NS) : mbar_wait(bar, parity);
 }
 
-// k[j] for a j known only at run time, without local memory: a tree of
-// selects on the bits of j (E - 1 selects on log2(E) bit tests).
-template <typename KU, int E>
-__device__ __forceinline__ KU pick(const KU (&k)[E], int j) {
-    static_assert(E == 4 || E == 8, "four or eight keys");
-    const bool b0 = j & 1, b1 = j & 2;
-    const KU a0 = b0 ? k[1] : k[0], a1 = b0 ? k[3] : k[2];
-    const KU lo = b1 ? a1 : a0;
-    if constexpr (E == 4) {
-        return lo;
+// Key J of the vector in register slot `slot` (known only at run time), by a
+// tree of selects on the slot's bits.
+template <typename KU, int VK, int J>
+__device__ __forceinline__ KU pick_slot(const KU (&k)[8][VK], int slot) {
+    const bool b0 = slot & 1, b1 = slot & 2;
+    const KU a0 = b0 ? k[1][J] : k[0][J], a1 = b0 ? k[3][J] : k[2][J];
+    const KU a2 = b0 ? k[5][J] : k[4][J], a3 = b0 ? k[7][J] : k[6][J];
+    const KU lo = b1 ? a1 : a0, hi = b1 ? a3 : a2;
+    return (slot & 4) ? hi : lo;
+}
+
+// A lane's head mask from slot order to key order: the KPL-bit mask rotated
+// left by `sh` bits (slot v holds the lane's vector (v + rot) & 7).
+template <int KPL> __device__ __forceinline__ uint32_t rle_unrotate(uint32_t m, int sh) {
+    static_assert(KPL == 32 || KPL == 16, "32 or 16 keys per lane");
+    if constexpr (KPL == 32) {
+        return __funnelshift_l(m, m, sh);
     } else {
-        const KU a2 = b0 ? k[5] : k[4], a3 = b0 ? k[7] : k[6];
-        const KU hi = b1 ? a3 : a2;
-        return (j & 4) ? hi : lo;
+        const uint32_t x = m | (m << 16);   // period 16: a 32-bit rotation rotates each half
+        return __funnelshift_l(x, x, sh) & 0xffffu;
     }
 }
 
@@ -183,7 +192,9 @@ rle_kernel(RbkArgs a, long long num_tiles) {
     constexpr int VK = KV::N;
     constexpr long long TILE = rle_tile<KU>();
     constexpr int ITEMS = (int)(TILE / kThreads);   // keys per compute lane
-    constexpr int EPL = 2 * VK;                     // keys per lane per row: two vectors
+    constexpr int KPL = 8 * VK;                     // a lane's keys in the pass: eight vectors
+    static_assert(ITEMS == KPL, "a lane's keys are 128 bytes");
+    constexpr int EPL = 2 * VK;                     // keys per lane per row of a dense write: two vectors
     constexpr int ROWS = ITEMS / EPL;
     constexpr int S = kLStages, R = kLRing, NOB = kLOut;
     constexpr uint32_t KEY_BYTES = (uint32_t)(TILE * sizeof(KU));
@@ -237,7 +248,7 @@ rle_kernel(RbkArgs a, long long num_tiles) {
         s_abort = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);     // the compute warps, or the writer of a dense tile
+            mbar_init(&empty[s], kLCW);  // each compute warp once it is done with the stage
         }
         for (int o = 0; o < NOB; ++o) mbar_init(&ob_empty[o], 1);   // the writer
         for (int slot = 0; slot < R; ++slot) {
@@ -360,22 +371,31 @@ rle_kernel(RbkArgs a, long long num_tiles) {
         }
     } else {
         // ---------------- compute warps: find the heads, pack the runs ----------------
-        const int seg = warp * 32 * ITEMS;   // the warp's first key in a tile
+        // Lane `lane` of warp `warp` owns the KPL consecutive keys of a tile
+        // that start at seg + lane * KPL: 128 bytes, eight 16-byte vectors.
+        // It reads them in an order rotated by its lane -- register slot v
+        // holds vector (v + lane) & 7 -- so that the eight lanes of each
+        // quarter-warp read eight distinct bank groups; consecutive slots
+        // hold consecutive vectors, except where the rotation wraps, at the
+        // lane's first key.
+        const int seg = warp * 32 * KPL;                      // the warp's first key in a tile
+        const int rot = lane & 7;
+        const uint32_t pos0 = (uint32_t)(seg + lane * KPL);   // the lane's first key in a tile
         // A dense tile waiting for the next iteration's pass: its stage, slot
         // and the slot's phase parity (pend_at: stage | slot << 8 | parity <<
         // 16), its tile (n < 2^32, so tile ids fit 32 bits), the pair of its
-        // keys before this warp's, and per row the lane's head mask (bits
-        // 0-7) and heads before it in the warp.
+        // keys before this warp's, and the lane's head mask and heads of the
+        // warp before its keys.
+        uint32_t pend_at = 0, pend_tile = 0, pend_m = 0, pend_before = 0;
         bool pend = false;
-        uint32_t pend_at = 0, pend_tile = 0;
         P pend_wex = 0;
-        uint32_t pend_info[ROWS];
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r) pend_info[r] = 0;
-        // Writes the pending dense tile once its pair is known: per row the
-        // row's runs -- run indices [cw + first, cw + first + nh) -- packed in
-        // this warp's slice of the stage, then keys and lengths written with
-        // consecutive lanes on consecutive runs; the stage goes back after.
+        // Writes the pending dense tile once its pair is known, in rows of 32
+        // lanes x EPL keys: per row the row's runs -- run indices [cw + first,
+        // cw + first + nh) -- packed in this warp's slice of the stage, then
+        // keys and lengths written with consecutive lanes on consecutive runs;
+        // the warp hands the stage back after.  Lane l's chunk of row r lies
+        // in the keys of lane 8r + l/4 in the pass, at bit EPL * (l % 4) of
+        // its mask.
         auto write_dense = [&]() {
             const int ps = (int)(pend_at & 0xffu), pslot = (int)((pend_at >> 8) & 0xffu);
             const unsigned long long pbase = (unsigned long long)pend_tile * TILE;
@@ -386,16 +406,16 @@ rle_kernel(RbkArgs a, long long num_tiles) {
             const P pre = OpRle::combine(excl_of[pslot], pend_wex);
             const uint32_t cw = (uint32_t)(pre >> 32);
             const uint32_t wbase = (uint32_t)(pbase + (unsigned long long)seg);
-            // the warp's keys again, all of them before the slice is reused
+            // the warp's keys again, in rows, all of them before the slice is reused
             KU kp[ROWS][EPL];
             if (pstaged) {
                 const V *kv = reinterpret_cast<const V *>(stage_keys(ps));
-                const int rot = (lane >> 2) & 1;
+                const int rr = (lane >> 2) & 1;   // pairs read in swapped order by lanes 4-7 of each quarter
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
                     const int e0 = seg + (r * 32 + lane) * EPL;
-                    const V x0 = kv[e0 / VK + rot], x1 = kv[e0 / VK + (rot ^ 1)];
-                    const V lo = rot ? x1 : x0, hi = rot ? x0 : x1;
+                    const V x0 = kv[e0 / VK + rr], x1 = kv[e0 / VK + (rr ^ 1)];
+                    const V lo = rr ? x1 : x0, hi = rr ? x0 : x1;
 #pragma unroll
                     for (int j = 0; j < VK; ++j) {
                         kp[r][j] = KV::key(lo, j);
@@ -415,18 +435,23 @@ rle_kernel(RbkArgs a, long long num_tiles) {
             KU *pk = stage_keys(ps) + seg;                                 // 32 * EPL keys
             uint32_t *pp = reinterpret_cast<uint32_t *>(pk + 32 * EPL);   // 32 * EPL offsets
             uint32_t row_prev = (uint32_t)pre;   // position of the last head before the row
+            const uint32_t sh = (uint32_t)(EPL * (lane & 3));
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
-                const uint32_t mr = pend_info[r] & 0xffu, rb = pend_info[r] >> 8;
+                const int src = 8 * r + (lane >> 2);
+                const uint32_t ml = __shfl_sync(kFull, pend_m, src);
+                const uint32_t rb = __shfl_sync(kFull, pend_before, src) + (uint32_t)__popc(ml & ((1u << sh) - 1u));
+                const uint32_t mr = (ml >> sh) & ((1u << EPL) - 1u);
                 const uint32_t first = __shfl_sync(kFull, rb, 0);
                 const uint32_t nh = __shfl_sync(kFull, rb + (uint32_t)__popc(mr), 31) - first;
                 uint32_t q = rb - first;
-                for (uint32_t mm = mr; mm; mm &= mm - 1u) {
-                    const int j = __ffs(mm) - 1;
-                    pk[rle_sw(q)] = pick<KU, EPL>(kp[r], j);
-                    pp[rle_sw(q)] = (uint32_t)((r * 32 + lane) * EPL + j);
-                    ++q;
-                }
+#pragma unroll
+                for (int j = 0; j < EPL; ++j)
+                    if ((mr >> j) & 1u) {
+                        pk[rle_sw(q)] = kp[r][j];
+                        pp[rle_sw(q)] = (uint32_t)((r * 32 + lane) * EPL + j);
+                        ++q;
+                    }
                 __syncwarp();
                 const uint32_t c0 = cw + first;
                 for (uint32_t t = lane; t < nh; t += 32) {
@@ -438,10 +463,9 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 if (nh) row_prev = wbase + pp[rle_sw(nh - 1u)];
                 __syncwarp();
             }
-            // the stage goes back once every warp has written from its slice
-            named_barrier(2, CT);
-            if (warp == 0 && lane == 0) {
-                PS_TRACE_POINT(pend_tile, PS_TRACE_STORED);
+            // this warp is done with the stage
+            if (lane == 0) {
+                if (warp == 0) PS_TRACE_POINT(pend_tile, PS_TRACE_STORED);
                 mbar_arrive(&empty[ps]);
             }
             pend = false;
@@ -480,93 +504,81 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
             }
 
-            // Rows of two 16-byte vectors per lane (EPL keys); lanes 4-7 of
-            // each quarter-warp read their pair in swapped order, so that
-            // the eight 16-byte reads of a quarter-warp fall in distinct bank
-            // groups.  Bit j of m[r]: key j of the lane's chunk of row r
-            // opens a run.
-            KU kk[ROWS][EPL];
-            uint32_t m[ROWS];
+            // Bit p of m: the lane's key p opens a run.
+            const KU *ks = stage_keys(s);
+            uint32_t m = 0;
             if (staged) {
-                const KU *ks = stage_keys(s);
-                const V *kv = reinterpret_cast<const V *>(ks);
-                const int rot = (lane >> 2) & 1;
+                const V *kv = reinterpret_cast<const V *>(ks + pos0);
+                KU kr[8][VK];
 #pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    const int e0 = seg + (r * 32 + lane) * EPL;
-                    const V x0 = kv[e0 / VK + rot], x1 = kv[e0 / VK + (rot ^ 1)];
-                    const V lo = rot ? x1 : x0, hi = rot ? x0 : x1;
+                for (int v = 0; v < 8; ++v) {
+                    const V x = kv[(v + rot) & 7];
 #pragma unroll
-                    for (int j = 0; j < VK; ++j) {
-                        kk[r][j] = KV::key(lo, j);
-                        kk[r][VK + j] = KV::key(hi, j);
-                    }
-                    KU prev = __shfl_up_sync(kFull, kk[r][EPL - 1], 1);
-                    if (lane == 0) prev = ks[e0 - 1];   // e0 == 0 reads the halo
-                    uint32_t mm = 0;
-#pragma unroll
-                    for (int j = 0; j < EPL; ++j) mm |= (uint32_t)(kk[r][j] != (j ? kk[r][j - 1] : prev)) << j;
-                    if (tile == 0 && e0 == 0) mm |= 1u;
-                    m[r] = mm;
+                    for (int j = 0; j < VK; ++j) kr[v][j] = KV::key(x, j);
                 }
+                // in slot order, each key against the one in the slot before
+                // (slot 0 against slot 7's last key: right except at the wrap)
+                uint32_t mrot = 0;
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+#pragma unroll
+                    for (int j = 0; j < VK; ++j)
+                        mrot |= (uint32_t)(kr[v][j] != (j ? kr[v][j - 1] : kr[(v + 7) & 7][VK - 1])) << (v * VK + j);
+                m = rle_unrotate<KPL>(mrot, VK * rot);
+                // bit 0 compared the lane's first key with its own last one;
+                // the key before it is the previous lane's last (for lane 0 the
+                // key before the warp, the tile's halo for warp 0)
+                const KU first = pick_slot<KU, VK, 0>(kr, (8 - rot) & 7);
+                const KU last = pick_slot<KU, VK, VK - 1>(kr, (7 - rot) & 7);
+                KU prev = __shfl_up_sync(kFull, last, 1);
+                if (lane == 0) prev = ks[seg - 1];
+                m = (m & ~1u) | (uint32_t)(first != prev);
             } else {
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    uint32_t mm = 0;
-#pragma unroll
-                    for (int j = 0; j < EPL; ++j) {
-                        const unsigned long long i = base + seg + (unsigned long long)((r * 32 + lane) * EPL + j);
-                        kk[r][j] = i < n ? keys[i] : KU(0);
-                        mm |= (uint32_t)(i < n && (i == 0 || kk[r][j] != keys[i - 1])) << j;
-                    }
-                    m[r] = mm;
+#pragma unroll 4
+                for (int p = 0; p < KPL; ++p) {
+                    const unsigned long long i = base + pos0 + (unsigned long long)p;
+                    m |= (uint32_t)(i < n && (i == 0 || keys[i] != keys[i - 1])) << p;
                 }
             }
+            if (tile == 0 && seg == 0 && lane == 0) m |= 1u;
 
-            // Per row: heads before each lane's chunk within the warp (warp
-            // scan of the chunk counts); the warp's heads and its last one.
-            uint32_t before[ROWS];
-            uint32_t run_c = 0;
-            int run_last = -1;   // the warp's last head, from the warp's first key
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                const uint32_t t = (uint32_t)__popc(m[r]);
-                const uint32_t sc = warp_inclusive<uint32_t>(t, lane);
-                before[r] = run_c + (sc - t);
-                run_c += __shfl_sync(kFull, sc, 31);
-                const int lp = m[r] ? (r * 32 + lane) * EPL + 31 - __clz(m[r]) : -1;
-                const int row_last = __reduce_max_sync(kFull, lp);
-                run_last = row_last > run_last ? row_last : run_last;
-            }
+            // the warp's heads before this lane's keys, its heads and its
+            // last head (from the warp's first key)
+            const uint32_t cnt = (uint32_t)__popc(m);
+            const uint32_t sc = warp_inclusive<uint32_t>(cnt, lane);
+            const uint32_t before = sc - cnt;
+            const uint32_t run_c = __shfl_sync(kFull, sc, 31);
+            const int run_last = __reduce_max_sync(kFull, m ? lane * KPL + 31 - __clz(m) : -1);
             P *sw = s_warp[k & 1];
             if (lane == 0)
                 sw[warp] = ((P)run_c << 32) |
                            (run_last >= 0 ? (uint32_t)(base + (unsigned long long)(seg + run_last)) : 0u);
-            named_barrier(1, CT);   // every warp has read the stage and posted its pair
+            named_barrier(1, CT);   // every warp has posted its pair
             if (aborted(&s_abort)) break;
-            P wex = 0;   // the pair of the tile's keys before this warp's
-            P agg = 0;
+            // the warps' pairs scanned across lanes 0 .. kLCW-1: the pair of
+            // the tile's keys before this warp's, and the tile's
+            P wp = lane < kLCW ? sw[lane] : (P)0;
 #pragma unroll
-            for (int w = 0; w < kLCW; ++w) {
-                const P pw = sw[w];
-                if (w < warp) wex = OpRle::combine(wex, pw);
-                agg = OpRle::combine(agg, pw);
+            for (int d = 1; d < kLCW; d <<= 1) {
+                const P o = __shfl_up_sync(kFull, wp, d);
+                if (lane >= d) wp = OpRle::combine(o, wp);
             }
+            const P agg = __shfl_sync(kFull, wp, kLCW - 1);
+            P wex = __shfl_sync(kFull, wp, warp > 0 ? warp - 1 : 0);
+            if (warp == 0) wex = 0;
             const bool sparse = (agg >> 32) <= (P)CAP;
             if (warp == 0 && lane == 0) {
-                // A at once (P for tile 0, whose exclusive pair is empty); a
-                // sparse tile's keys are all in registers, so its stage goes
-                // back now, before the pair of the tile is known
+                // A at once (P for tile 0, whose exclusive pair is empty)
                 Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
                 PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
                 agg_of[slot] = agg;
                 sparse_of[slot] = sparse ? 1 : 0;
                 mbar_arrive(&agg_done[slot]);
-                if (sparse) mbar_arrive(&empty[s]);
             }
             if (sparse) {
                 // pack the runs in the iteration's output buffer, once the
-                // writer is done with its previous tile
+                // writer is done with its previous tile: the keys come from
+                // the stage, which goes back to the producer after
                 const int o = (int)(k % NOB);
                 if (k >= NOB && !rle_wait(&ob_empty[o], (uint32_t)((k / NOB - 1) & 1))) {
                     report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
@@ -575,20 +587,18 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 }
                 KU *ok = out_keys(o);
                 uint16_t *op = out_pos(o);
-                const uint32_t wq0 = (uint32_t)(wex >> 32);   // heads before this warp in the tile
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    const uint32_t pos0 = (uint32_t)(seg + (r * 32 + lane) * EPL);
-                    uint32_t q = wq0 + before[r];
-                    for (uint32_t mm = m[r]; mm; mm &= mm - 1u) {
-                        const int j = __ffs(mm) - 1;
-                        ok[rle_sw(q)] = pick<KU, EPL>(kk[r], j);
-                        op[rle_sw(q)] = (uint16_t)(pos0 + (uint32_t)j);
-                        ++q;
-                    }
+                uint32_t q = (uint32_t)(wex >> 32) + before;
+                for (uint32_t mm = m; mm; mm &= mm - 1u) {
+                    const uint32_t p = pos0 + (uint32_t)(__ffs(mm) - 1);
+                    ok[rle_sw(q)] = staged ? ks[p] : keys[base + p];
+                    op[rle_sw(q)] = (uint16_t)p;
+                    ++q;
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&packed[slot]);
+                if (lane == 0) {
+                    mbar_arrive(&packed[slot]);
+                    mbar_arrive(&empty[s]);   // this warp is done with the stage
+                }
             } else {
                 // a dense tile: nothing for the writer (it only frees the
                 // buffer); the compute warps write it after the next tile's
@@ -601,8 +611,8 @@ rle_kernel(RbkArgs a, long long num_tiles) {
                 pend_at = (uint32_t)s | ((uint32_t)slot << 8) | ((uint32_t)((k / R) & 1) << 16);
                 pend_tile = (uint32_t)tile;
                 pend_wex = wex;
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) pend_info[r] = m[r] | (before[r] << 8);
+                pend_m = m;
+                pend_before = before;
             }
         }
         if (warp == 0 && lane == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_DONE);
