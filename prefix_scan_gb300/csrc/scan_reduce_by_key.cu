@@ -580,14 +580,18 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             if (lane == 0) sw[warp] = pair_of(rc, rv);
             named_barrier(1, CT);   // every warp has read the stage and posted its pair
             if (aborted(&s_abort)) break;
-            P wex = 0;   // the pair of the tile's elements before this warp's
-            P agg = 0;
+            // the warps' pairs scanned across lanes 0 .. kRCW-1 (earlier part
+            // on the left): the pair of the tile's elements before this
+            // warp's, and the tile's
+            P wp = lane < kRCW ? sw[lane] : (P)0;
 #pragma unroll
-            for (int w = 0; w < kRCW; ++w) {
-                const P pw = sw[w];
-                if (w < warp) wex = Op::combine(wex, pw);
-                agg = Op::combine(agg, pw);
+            for (int d = 1; d < kRCW; d <<= 1) {
+                const P o = __shfl_up_sync(kFull, wp, d);
+                if (lane >= d) wp = Op::combine(o, wp);
             }
+            const P agg = __shfl_sync(kFull, wp, kRCW - 1);
+            P wex = __shfl_sync(kFull, wp, warp > 0 ? warp - 1 : 0);
+            if (warp == 0) wex = 0;
             const bool sparse = pair_count(agg) <= (uint32_t)CAP;
             if (warp == 0 && lane == 0) {
                 // A at once (P for tile 0, whose exclusive pair is empty); a
