@@ -23,30 +23,31 @@
 //
 // Roles.  A producer warp takes tile ids and bulk-copies each tile's keys --
 // starting one 16-byte vector early, so the key before the tile (the "halo")
-// is in shared memory too -- into a ring of stages.  Eight compute warps
-// take the tiles in order and never wait for a tile's prefix: each lane
-// finds the heads among 128 consecutive bytes of keys (one 32-bit mask), a
-// warp scan and a scan of the eight warps' totals count them, the warps
+// is in shared memory too -- into a ring of stages.  The compute warps
+// (sixteen: one CTA per SM and 64 KiB tiles, so that every look-back covers
+// twice the bytes it did with two CTAs of 32 KiB tiles) take the tiles in
+// order and never wait for a tile's
+// prefix: each lane finds the heads among 128 consecutive bytes of keys (one
+// mask), a warp scan and a scan of the warps' totals count them, the warps
 // publish the tile's pair (A; P for tile 0) themselves and pack the tile's
 // runs into an output buffer -- each head's key, read back from the stage,
-// and its 16-bit position within the tile, in order -- after which the
-// stage goes straight back to the producer.  Look-back
-// warps resolve each tile's exclusive pair; a writer warp waits for it and
-// writes the buffer out as contiguous ranges (keys, and lengths as
-// differences of consecutive head positions), then frees the buffer.  So a stage is held only from its copy
+// and its 16-bit position within the tile, in order -- after which the stage
+// goes straight back to the producer.  Look-back warps resolve each tile's
+// exclusive pair; writer warps wait for it and write the buffer out as
+// contiguous ranges (keys, and lengths as differences of consecutive head
+// positions), then free the buffer.  So a stage is held only from its copy
 // to the compute warps' pass, and the look-back's latency stays off both the
 // stages and the compute warps: it is covered by the output buffers, which
-// hold a few bytes per head.  A tile with more heads than a buffer holds
-// (a dense tile) is written by the compute warps themselves -- eight warps
-// instead of one for a tile that writes as much as it reads -- one
-// iteration late: they publish its pair, keep its stage, do the next tile's
-// pass (so that tile's pair is published too), and only then wait for the
-// dense tile's prefix, re-read its keys from the stage, pack each row's runs
-// in their slice of the stage (the head masks kept from the pass) and write
-// them as contiguous ranges.  Waiting
-// for a tile's prefix before publishing the next tile's pair would chain
-// every CTA's tiles behind the look-backs of its earlier ones.  Counts and
-// positions are 32-bit (n < 2^32).
+// hold a few bytes per head.  A tile with more heads than a buffer holds (a
+// dense tile) is written by the compute warps themselves -- all of them
+// instead of one for a tile that writes as much as it reads -- one iteration
+// late: they publish its pair, keep its stage, do the next tile's pass (so
+// that tile's pair is published too), and only then wait for the dense
+// tile's prefix, re-read its keys from the stage, pack each row's runs in
+// their slice of the stage (the head masks kept from the pass) and write
+// them as contiguous ranges.  Waiting for a tile's prefix before publishing
+// the next tile's pair would chain every CTA's tiles behind the look-backs
+// of its earlier ones.  Counts and positions are 32-bit (n < 2^32).
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
 #include "scan_trace.cuh"
@@ -55,8 +56,18 @@ namespace ps {
 
 namespace {
 
-constexpr int kLCW = kThreads / 32;   // compute warps per CTA
-// Stages of keys (32 KiB each) and output buffers (a macro each, so that a
+// Compute warps per CTA and CTAs per SM (macros, so that a tuning sweep can
+// rebuild); a tile is 128 bytes of keys per compute lane.
+#ifndef PS_RLE_COMPUTE_WARPS
+#define PS_RLE_COMPUTE_WARPS 16
+#endif
+#ifndef PS_RLE_CTAS_PER_SM
+#define PS_RLE_CTAS_PER_SM 1
+#endif
+constexpr int kLCW = PS_RLE_COMPUTE_WARPS;
+constexpr int kLCtasPerSm = PS_RLE_CTAS_PER_SM;
+static_assert(kLCW >= 1 && kLCW <= 32, "the warps' pairs are scanned across the lanes of one warp");
+// Stages of keys (one tile each) and output buffers (a macro each, so that a
 // tuning sweep can rebuild).
 #ifndef PS_RLE_STAGES
 #define PS_RLE_STAGES 3
@@ -65,7 +76,7 @@ constexpr int kLCW = kThreads / 32;   // compute warps per CTA
 #define PS_RLE_OUT_BUFFERS 4
 #endif
 #ifndef PS_RLE_OUT_BYTES
-#define PS_RLE_OUT_BYTES 4096
+#define PS_RLE_OUT_BYTES 8192
 #endif
 // Descriptors per lane in the look-back window (the operator is commutative).
 #ifndef PS_RLE_LOOKBACK_K
@@ -77,7 +88,7 @@ constexpr int kLCW = kThreads / 32;   // compute warps per CTA
 #define PS_RLE_LOOKBACK_WARPS 2
 #endif
 #ifndef PS_RLE_WRITER_WARPS
-#define PS_RLE_WRITER_WARPS 1
+#define PS_RLE_WRITER_WARPS 2
 #endif
 constexpr int kLStages = PS_RLE_STAGES;
 constexpr int kLOut = PS_RLE_OUT_BUFFERS;
@@ -163,11 +174,9 @@ template <> struct RleVec<unsigned long long> {
     static __device__ __forceinline__ unsigned long long key(const V &v, int j) { return vget(v, j); }
 };
 
-// Bytes of keys per tile (a macro so that a tuning sweep can rebuild).
-#ifndef PS_RLE_TILE_BYTES
-#define PS_RLE_TILE_BYTES 32768
-#endif
-template <typename KU> constexpr long long rle_tile() { return PS_RLE_TILE_BYTES / (long long)sizeof(KU); }
+// Bytes of keys per tile: 128 per compute lane.
+constexpr long long kLTileBytes = (long long)kLCW * 32 * 128;
+template <typename KU> constexpr long long rle_tile() { return kLTileBytes / (long long)sizeof(KU); }
 template <typename KU> constexpr uint32_t rle_stage_bytes() { return (uint32_t)(rle_tile<KU>() * sizeof(KU) + 16); }
 // Runs an output buffer holds: a key and a 16-bit position within the tile
 // each, a multiple of 32 entries (the swizzle stays within each 32).
@@ -184,14 +193,14 @@ template <typename KU> constexpr size_t rle_smem_bytes() {
 
 
 template <typename KU>
-__global__ void __launch_bounds__(kLThreads, kPCtasPerSm)
+__global__ void __launch_bounds__(kLThreads, kLCtasPerSm)
 rle_kernel(RbkArgs a, long long num_tiles) {
     using KV = RleVec<KU>;
     using V = typename KV::V;
     using P = unsigned long long;
     constexpr int VK = KV::N;
     constexpr long long TILE = rle_tile<KU>();
-    constexpr int ITEMS = (int)(TILE / kThreads);   // keys per compute lane
+    constexpr int ITEMS = (int)(TILE / (kLCW * 32));   // keys per compute lane
     constexpr int KPL = 8 * VK;                     // a lane's keys in the pass: eight vectors
     static_assert(ITEMS == KPL, "a lane's keys are 128 bytes");
     constexpr int EPL = 2 * VK;                     // keys per lane per row of a dense write: two vectors
@@ -637,7 +646,7 @@ static cudaError_t launch_rle_keys(const RbkArgs &a, cudaStream_t s) {
         if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    long long grid = (long long)sms * kPCtasPerSm;
+    long long grid = (long long)sms * kLCtasPerSm;
     if (grid > tiles) grid = tiles;
     rle_kernel<KU><<<(unsigned int)grid, kLThreads, smem, s>>>(a, tiles);
     return cudaGetLastError();

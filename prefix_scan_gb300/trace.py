@@ -24,7 +24,9 @@ look-back off the critical path; these figures say whether it does.
 settings of the kernel (for example the look-back's poll back-off), and
 ``--launch-only K`` only launches the scan K times after one warm-up call
 (no trace read, no summary): the command to put under a profiler when
-comparing such variants.
+comparing such variants.  ``--l2-probe`` and ``--read-probe`` build and run
+the two measurement probes under ``probes/`` instead (one look-back window's
+L2 round trip; HBM read bandwidth by loads and by bulk copies).
 """
 from __future__ import annotations
 
@@ -85,7 +87,7 @@ def launch_only(lib: ctypes.CDLL, w: workloads.Workload, n: int, launches: int) 
 # Kernels the trace covers: the record each keeps (include/prefix_scan_trace.h)
 # and the elements of one of its tiles (32-bit keys / elements).
 KERNELS = {"scan": 0, "select": 1, "partition": 1, "rbk": 2, "rle": 3}
-RBK_TILE, RLE_TILE = 4096, 8192
+RBK_TILE, RLE_TILE = 4096, 16384
 
 
 def make_call(lib: ctypes.CDLL, kernel: str, w: workloads.Workload | None, n: int, mean_run: int, dev):
@@ -260,6 +262,17 @@ def run_l2_probe() -> None:
     subprocess.run([str(exe)], check=True)
 
 
+def run_read_probe() -> None:
+    """Builds (under _build/) and runs the read-bandwidth probe: 1 GiB read by
+    plain loads and by bulk copies into shared-memory stages; prints its lines."""
+    import subprocess
+    src = Path(__file__).resolve().parent / "probes" / "read_bandwidth.cu"
+    exe = nvbuild.BUILD_DIR / "read_bandwidth"
+    exe.parent.mkdir(parents=True, exist_ok=True)
+    subprocess.run([nvbuild.nvcc_path(), *nvbuild.ARCH, "-O3", "-std=c++17", "-o", str(exe), str(src)], check=True)
+    subprocess.run([str(exe)], check=True)
+
+
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--workload", action="append", choices=sorted(workloads.BY_NAME), default=[],
@@ -274,11 +287,16 @@ def main(argv=None) -> None:
                     help="compile-time setting of the variant build (repeatable)")
     ap.add_argument("--l2-probe", action="store_true",
                     help="build and run the L2 window-latency probe (probes/l2_window_latency.cu)")
+    ap.add_argument("--read-probe", action="store_true",
+                    help="build and run the read-bandwidth probe (probes/read_bandwidth.cu)")
     ap.add_argument("--launch-only", type=int, default=0, metavar="K",
                     help="only launch the scan K times (a build without the trace)")
     args = ap.parse_args(argv)
     if args.l2_probe:
         run_l2_probe()
+        return
+    if args.read_probe:
+        run_read_probe()
         return
     defines = {}
     for d in args.define:

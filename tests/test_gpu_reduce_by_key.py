@@ -192,13 +192,14 @@ def test_full_size_32m_pairs(vkind):
     torch.cuda.empty_cache()
 
 
-RLE_TILE = {"int32": 8192, "float32": 8192, "int64": 4096}   # keys per run-length-encoding tile
+RLE_TILE = {"int32": 16384, "float32": 16384, "int64": 8192}   # keys per run-length-encoding tile
 
 
 @pytest.mark.parametrize("kdt", list(KEYS))
 def test_rle_tile_geometry(kdt):
-    # run-length encoding has tiles of its own (32 KiB of keys): lengths
-    # around them, and runs cut at tile, warp (1/8 tile) and row boundaries
+    # run-length encoding has tiles of its own (64 KiB of keys): lengths
+    # around them, and runs cut at tile, warp (1/16 tile), lane (32 or 16
+    # keys) and row boundaries
     T = RLE_TILE[kdt]
     for k, n in enumerate([T - 1, T, T + 1, 2 * T, 2 * T + 1, 3 * T - 1, 7 * T + 5]):
         for mean in (1, 2, 7, 1024, T):
@@ -206,8 +207,8 @@ def test_rle_tile_geometry(kdt):
             uk, cnt, runs = run(keys, None)
             check(keys, None, uk, cnt, runs)
     n = 6 * T + 3
-    cuts = sorted({0, T // 8 - 1, T // 8, T // 32, T // 32 + 1, T - 1, T, 2 * T - T // 8, 2 * T + 1,
-                   4 * T - 1, 4 * T, 5 * T + T // 2})
+    cuts = sorted({0, T // 16 - 1, T // 16, T // 8, T // 32, T // 32 + 1, T // 512, T // 512 + 1,
+                   3 * T // 512 - 1, T - 1, T, 2 * T - T // 16, 2 * T + 1, 4 * T - 1, 4 * T, 5 * T + T // 2})
     keys = np.zeros(n, dtype=np.int64)
     for j, c in enumerate(cuts):
         keys[c:] = j + 1
