@@ -46,7 +46,17 @@ namespace ps {
 
 namespace {
 
-constexpr int kRCW = kThreads / 32;   // compute warps per CTA
+// Compute warps per CTA and CTAs per SM (macros, so that a tuning sweep can
+// rebuild).
+#ifndef PS_RBK_COMPUTE_WARPS
+#define PS_RBK_COMPUTE_WARPS 8
+#endif
+#ifndef PS_RBK_CTAS_PER_SM
+#define PS_RBK_CTAS_PER_SM 2
+#endif
+constexpr int kRCW = PS_RBK_COMPUTE_WARPS;
+constexpr int kRCtasPerSm = PS_RBK_CTAS_PER_SM;
+static_assert(kRCW >= 1 && kRCW <= 32, "the warps' pairs are scanned across the lanes of one warp");
 // Stages, output buffers and their bytes, look-back and writer warps (macros
 // so that a tuning sweep can rebuild).
 #ifndef PS_RBK_STAGES
@@ -175,7 +185,7 @@ template <typename KU> constexpr size_t rbk_smem_bytes() {
 
 
 template <typename KU, typename VU>
-__global__ void __launch_bounds__(kRbkThreads, kPCtasPerSm)
+__global__ void __launch_bounds__(kRbkThreads, kRCtasPerSm)
 reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     using KV = KeyVec<KU>;
     using V = typename KV::V;
@@ -183,7 +193,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
     using P = unsigned long long;
     constexpr int VK = KV::N;
     constexpr long long TILE = rbk_tile<KU>();
-    constexpr int ITEMS = (int)(TILE / kThreads);
+    constexpr int ITEMS = (int)(TILE / (kRCW * 32));
     // A compute lane's share of a row: two key vectors (EPL keys) and their
     // EPL 32-bit values (one or two 16-byte vectors), so that a tile takes
     // half as many segmented warp scans as with one key vector per row.
@@ -679,7 +689,7 @@ static cudaError_t launch_rbk_variant(const RbkArgs &a, cudaStream_t s) {
         if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    long long grid = (long long)sms * kPCtasPerSm;
+    long long grid = (long long)sms * kRCtasPerSm;
     if (grid > tiles) grid = tiles;
     reduce_by_key_kernel<KU, VU><<<(unsigned int)grid, kRbkThreads, smem, s>>>(a, tiles);
     return cudaGetLastError();

@@ -33,7 +33,16 @@ namespace ps {
 
 namespace {
 
-constexpr int kSCW = kThreads / 32;   // compute warps per CTA
+// Compute warps per CTA and CTAs per SM (macros, so that a tuning sweep can
+// rebuild).
+#ifndef PS_SEL_COMPUTE_WARPS
+#define PS_SEL_COMPUTE_WARPS (PS_THREADS / 32)
+#endif
+#ifndef PS_SEL_CTAS_PER_SM
+#define PS_SEL_CTAS_PER_SM PS_PERSIST_CTAS_PER_SM
+#endif
+constexpr int kSCW = PS_SEL_COMPUTE_WARPS;
+constexpr int kSCtasPerSm = PS_SEL_CTAS_PER_SM;
 
 // Elements per thread of a select / partition tile and the stages of the
 // flag-array form (macros so that a tuning sweep can rebuild with others).
@@ -62,7 +71,7 @@ template <bool PARTITION> constexpr int sel_threads() { return (kSCW + 2 + sel_l
 template <typename T> struct SelItems { static constexpr int value = PS_SEL_ITEMS32; };
 template <> struct SelItems<int64_t> { static constexpr int value = kItems64; };
 
-template <typename T> constexpr long long sel_tile() { return (long long)kThreads * SelItems<T>::value; }
+template <typename T> constexpr long long sel_tile() { return (long long)kSCW * 32 * SelItems<T>::value; }
 // Stages: 2 with a flag array (values + flags, 40 KiB per int32 tile), else
 // 3; partition keeps 2 either way to make room for its pack buffer.
 template <int OP, bool PARTITION> constexpr int sel_stages() {
@@ -109,7 +118,7 @@ template <> __device__ __forceinline__ int64_t vget_t<int64_t>(const ulonglong2 
 
 
 template <typename T, int OP, bool PARTITION>
-__global__ void __launch_bounds__(sel_threads<PARTITION>(), kPCtasPerSm)
+__global__ void __launch_bounds__(sel_threads<PARTITION>(), kSCtasPerSm)
 select_kernel(SelectArgs a, long long num_tiles) {
     using V = typename Traits<T>::V;
     using U = uint32_t;                     // counts
@@ -124,6 +133,9 @@ select_kernel(SelectArgs a, long long num_tiles) {
     constexpr int CT = kSCW * 32;
     constexpr int LB = sel_lookback_warps<PARTITION>();
     static_assert(ITEMS % VEC == 0, "ITEMS must be a multiple of the vector width");
+    // the producer sends one end marker per look-back warp, each in a stage
+    // of its own, and the compute warps hand back none after the first
+    static_assert(LB <= S, "at most one look-back warp per stage");
 
     extern __shared__ __align__(128) unsigned char smem[];
     T *vals = reinterpret_cast<T *>(smem);
@@ -435,7 +447,7 @@ static cudaError_t launch_select_variant(const SelectArgs &a, cudaStream_t s) {
         if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    long long grid = (long long)sms * kPCtasPerSm;
+    long long grid = (long long)sms * kSCtasPerSm;
     if (grid > tiles) grid = tiles;
     select_kernel<T, OP, PARTITION><<<(unsigned int)grid, sel_threads<PARTITION>(), smem, s>>>(a, tiles);
     return cudaGetLastError();
