@@ -679,7 +679,9 @@ def run_reduce_by_key(args, n: int = 1 << 25) -> dict:
     """Single-pass reduce-by-key of {int32 key, fp32 value} pairs and
     run-length encoding of the int32 keys, for several mean run lengths, GB/s
     with the algorithmic bytes: keys (and values) read + one (key, 32-bit
-    aggregate) pair written per run."""
+    aggregate) pair written per run.  The keys of 2^25 pairs are about the
+    size of L2, so L2 is flushed (a 512 MiB write) before every call and
+    each call is timed on its own; the leg reports the mean call time."""
     import torch
     from prefix_scan_gb300 import api, inputs
     dev = torch.device("cuda", 0)
@@ -690,8 +692,9 @@ def run_reduce_by_key(args, n: int = 1 << 25) -> dict:
     cnts = agg.view(torch.int32)
     nr = torch.zeros(1, dtype=torch.int64, device=dev)   # reused: no allocation or fill per call
     stream = torch.cuda.current_stream(dev)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    res = {"n": n, "keys": "int32, runs of uniform length in [1, 2L-1]", "values": "fp32 uniform [-1, 1)"}
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    res = {"n": n, "keys": "int32, runs of uniform length in [1, 2L-1]", "values": "fp32 uniform [-1, 1)",
+           "l2": "flushed before each call"}
     for mean in (1, 16, 256):
         kt = torch.from_numpy(inputs.run_keys(n, mean, 11 + mean)).to(dev)
         for name, fn in (("reduce_by_key", lambda: api.reduce_by_key(kt, vt, unique_keys=uk, aggregates=agg,
@@ -702,13 +705,15 @@ def run_reduce_by_key(args, n: int = 1 << 25) -> dict:
                 _, _, cnt = fn()
             torch.cuda.synchronize()
             m = int(cnt.item())
-            reps = max(3, min(args.steps, 20))
-            ev0.record(stream)
-            for _ in range(reps):
+            reps = max(3, min(args.steps, 40))
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+            for k in range(reps):
+                flush.fill_(k & 0xFF)   # evict the keys and values from L2
+                ev[2 * k].record(stream)
                 fn()
-            ev1.record(stream)
+                ev[2 * k + 1].record(stream)
             torch.cuda.synchronize()
-            t = ev0.elapsed_time(ev1) / 1e3 / reps
+            t = sum(ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(reps)) / 1e3 / reps
             b = n * (8 if name == "reduce_by_key" else 4) + m * 8 + 8
             res[f"{name}_L{mean}"] = {"ms": round(t * 1000, 4), "gbs": round(b / t / 1e9, 2),
                                        "gpairs_per_s": round(n / t / 1e9, 3), "runs": m,
