@@ -26,6 +26,7 @@
 // That argument needs the bulk copies, so in place requires 16-byte
 // aligned values and flags.
 #include "scan_device.cuh"
+#include "scan_cluster.cuh"
 #include "scan_pipeline.cuh"
 #include "scan_trace.cuh"
 
@@ -432,24 +433,398 @@ select_kernel(SelectArgs a, long long num_tiles) {
     if (epoch == kEpochMask) finish_call(hdr, a.ws, a.ws_bytes, epoch);
 }
 
+// ---- paired tiles -------------------------------------------------------------
+// The same operation with one look-back per two tiles: the two CTAs of a
+// cluster take tiles 2u and 2u+1 as one unit u (one claim and one
+// descriptor per unit), each copying and scanning its own tile at the same
+// time.  CTA 0 (the leader) claims the unit and passes its id to CTA 1;
+// CTA 1 passes its tile's count back; the leader publishes the unit's
+// count, looks back over the units, publishes P, and hands CTA 1 the
+// offset of its tile (the unit's offset plus the leader's count) -- all
+// through distributed shared memory, with bounded waits.  Half the
+// descriptors and look-backs per byte; CTA 1 runs none.  An odd number of
+// tiles leaves CTA 1 an empty tile in the last unit.  In place is safe as
+// before: a tile learns its offset after every earlier unit and the leader's
+// own tile have published their counts, which each does after its data sits
+// in shared memory.
+#ifndef PS_SEL_PAIR
+#define PS_SEL_PAIR 0
+#endif
+template <typename T, int OP, bool PARTITION> constexpr size_t sel_pair_smem_bytes() {
+    // unit id and its mailbox, partner's and own count, and three mbarriers
+    // per hand-off slot
+    return sel_smem_bytes<T, OP, PARTITION>() + ((size_t)sel_ring<OP, PARTITION>() * 48 + 127) / 128 * 128;
+}
+
+template <typename T, int OP, bool PARTITION>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(sel_threads<PARTITION>(), kSCtasPerSm)
+select_pair_kernel(SelectArgs a, long long num_tiles) {
+    using V = typename Traits<T>::V;
+    using U = uint32_t;                     // counts
+    constexpr int VEC = Traits<T>::VEC;
+    constexpr int ITEMS = SelItems<T>::value;
+    constexpr int ROWS = ITEMS / VEC;
+    constexpr long long TILE = sel_tile<T>();
+    constexpr int S = sel_stages<OP, PARTITION>();
+    constexpr int R = sel_ring<OP, PARTITION>();
+    constexpr uint32_t VAL_BYTES = (uint32_t)(TILE * sizeof(T));
+    constexpr uint32_t FLAG_BYTES = OP == 0 ? (uint32_t)TILE : 0u;
+    constexpr int CT = kSCW * 32;
+    constexpr int LB = sel_lookback_warps<PARTITION>();
+    static_assert(ITEMS % VEC == 0, "ITEMS must be a multiple of the vector width");
+    static_assert(LB <= S, "at most one look-back warp per stage");
+    static_assert(R % 2 == 0, "8-byte alignment of the hand-off slots");
+    const long long num_units = (num_tiles + 1) / 2;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    T *vals = reinterpret_cast<T *>(smem);
+    uint8_t *flg = smem + (size_t)S * VAL_BYTES;
+    T *pack = reinterpret_cast<T *>(smem + (size_t)S * (VAL_BYTES + FLAG_BYTES));   // partition only
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * (VAL_BYTES + FLAG_BYTES) +
+                                                  sel_pack_bytes<T, PARTITION>());
+    uint64_t *empty = full + S;
+    uint64_t *agg_done = empty + S;          // the rest: R slots, slot k % R
+    uint64_t *prefix_ready = agg_done + R;
+    long long *tile_of = reinterpret_cast<long long *>(prefix_ready + R);
+    U *agg_of = reinterpret_cast<U *>(tile_of + R);   // the leader: the unit's count
+    U *excl_of = agg_of + R;
+    long long *unit_of = reinterpret_cast<long long *>(excl_of + R);   // written by this CTA's producer
+    long long *unit_box = unit_of + R;                // CTA 1: the leader writes the unit id here
+    U *part_of = reinterpret_cast<U *>(unit_box + R); // the leader: CTA 1's count
+    U *own_of = part_of + R;                          // the leader: its own tile's count
+    uint64_t *unit_rdy = reinterpret_cast<uint64_t *>(own_of + R);   // CTA 1: unit id arrived
+    uint64_t *unit_free = unit_rdy + R;                              // leader: CTA 1 has read it
+    uint64_t *part_rdy = unit_free + R;                              // leader: CTA 1's count arrived
+    __shared__ U s_warp[2][kSCW];
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = cluster_rank();
+    Header *hdr = reinterpret_cast<Header *>(a.ws);
+    void *desc = a.ws + kHeaderBytes;
+    const unsigned long long n = a.n;
+    const T *in = reinterpret_cast<const T *>(a.in);
+    T *out = reinterpret_cast<T *>(a.out);
+    const T thr = from_raw<T>(a.threshold_bits);
+
+    __shared__ uint32_t s_epoch;
+    __shared__ int s_ok;
+    if (tid == 0) {
+        uint32_t e;
+        s_ok = begin_call(hdr, &e) ? 1 : 0;
+        s_epoch = e;
+        s_abort = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kSCW + 1);
+        }
+        for (int slot = 0; slot < R; ++slot) {
+            mbar_init(&agg_done[slot], 1);
+            mbar_init(&prefix_ready[slot], 1);
+            mbar_init(&unit_rdy[slot], 1);
+            mbar_init(&unit_free[slot], 1);
+            mbar_init(&part_rdy[slot], 1);
+            tile_of[slot] = num_tiles;
+            unit_of[slot] = num_units;
+            unit_box[slot] = num_units;
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    cluster_sync_all();   // both CTAs' barriers are ready before either arrives on the other's
+    if (!s_ok) return;    // the same verdict in both CTAs of the cluster (one header)
+    const uint32_t epoch = s_epoch;
+
+    if (warp == kSCW) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            int ends = 0;   // end markers: one per look-back warp in the leader, one in CTA 1
+            for (long long k = 0;; ++k) {
+                const int s = (int)(k % S);
+                const int slot = (int)(k % R);
+                if (k >= S && !mbar_wait(&empty[s], (uint32_t)((k / S - 1) & 1))) {
+                    report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                    break;
+                }
+                long long u;
+                if (rank == 0) {
+                    u = ends ? num_units : (long long)atomicAdd(&hdr->tile_counter, 1ull);
+                    if (ends == 0) {
+                        // CTA 1 follows the same units: pass the id on, once it
+                        // has read the one this slot held R iterations ago
+                        if (k >= R && !mbar_wait_cluster(&unit_free[slot], (uint32_t)((k / R - 1) & 1))) {
+                            report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                            break;
+                        }
+                        st_cluster_u64(cluster_addr(&unit_box[slot], 1), (unsigned long long)u);
+                        mbar_arrive_cluster(cluster_addr(&unit_rdy[slot], 1));
+                    }
+                    if (u < num_units) prefetch_descriptor<1>(desc, u);
+                } else {
+                    // the leader may refill the mailbox as soon as this
+                    // iteration has read it; the CTA's other warps read the
+                    // local copy, which only this producer writes
+                    if (!mbar_wait_cluster(&unit_rdy[slot], (uint32_t)((k / R) & 1))) {
+                        report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                        break;
+                    }
+                    u = unit_box[slot];
+                    mbar_arrive_cluster(cluster_addr(&unit_free[slot], 0));
+                }
+                unit_of[slot] = u;
+                const long long t = u < num_units ? 2 * u + (long long)rank : num_tiles;
+                tile_of[slot] = t;
+                if (a.use_bulk && t < num_tiles && (unsigned long long)(t + 1) * TILE <= n) {
+                    mbar_arrive_expect_tx(&full[s], VAL_BYTES + FLAG_BYTES);
+                    bulk_load(vals + (size_t)s * TILE, in + t * TILE, VAL_BYTES, &full[s]);
+                    if (OP == 0) bulk_load(flg + (size_t)s * TILE, a.flags + t * TILE, FLAG_BYTES, &full[s]);
+                } else {
+                    mbar_arrive(&full[s]);   // end marker, an empty tile, or one read from global
+                }
+                if (u >= num_units && (rank == 1 || ++ends == LB)) break;
+            }
+            if (epoch != kEpochMask) claims_done(hdr, a.ws_bytes, epoch);
+        }
+    } else if (warp == kSCW + 1) {
+        // ---------------- aggregator: count; the leader publishes the unit's ----------------
+        int ends = 0;
+        for (long long k = 0;; ++k) {
+            const int s = (int)(k % S);
+            if (!mbar_wait(&full[s], (uint32_t)((k / S) & 1))) {
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                break;
+            }
+            const int slot = (int)(k % R);
+            const long long u = unit_of[slot];
+            const long long tile = tile_of[slot];
+            if (u >= num_units) {   // end marker: pass it on to the look-back warps
+                if (lane == 0) mbar_arrive(&agg_done[slot]);
+                if (rank == 1 || ++ends == LB) break;
+                continue;
+            }
+            const unsigned long long base = (unsigned long long)tile * TILE;
+            U cnt = 0;
+            if (a.use_bulk && base + TILE <= n) {
+                if (OP == 0) {
+                    const uint4 *f4 = reinterpret_cast<const uint4 *>(flg + (size_t)s * TILE);
+                    U bits = 0;
+#pragma unroll 4
+                    for (int i = lane; i < (int)(TILE / 16); i += 32) {
+                        const uint4 w = f4[i];
+                        bits += __popc(__vcmpne4(w.x, 0u)) + __popc(__vcmpne4(w.y, 0u)) +
+                                __popc(__vcmpne4(w.z, 0u)) + __popc(__vcmpne4(w.w, 0u));
+                    }
+                    cnt = bits >> 3;
+                } else {
+                    const V *src = reinterpret_cast<const V *>(vals + (size_t)s * TILE);
+                    for (int i = lane; i < (int)(TILE / VEC); i += 32) {
+                        const V x = src[i];
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) cnt += keep<T, OP>(vget_t<T>(x, j), 0, thr);
+                    }
+                }
+            } else {   // a tile read from global, or CTA 1's empty tile (base >= n)
+                const unsigned long long end = base + TILE < n ? base + TILE : n;
+                for (unsigned long long i = base + lane; i < end; i += 32)
+                    cnt += keep<T, OP>(OP == 0 ? T(0) : in[i], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            const U agg = __reduce_add_sync(kFull, cnt);
+            if (lane == 0) {
+                if (rank == 1) {
+                    st_cluster_u32(cluster_addr(&part_of[slot], 0), agg);
+                    mbar_arrive_cluster(cluster_addr(&part_rdy[slot], 0));
+                } else {
+                    U pc = 0;
+                    if (mbar_wait_cluster(&part_rdy[slot], (uint32_t)((k / R) & 1)))
+                        pc = part_of[slot];
+                    else
+                        report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                    Desc<U, 1>::store(desc, u, u == 0 ? kFlagP : kFlagA, agg + pc, epoch);
+                    own_of[slot] = agg;
+                    agg_of[slot] = agg + pc;
+                    mbar_arrive(&agg_done[slot]);
+                }
+            }
+        }
+    } else if (warp >= kSCW + 2) {
+        // ---------------- look-back warps (the leader): the unit's offset ----------------
+        if (rank == 0) {
+            for (long long k = warp - (kSCW + 2);; k += LB) {
+                const int slot = (int)(k % R);
+                if (!mbar_wait(&agg_done[slot], (uint32_t)((k / R) & 1))) {
+                    report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                    break;
+                }
+                const long long u = unit_of[slot];
+                if (u >= num_units) break;
+                const U agg = agg_of[slot];
+                __syncwarp();
+                U excl = 0;
+                if (u != 0) {
+                    excl = look_back<U, 1, kLookbackK>(desc, u, epoch, a.max_polls, &hdr->status);
+                    if (lane == 0) Desc<U, 1>::store(desc, u, kFlagP, excl + agg, epoch);
+                }
+                if (lane == 0) {
+                    if (a.num_selected && u == num_units - 1) *a.num_selected = (unsigned long long)(excl + agg);
+                    excl_of[slot] = excl;
+                    mbar_arrive(&prefix_ready[slot]);
+                    // CTA 1's tile follows the leader's in the unit
+                    st_cluster_u32(cluster_addr(&excl_of[slot], 1), excl + own_of[slot]);
+                    mbar_arrive_cluster(cluster_addr(&prefix_ready[slot], 1));
+                }
+            }
+        }
+    } else {
+        // ---------------- compute warps: scan the flags, scatter ----------------
+        for (long long k = 0;; ++k) {
+            const int s = (int)(k % S);
+            if (!mbar_wait(&full[s], (uint32_t)((k / S) & 1))) {
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                abort_meet(&s_abort, 1, CT);
+                break;
+            }
+            const int slot = (int)(k % R);
+            if (unit_of[slot] >= num_units) break;
+            const long long tile = tile_of[slot];
+            const unsigned long long base = (unsigned long long)tile * TILE;
+            const bool staged = a.use_bulk && base + TILE <= n;
+            const int seg = warp * 32 * ITEMS;
+
+            T v[ROWS][VEC];
+            uint32_t sel[ROWS];
+            if (staged) {
+                const V *src = reinterpret_cast<const V *>(vals + (size_t)s * TILE + seg) + lane;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const V x = src[r * 32];
+                    uint32_t fb = 0;
+                    if (OP == 0) {
+                        const uint8_t *fp = flg + (size_t)s * TILE + seg + (r * 32 + lane) * VEC;
+                        fb = VEC == 4 ? *reinterpret_cast<const uint32_t *>(fp)
+                                      : (uint32_t)*reinterpret_cast<const uint16_t *>(fp);
+                    }
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        v[r][j] = vget_t<T>(x, j);
+                        m |= (uint32_t)keep<T, OP>(v[r][j], (uint8_t)(fb >> (8 * j)), thr) << j;
+                    }
+                    sel[r] = m;
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const unsigned long long i = base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
+                        v[r][j] = i < n ? in[i] : T(0);
+                        const bool kp = i < n && keep<T, OP>(v[r][j], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
+                        m |= (uint32_t)kp << j;
+                    }
+                    sel[r] = m;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            U off[ROWS];
+            U running = 0;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const U t = (U)__popc(sel[r]);
+                const U sc = warp_inclusive<U>(t, lane);
+                off[r] = running + (sc - t);
+                running += __shfl_sync(kFull, sc, 31);
+            }
+            U *sw = s_warp[k & 1];
+            if (lane == 0) sw[warp] = running;
+            named_barrier(1, CT);
+            if (aborted(&s_abort)) break;
+            U warp_excl = 0;
+#pragma unroll
+            for (int w = 0; w < kSCW; ++w)
+                if (w < warp) warp_excl += sw[w];
+            if (!mbar_wait_cluster(&prefix_ready[slot], (uint32_t)((k / R) & 1)))
+                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+            const U tile_excl = excl_of[slot];
+
+            if (!PARTITION) {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const U before = tile_excl + warp_excl + off[r];
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        if ((sel[r] >> j) & 1u) out[before + (U)__popc(sel[r] & ((1u << j) - 1u))] = v[r][j];
+                }
+            } else {
+                T *wbuf = pack + seg;
+                const U w_sel = running;
+                const unsigned long long w_first = base + seg;
+                const U w_valid = w_first >= n ? 0u
+                                  : (n - w_first >= (unsigned long long)(32 * ITEMS) ? (U)(32 * ITEMS)
+                                                                                    : (U)(n - w_first));
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    U c = off[r];
+                    const U e0 = (U)((r * 32 + lane) * VEC);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const U e = e0 + (U)j;
+                        const bool kp = (sel[r] >> j) & 1u;
+                        const U pos = kp ? c : w_sel + (e - c);
+                        if (kp || e < w_valid) wbuf[pos] = v[r][j];
+                        c += kp ? 1u : 0u;
+                    }
+                }
+                __syncwarp();
+                const U dst = tile_excl + warp_excl;
+                for (U q = lane; q < w_sel; q += 32) out[dst + q] = wbuf[q];
+                const unsigned long long rej_before = w_first - dst;
+                const U w_rej = w_valid - w_sel;
+                for (U q = lane; q < w_rej; q += 32) out[n - 1 - (rej_before + q)] = wbuf[w_sel + q];
+                __syncwarp();
+            }
+        }
+    }
+
+    // no CTA leaves while its partner may still write to its shared memory
+    cluster_sync_all();
+    if (epoch == kEpochMask) finish_call(hdr, a.ws, a.ws_bytes, epoch);
+}
+
 template <typename T, int OP, bool PARTITION>
 static cudaError_t launch_select_variant(const SelectArgs &a, cudaStream_t s) {
-    constexpr size_t smem = sel_smem_bytes<T, OP, PARTITION>();
+    constexpr bool kPair = PS_SEL_PAIR != 0;
+    constexpr size_t smem = kPair ? sel_pair_smem_bytes<T, OP, PARTITION>() : sel_smem_bytes<T, OP, PARTITION>();
     const long long tiles = (long long)((a.n + sel_tile<T>() - 1) / sel_tile<T>());
     static volatile int configured[64] = {};
     int dev = 0, sms = 0;
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(select_kernel<T, OP, PARTITION>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if constexpr (kPair)
+            e = cudaFuncSetAttribute(select_pair_kernel<T, OP, PARTITION>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        else
+            e = cudaFuncSetAttribute(select_kernel<T, OP, PARTITION>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     long long grid = (long long)sms * kSCtasPerSm;
-    if (grid > tiles) grid = tiles;
-    select_kernel<T, OP, PARTITION><<<(unsigned int)grid, sel_threads<PARTITION>(), smem, s>>>(a, tiles);
+    if constexpr (kPair) {
+        // clusters of two CTAs, one per unit of two tiles
+        const long long units = (tiles + 1) / 2;
+        if (grid > 2 * units) grid = 2 * units;
+        grid &= ~1ll;
+        select_pair_kernel<T, OP, PARTITION><<<(unsigned int)grid, sel_threads<PARTITION>(), smem, s>>>(a, tiles);
+    } else {
+        if (grid > tiles) grid = tiles;
+        select_kernel<T, OP, PARTITION><<<(unsigned int)grid, sel_threads<PARTITION>(), smem, s>>>(a, tiles);
+    }
     return cudaGetLastError();
 }
 
