@@ -28,7 +28,9 @@
 // and publish it (A; P for tile 0) themselves, and pack the tile's runs in
 // order into an output buffer -- each head's key and the value of the run it
 // closes, summed within the tile -- after which the stage goes back to the
-// producer.  Only the run closed by the tile's first head reaches back
+// producer.  The walk over each lane's chunk that precedes the scan leaves
+// each head's closing value in the warp's slice of the stage, so the pack
+// visits the heads only.  Only the run closed by the tile's first head reaches back
 // before the tile; its packed value lacks the value the tile's exclusive
 // pair carries.  Look-back warps resolve that pair; a writer warp adds its
 // value to the first run and writes the buffer out as contiguous ranges,
@@ -254,7 +256,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
         s_abort = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);   // the compute warps, once the tile needs the stage no more
+            mbar_init(&empty[s], kRCW);   // each compute warp, once it needs the stage no more
         }
         for (int o = 0; o < NOB; ++o) mbar_init(&ob_empty[o], 1);   // the writer
         for (int slot = 0; slot < R; ++slot) {
@@ -462,10 +464,17 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             if (warp == 0 && lane == 0) PS_TRACE_POINT(pend_tile, PS_TRACE_PREFIX_RECEIVED);
             const P pre = Op::combine(excl_of[pslot], pend_wex);
             const uint32_t cw = pair_count(pre), pv = pair_value(pre);
-            // the warp's keys and values again, all of them before the slice is reused
+            // the warp's keys again, and the closing values its pass left in
+            // the slice, all of them before the slice is reused (the values
+            // loaded beside the keys are not used)
             KU kp[ROWS][EPL];
-            uint32_t vp[ROWS][EPL], hp[ROWS];
+            uint32_t vp[ROWS][EPL], hp[ROWS], cl[ROWS][EPL];
             load_rows(ps, pend_tile, pbase, pstaged, kp, vp, hp);
+            const uint32_t *pcl = stage_vals(ps) + seg;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) cl[r][j] = pcl[(r * EPL + j) * 32 + lane];
             __syncwarp();
             KU *pk = stage_keys(ps) + seg;
             uint32_t *pvals = stage_vals(ps) + seg;
@@ -473,17 +482,17 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             for (int r = 0; r < ROWS; ++r) {
                 const uint32_t m = pend_info[r] & 0xffu, offc = pend_info[r] >> 8;
                 uint32_t q = offc;   // run index - cw of this chunk's first head
-                uint32_t v = offc ? pend_offv[r] : RunValue<VU>::add(pv, pend_offv[r]);
+                // the open run's value where the chunk starts
+                const uint32_t vin = offc ? pend_offv[r] : RunValue<VU>::add(pv, pend_offv[r]);
+                bool first = true;
 #pragma unroll
                 for (int j = 0; j < EPL; ++j) {
-                    const bool h = (m >> j) & 1u;
-                    if (h) {
+                    if ((m >> j) & 1u) {
                         pk[rbk_sw(q)] = kp[r][j];
-                        pvals[rbk_sw(q)] = v;
+                        pvals[rbk_sw(q)] = first ? RunValue<VU>::add(vin, cl[r][j]) : cl[r][j];
+                        first = false;
+                        ++q;
                     }
-                    const uint32_t sum = RunValue<VU>::add(v, vp[r][j]);
-                    v = h ? vp[r][j] : sum;
-                    q += h ? 1u : 0u;
                 }
             }
             __syncwarp();
@@ -491,10 +500,10 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 ukeys[cw + q] = pk[rbk_sw(q)];
                 if (cw + q > 0u) aggs[cw + q - 1u] = pvals[rbk_sw(q)];
             }
-            // the stage goes back once every warp has written from its slice
-            named_barrier(2, CT);
-            if (warp == 0 && lane == 0) {
-                PS_TRACE_POINT(pend_tile, PS_TRACE_STORED);
+            // this warp is done with the stage
+            __syncwarp();
+            if (lane == 0) {
+                if (warp == 0) PS_TRACE_POINT(pend_tile, PS_TRACE_STORED);
                 mbar_arrive(&empty[ps]);
             }
             pend = false;
@@ -544,6 +553,13 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             // partial from lane l-d joins only while l-d lies in it.
             uint32_t offc[ROWS], offv[ROWS];   // exclusive pair of the chunk within the warp
             uint32_t rc = 0u, rv = 0u;         // pair of the warp's rows so far
+            // Each head's closing value -- the value of the run it closes,
+            // summed from the chunk's start at most -- goes to the warp's
+            // slice of the stage's values, entry (r * EPL + j) * 32 + lane
+            // (consecutive lanes, consecutive words): the pack then visits
+            // the heads only.  The warp's values are all in registers first.
+            uint32_t *cls = stage_vals(s) + seg;
+            __syncwarp();
             {
                 uint32_t cc[ROWS], cv[ROWS], cnt[ROWS];
                 int seg_lo[ROWS];
@@ -553,6 +569,7 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
 #pragma unroll
                     for (int j = 0; j < EPL; ++j) {
                         const bool h = (hm[r] >> j) & 1u;
+                        if (h) cls[(r * EPL + j) * 32 + lane] = v;
                         const uint32_t sum = RunValue<VU>::add(v, vv[r][j]);
                         v = h ? vv[r][j] : sum;
                     }
@@ -605,15 +622,12 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
             if (warp == 0) wex = 0;
             const bool sparse = pair_count(agg) <= (uint32_t)CAP;
             if (warp == 0 && lane == 0) {
-                // A at once (P for tile 0, whose exclusive pair is empty); a
-                // sparse tile's elements are all in registers, so its stage
-                // goes back now, before the pair of the tile is known
+                // A at once (P for tile 0, whose exclusive pair is empty)
                 Desc<P, 2>::store(desc, tile, tile == 0 ? kFlagP : kFlagA, agg, epoch);
                 PS_TRACE_POINT(tile, PS_TRACE_AGGREGATE);
                 agg_of[slot] = agg;
                 sparse_of[slot] = sparse ? 1 : 0;
                 mbar_arrive(&agg_done[slot]);
-                if (sparse) mbar_arrive(&empty[s]);
             }
             if (sparse) {
                 // pack the runs in the iteration's output buffer, once the
@@ -629,24 +643,27 @@ reduce_by_key_kernel(RbkArgs a, long long num_tiles) {
                 KU *ok = out_keys(o);
                 uint32_t *ov = out_vals(o);
                 const uint32_t wq0 = pair_count(wex), wv0 = pair_value(wex);
+                const KU *ks = stage_keys(s);
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
                     uint32_t q = wq0 + offc[r];
-                    uint32_t v = offc[r] ? offv[r] : RunValue<VU>::add(wv0, offv[r]);
-#pragma unroll
-                    for (int j = 0; j < EPL; ++j) {
-                        const bool h = (hm[r] >> j) & 1u;
-                        if (h) {
-                            ok[rbk_sw(q)] = kk[r][j];
-                            ov[rbk_sw(q)] = v;
-                        }
-                        const uint32_t sum = RunValue<VU>::add(v, vv[r][j]);
-                        v = h ? vv[r][j] : sum;
-                        q += h ? 1u : 0u;
+                    // the open run's value where the chunk starts: the chunk's
+                    // first head adds it to its closing value
+                    uint32_t vin = offc[r] ? offv[r] : RunValue<VU>::add(wv0, offv[r]);
+                    const uint32_t e0 = (uint32_t)(seg + (r * 32 + lane) * EPL);
+                    for (uint32_t mm = hm[r]; mm; mm &= mm - 1u) {
+                        const uint32_t j = (uint32_t)(__ffs(mm) - 1);
+                        ok[rbk_sw(q)] = staged ? ks[e0 + j] : keys[base + e0 + j];
+                        ov[rbk_sw(q)] = RunValue<VU>::add(vin, cls[((uint32_t)r * EPL + j) * 32 + lane]);
+                        vin = 0u;   // later heads' runs begin inside the chunk
+                        ++q;
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&packed[slot]);
+                if (lane == 0) {
+                    mbar_arrive(&packed[slot]);
+                    mbar_arrive(&empty[s]);   // this warp is done with the stage
+                }
             } else {
                 // a dense tile: nothing for the writer (it only frees the
                 // buffer); the compute warps write it after the next tile's
