@@ -115,17 +115,194 @@ template <> __device__ __forceinline__ int32_t vget_t<int32_t>(const uint4 &v, i
 template <> __device__ __forceinline__ float vget_t<float>(const float4 &v, int j) { return vget(v, j); }
 template <> __device__ __forceinline__ int64_t vget_t<int64_t>(const ulonglong2 &v, int j) { return (int64_t)vget(v, j); }
 
+// The lane's part of a tile's kept count (the aggregator warp sums the
+// lanes'): from the stage when the tile was bulk-copied, else from global
+// memory with bounds (a tile cut by the end of the array, or past it).
+template <typename T, int OP>
+__device__ __forceinline__ uint32_t count_tile(const SelectArgs &a, T thr, const T *vals_s, const uint8_t *flg_s,
+                                               unsigned long long base, int lane) {
+    using V = typename Traits<T>::V;
+    constexpr int VEC = Traits<T>::VEC;
+    constexpr long long TILE = sel_tile<T>();
+    const unsigned long long n = a.n;
+    const T *in = reinterpret_cast<const T *>(a.in);
+    uint32_t cnt = 0;
+    if (a.use_bulk && base + TILE <= n) {
+        if (OP == 0) {
+            // __vcmpne4 sets a byte to 0xff where the flag byte is nonzero:
+            // eight set bits per kept element
+            const uint4 *f4 = reinterpret_cast<const uint4 *>(flg_s);
+            uint32_t bits = 0;
+#pragma unroll 4
+            for (int i = lane; i < (int)(TILE / 16); i += 32) {
+                const uint4 w = f4[i];
+                bits += __popc(__vcmpne4(w.x, 0u)) + __popc(__vcmpne4(w.y, 0u)) +
+                        __popc(__vcmpne4(w.z, 0u)) + __popc(__vcmpne4(w.w, 0u));
+            }
+            cnt = bits >> 3;
+        } else {
+            const V *src = reinterpret_cast<const V *>(vals_s);
+            for (int i = lane; i < (int)(TILE / VEC); i += 32) {
+                const V x = src[i];
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) cnt += keep<T, OP>(vget_t<T>(x, j), 0, thr);
+            }
+        }
+    } else {
+        const unsigned long long end = base + TILE < n ? base + TILE : n;
+        for (unsigned long long i = base + lane; i < end; i += 32)
+            cnt += keep<T, OP>(OP == 0 ? T(0) : in[i], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
+    }
+    return cnt;
+}
+
+// One tile's pass by the compute warps: the values (and flags) into
+// registers, the stage back to the producer (it is not read again), the
+// kept elements counted within each warp and across the warps, then -- once
+// wait_prefix() has the tile's output offset -- the scatter.  Select writes
+// each warp row's kept elements, one contiguous run, straight from the
+// registers; partition packs each warp's kept elements and then its
+// rejected ones into the warp's slice of the pack buffer and writes them as
+// two contiguous runs (the rejected one downwards from the end of `out`).
+// False when the compute warps' abort flag is up (a wait ran out).
+template <typename T, int OP, bool PARTITION, typename WaitPrefix>
+__device__ __forceinline__ bool select_tile_pass(const SelectArgs &a, T thr, long long tile, const T *vals_s,
+                                                 const uint8_t *flg_s, T *pack, uint64_t *empty_s, uint32_t *sw,
+                                                 volatile int *abort_flag, WaitPrefix wait_prefix) {
+    using V = typename Traits<T>::V;
+    using U = uint32_t;
+    constexpr int VEC = Traits<T>::VEC;
+    constexpr int ITEMS = SelItems<T>::value;
+    constexpr int ROWS = ITEMS / VEC;
+    constexpr long long TILE = sel_tile<T>();
+    constexpr int CT = kSCW * 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned long long n = a.n;
+    const T *in = reinterpret_cast<const T *>(a.in);
+    T *out = reinterpret_cast<T *>(a.out);
+    const unsigned long long base = (unsigned long long)tile * TILE;
+    const bool staged = a.use_bulk && base + TILE <= n;
+    const int seg = warp * 32 * ITEMS;
+    if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
+
+    T v[ROWS][VEC];
+    uint32_t sel[ROWS];   // bit j: element j of this lane's row chunk is kept
+    if (staged) {
+        const V *src = reinterpret_cast<const V *>(vals_s + seg) + lane;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const V x = src[r * 32];
+            uint32_t fb = 0;
+            if (OP == 0) {
+                const uint8_t *fp = flg_s + seg + (r * 32 + lane) * VEC;
+                fb = VEC == 4 ? *reinterpret_cast<const uint32_t *>(fp)
+                              : (uint32_t)*reinterpret_cast<const uint16_t *>(fp);
+            }
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                v[r][j] = vget_t<T>(x, j);
+                m |= (uint32_t)keep<T, OP>(v[r][j], (uint8_t)(fb >> (8 * j)), thr) << j;
+            }
+            sel[r] = m;
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const unsigned long long i = base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
+                v[r][j] = i < n ? in[i] : T(0);
+                const bool kp = i < n && keep<T, OP>(v[r][j], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
+                m |= (uint32_t)kp << j;
+            }
+            sel[r] = m;
+        }
+    }
+
+    // the tile is in registers and the stage is not read again: it goes
+    // back to the producer now, before the offset arrives (the hand-off ring
+    // keeps the slots apart)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_s);
+    // exclusive count of kept elements before each lane's row chunk
+    U off[ROWS];
+    U running = 0;
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const U t = (U)__popc(sel[r]);
+        const U sc = warp_inclusive<U>(t, lane);
+        off[r] = running + (sc - t);
+        running += __shfl_sync(kFull, sc, 31);
+    }
+    if (lane == 0) sw[warp] = running;
+    named_barrier(1, CT);
+    if (aborted(abort_flag)) return false;
+    U warp_excl = 0;
+#pragma unroll
+    for (int w = 0; w < kSCW; ++w)
+        if (w < warp) warp_excl += sw[w];
+    const U tile_excl = wait_prefix();
+    if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
+
+    if (!PARTITION) {
+        // select: kept elements straight to their places; within a warp row
+        // they form one contiguous run
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const U before = tile_excl + warp_excl + off[r];
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                if ((sel[r] >> j) & 1u) out[before + (U)__popc(sel[r] & ((1u << j) - 1u))] = v[r][j];
+        }
+    } else {
+        // partition: each warp packs its kept elements, then its rejected
+        // ones, into its own slice of the pack buffer and writes them as two
+        // contiguous runs, consecutive lanes to consecutive addresses
+        T *wbuf = pack + seg;
+        const U w_sel = running;   // kept elements of this warp
+        const unsigned long long w_first = base + seg;
+        const U w_valid = w_first >= n ? 0u
+                          : (n - w_first >= (unsigned long long)(32 * ITEMS) ? (U)(32 * ITEMS)
+                                                                            : (U)(n - w_first));
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            // c: kept elements of the warp before element e (a running count
+            // over the chunk); a rejected element goes after the warp's kept
+            // ones, at its count of rejected predecessors
+            U c = off[r];
+            const U e0 = (U)((r * 32 + lane) * VEC);   // index within the warp's slice
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const U e = e0 + (U)j;
+                const bool kp = (sel[r] >> j) & 1u;
+                const U pos = kp ? c : w_sel + (e - c);
+                if (kp || e < w_valid) wbuf[pos] = v[r][j];
+                c += kp ? 1u : 0u;
+            }
+        }
+        __syncwarp();
+        const U dst = tile_excl + warp_excl;   // kept elements before this warp
+        for (U q = lane; q < w_sel; q += 32) out[dst + q] = wbuf[q];
+        const unsigned long long rej_before = w_first - dst;   // rejected before this warp
+        const U w_rej = w_valid - w_sel;
+        for (U q = lane; q < w_rej; q += 32) out[n - 1 - (rej_before + q)] = wbuf[w_sel + q];
+        __syncwarp();   // the slice is packed again next iteration
+    }
+    if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_STORED);
+    return true;
+}
+
 }  // namespace
 
 
 template <typename T, int OP, bool PARTITION>
 __global__ void __launch_bounds__(sel_threads<PARTITION>(), kSCtasPerSm)
 select_kernel(SelectArgs a, long long num_tiles) {
-    using V = typename Traits<T>::V;
     using U = uint32_t;                     // counts
     constexpr int VEC = Traits<T>::VEC;
     constexpr int ITEMS = SelItems<T>::value;
-    constexpr int ROWS = ITEMS / VEC;
     constexpr long long TILE = sel_tile<T>();
     constexpr int S = sel_stages<OP, PARTITION>();
     constexpr int R = sel_ring<OP, PARTITION>();
@@ -158,7 +335,6 @@ select_kernel(SelectArgs a, long long num_tiles) {
     void *desc = a.ws + kHeaderBytes;
     const unsigned long long n = a.n;
     const T *in = reinterpret_cast<const T *>(a.in);
-    T *out = reinterpret_cast<T *>(a.out);
     const T thr = from_raw<T>(a.threshold_bits);
 
     // thread 0 alone reads the header (one request per CTA to its line)
@@ -231,34 +407,8 @@ select_kernel(SelectArgs a, long long num_tiles) {
                 continue;
             }
             if (lane == 0) PS_TRACE_POINT(tile, PS_TRACE_DATA);
-            const unsigned long long base = (unsigned long long)tile * TILE;
-            U cnt = 0;
-            if (a.use_bulk && base + TILE <= n) {
-                if (OP == 0) {
-                    // __vcmpne4 sets a byte to 0xff where the flag byte is
-                    // nonzero: eight set bits per kept element
-                    const uint4 *f4 = reinterpret_cast<const uint4 *>(flg + (size_t)s * TILE);
-                    U bits = 0;
-#pragma unroll 4
-                    for (int i = lane; i < (int)(TILE / 16); i += 32) {
-                        const uint4 w = f4[i];
-                        bits += __popc(__vcmpne4(w.x, 0u)) + __popc(__vcmpne4(w.y, 0u)) +
-                                __popc(__vcmpne4(w.z, 0u)) + __popc(__vcmpne4(w.w, 0u));
-                    }
-                    cnt = bits >> 3;
-                } else {
-                    const V *src = reinterpret_cast<const V *>(vals + (size_t)s * TILE);
-                    for (int i = lane; i < (int)(TILE / VEC); i += 32) {
-                        const V x = src[i];
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) cnt += keep<T, OP>(vget_t<T>(x, j), 0, thr);
-                    }
-                }
-            } else {
-                const unsigned long long end = base + TILE < n ? base + TILE : n;
-                for (unsigned long long i = base + lane; i < end; i += 32)
-                    cnt += keep<T, OP>(OP == 0 ? T(0) : in[i], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
-            }
+            const U cnt = count_tile<T, OP>(a, thr, vals + (size_t)s * TILE, flg + (size_t)s * TILE,
+                                            (unsigned long long)tile * TILE, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             const U agg = __reduce_add_sync(kFull, cnt);
@@ -308,122 +458,14 @@ select_kernel(SelectArgs a, long long num_tiles) {
             const int slot = (int)(k % R);
             const long long tile = tile_of[slot];
             if (tile < 0 || tile >= num_tiles) break;
-            const unsigned long long base = (unsigned long long)tile * TILE;
-            const bool staged = a.use_bulk && base + TILE <= n;
-            const int seg = warp * 32 * ITEMS;
-            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_COMPUTE_START);
-
-            T v[ROWS][VEC];
-            uint32_t sel[ROWS];   // bit j: element j of this lane's row chunk is kept
-            if (staged) {
-                const V *src = reinterpret_cast<const V *>(vals + (size_t)s * TILE + seg) + lane;
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    const V x = src[r * 32];
-                    uint32_t fb = 0;
-                    if (OP == 0) {
-                        const uint8_t *fp = flg + (size_t)s * TILE + seg + (r * 32 + lane) * VEC;
-                        fb = VEC == 4 ? *reinterpret_cast<const uint32_t *>(fp)
-                                      : (uint32_t)*reinterpret_cast<const uint16_t *>(fp);
-                    }
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        v[r][j] = vget_t<T>(x, j);
-                        m |= (uint32_t)keep<T, OP>(v[r][j], (uint8_t)(fb >> (8 * j)), thr) << j;
-                    }
-                    sel[r] = m;
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const unsigned long long i = base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
-                        v[r][j] = i < n ? in[i] : T(0);
-                        const bool kp = i < n && keep<T, OP>(v[r][j], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
-                        m |= (uint32_t)kp << j;
-                    }
-                    sel[r] = m;
-                }
-            }
-
-            // the tile is in registers and the stage is not read again: it
-            // goes back to the producer now, before the offset arrives (the
-            // hand-off ring keeps the slots apart)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            // exclusive count of kept elements before each lane's row chunk
-            U off[ROWS];
-            U running = 0;
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                const U t = (U)__popc(sel[r]);
-                const U sc = warp_inclusive<U>(t, lane);
-                off[r] = running + (sc - t);
-                running += __shfl_sync(kFull, sc, 31);
-            }
-            U *sw = s_warp[k & 1];
-            if (lane == 0) sw[warp] = running;
-            named_barrier(1, CT);
-            if (aborted(&s_abort)) break;
-            U warp_excl = 0;
-#pragma unroll
-            for (int w = 0; w < kSCW; ++w)
-                if (w < warp) warp_excl += sw[w];
-            if (!mbar_wait(&prefix_ready[slot], (uint32_t)((k / R) & 1)))
-                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
-            const U tile_excl = excl_of[slot];
-            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_PREFIX_RECEIVED);
-
-            if (!PARTITION) {
-                // select: kept elements straight to their places; within a
-                // warp row they form one contiguous run
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    const U before = tile_excl + warp_excl + off[r];
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        if ((sel[r] >> j) & 1u) out[before + (U)__popc(sel[r] & ((1u << j) - 1u))] = v[r][j];
-                }
-            } else {
-                // partition: each warp packs its kept elements, then its
-                // rejected ones, into its own slice of the pack buffer and
-                // writes them as two contiguous runs, consecutive lanes to
-                // consecutive addresses (the rejected run downwards from the
-                // end of `out`).
-                T *wbuf = pack + seg;
-                const U w_sel = running;   // kept elements of this warp
-                const unsigned long long w_first = base + seg;
-                const U w_valid = w_first >= n ? 0u
-                                  : (n - w_first >= (unsigned long long)(32 * ITEMS) ? (U)(32 * ITEMS)
-                                                                                    : (U)(n - w_first));
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    // c: kept elements of the warp before element e (a running
-                    // count over the chunk); a rejected element goes after the
-                    // warp's kept ones, at its count of rejected predecessors
-                    U c = off[r];
-                    const U e0 = (U)((r * 32 + lane) * VEC);   // index within the warp's slice
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const U e = e0 + (U)j;
-                        const bool kp = (sel[r] >> j) & 1u;
-                        const U pos = kp ? c : w_sel + (e - c);
-                        if (kp || e < w_valid) wbuf[pos] = v[r][j];
-                        c += kp ? 1u : 0u;
-                    }
-                }
-                __syncwarp();
-                const U dst = tile_excl + warp_excl;   // kept elements before this warp
-                for (U q = lane; q < w_sel; q += 32) out[dst + q] = wbuf[q];
-                const unsigned long long rej_before = w_first - dst;   // rejected before this warp
-                const U w_rej = w_valid - w_sel;
-                for (U q = lane; q < w_rej; q += 32) out[n - 1 - (rej_before + q)] = wbuf[w_sel + q];
-                __syncwarp();   // the slice is packed again next iteration
-            }
-            if (warp == 0 && lane == 0) PS_TRACE_POINT(tile, PS_TRACE_STORED);
+            const auto wait_prefix = [&]() -> U {
+                if (!mbar_wait(&prefix_ready[slot], (uint32_t)((k / R) & 1)))
+                    report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                return excl_of[slot];
+            };
+            if (!select_tile_pass<T, OP, PARTITION>(a, thr, tile, vals + (size_t)s * TILE, flg + (size_t)s * TILE,
+                                                    pack, &empty[s], s_warp[k & 1], &s_abort, wait_prefix))
+                break;
         }
         if (warp == 0 && lane == 0) PS_TRACE_CTA_POINT(PS_TRACE_CTA_DONE);
     }
@@ -459,11 +501,9 @@ template <typename T, int OP, bool PARTITION> constexpr size_t sel_pair_smem_byt
 template <typename T, int OP, bool PARTITION>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(sel_threads<PARTITION>(), kSCtasPerSm)
 select_pair_kernel(SelectArgs a, long long num_tiles) {
-    using V = typename Traits<T>::V;
     using U = uint32_t;                     // counts
     constexpr int VEC = Traits<T>::VEC;
     constexpr int ITEMS = SelItems<T>::value;
-    constexpr int ROWS = ITEMS / VEC;
     constexpr long long TILE = sel_tile<T>();
     constexpr int S = sel_stages<OP, PARTITION>();
     constexpr int R = sel_ring<OP, PARTITION>();
@@ -504,7 +544,6 @@ select_pair_kernel(SelectArgs a, long long num_tiles) {
     void *desc = a.ws + kHeaderBytes;
     const unsigned long long n = a.n;
     const T *in = reinterpret_cast<const T *>(a.in);
-    T *out = reinterpret_cast<T *>(a.out);
     const T thr = from_raw<T>(a.threshold_bits);
 
     __shared__ uint32_t s_epoch;
@@ -602,32 +641,9 @@ select_pair_kernel(SelectArgs a, long long num_tiles) {
                 if (rank == 1 || ++ends == LB) break;
                 continue;
             }
-            const unsigned long long base = (unsigned long long)tile * TILE;
-            U cnt = 0;
-            if (a.use_bulk && base + TILE <= n) {
-                if (OP == 0) {
-                    const uint4 *f4 = reinterpret_cast<const uint4 *>(flg + (size_t)s * TILE);
-                    U bits = 0;
-#pragma unroll 4
-                    for (int i = lane; i < (int)(TILE / 16); i += 32) {
-                        const uint4 w = f4[i];
-                        bits += __popc(__vcmpne4(w.x, 0u)) + __popc(__vcmpne4(w.y, 0u)) +
-                                __popc(__vcmpne4(w.z, 0u)) + __popc(__vcmpne4(w.w, 0u));
-                    }
-                    cnt = bits >> 3;
-                } else {
-                    const V *src = reinterpret_cast<const V *>(vals + (size_t)s * TILE);
-                    for (int i = lane; i < (int)(TILE / VEC); i += 32) {
-                        const V x = src[i];
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) cnt += keep<T, OP>(vget_t<T>(x, j), 0, thr);
-                    }
-                }
-            } else {   // a tile read from global, or CTA 1's empty tile (base >= n)
-                const unsigned long long end = base + TILE < n ? base + TILE : n;
-                for (unsigned long long i = base + lane; i < end; i += 32)
-                    cnt += keep<T, OP>(OP == 0 ? T(0) : in[i], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
-            }
+            // CTA 1's empty tile (past the array) counts nothing
+            const U cnt = count_tile<T, OP>(a, thr, vals + (size_t)s * TILE, flg + (size_t)s * TILE,
+                                            (unsigned long long)tile * TILE, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             const U agg = __reduce_add_sync(kFull, cnt);
@@ -687,105 +703,16 @@ select_pair_kernel(SelectArgs a, long long num_tiles) {
             }
             const int slot = (int)(k % R);
             if (unit_of[slot] >= num_units) break;
-            const long long tile = tile_of[slot];
-            const unsigned long long base = (unsigned long long)tile * TILE;
-            const bool staged = a.use_bulk && base + TILE <= n;
-            const int seg = warp * 32 * ITEMS;
-
-            T v[ROWS][VEC];
-            uint32_t sel[ROWS];
-            if (staged) {
-                const V *src = reinterpret_cast<const V *>(vals + (size_t)s * TILE + seg) + lane;
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    const V x = src[r * 32];
-                    uint32_t fb = 0;
-                    if (OP == 0) {
-                        const uint8_t *fp = flg + (size_t)s * TILE + seg + (r * 32 + lane) * VEC;
-                        fb = VEC == 4 ? *reinterpret_cast<const uint32_t *>(fp)
-                                      : (uint32_t)*reinterpret_cast<const uint16_t *>(fp);
-                    }
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        v[r][j] = vget_t<T>(x, j);
-                        m |= (uint32_t)keep<T, OP>(v[r][j], (uint8_t)(fb >> (8 * j)), thr) << j;
-                    }
-                    sel[r] = m;
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const unsigned long long i = base + seg + (unsigned long long)(r * 32 + lane) * VEC + j;
-                        v[r][j] = i < n ? in[i] : T(0);
-                        const bool kp = i < n && keep<T, OP>(v[r][j], OP == 0 ? a.flags[i] : (uint8_t)0, thr);
-                        m |= (uint32_t)kp << j;
-                    }
-                    sel[r] = m;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            U off[ROWS];
-            U running = 0;
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                const U t = (U)__popc(sel[r]);
-                const U sc = warp_inclusive<U>(t, lane);
-                off[r] = running + (sc - t);
-                running += __shfl_sync(kFull, sc, 31);
-            }
-            U *sw = s_warp[k & 1];
-            if (lane == 0) sw[warp] = running;
-            named_barrier(1, CT);
-            if (aborted(&s_abort)) break;
-            U warp_excl = 0;
-#pragma unroll
-            for (int w = 0; w < kSCW; ++w)
-                if (w < warp) warp_excl += sw[w];
-            if (!mbar_wait_cluster(&prefix_ready[slot], (uint32_t)((k / R) & 1)))
-                report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
-            const U tile_excl = excl_of[slot];
-
-            if (!PARTITION) {
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    const U before = tile_excl + warp_excl + off[r];
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        if ((sel[r] >> j) & 1u) out[before + (U)__popc(sel[r] & ((1u << j) - 1u))] = v[r][j];
-                }
-            } else {
-                T *wbuf = pack + seg;
-                const U w_sel = running;
-                const unsigned long long w_first = base + seg;
-                const U w_valid = w_first >= n ? 0u
-                                  : (n - w_first >= (unsigned long long)(32 * ITEMS) ? (U)(32 * ITEMS)
-                                                                                    : (U)(n - w_first));
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    U c = off[r];
-                    const U e0 = (U)((r * 32 + lane) * VEC);
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const U e = e0 + (U)j;
-                        const bool kp = (sel[r] >> j) & 1u;
-                        const U pos = kp ? c : w_sel + (e - c);
-                        if (kp || e < w_valid) wbuf[pos] = v[r][j];
-                        c += kp ? 1u : 0u;
-                    }
-                }
-                __syncwarp();
-                const U dst = tile_excl + warp_excl;
-                for (U q = lane; q < w_sel; q += 32) out[dst + q] = wbuf[q];
-                const unsigned long long rej_before = w_first - dst;
-                const U w_rej = w_valid - w_sel;
-                for (U q = lane; q < w_rej; q += 32) out[n - 1 - (rej_before + q)] = wbuf[w_sel + q];
-                __syncwarp();
-            }
+            // CTA 1's offset comes from the leader: acquire at cluster scope
+            const auto wait_prefix = [&]() -> U {
+                if (!mbar_wait_cluster(&prefix_ready[slot], (uint32_t)((k / R) & 1)))
+                    report_error(&hdr->status, epoch, PS_ERR_LOOKBACK_TIMEOUT);
+                return excl_of[slot];
+            };
+            if (!select_tile_pass<T, OP, PARTITION>(a, thr, tile_of[slot], vals + (size_t)s * TILE,
+                                                    flg + (size_t)s * TILE, pack, &empty[s], s_warp[k & 1],
+                                                    &s_abort, wait_prefix))
+                break;
         }
     }
 
