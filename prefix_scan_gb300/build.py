@@ -85,13 +85,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 # Smallest tile geometry the scan and select kernels accept: four elements
 # per thread, so tiles of 1024 elements (256 threads) for every element
 # type -- eight times as many tiles, look-backs and descriptor hand-offs per
-# byte as the product build.  The reduce-by-key and run-length kernels keep
-# their own fixed tiles.  The look-back reads two descriptors per lane (a
-# window of 64 tiles), so this build also runs the multi-descriptor window
-# fold, which must keep sequence order for the non-commutative operators.
-# The allocation-free entry point is left out: its fixed scratch is sized
-# for the product geometry.
-TINY_TILE_DEFINES = {"PS_ITEMS32": 4, "PS_ITEMS64": 4, "PS_LOOKBACK_K": 2}
+# byte as the product build.  Run-length encoding runs four compute warps,
+# so 16 KiB tiles (four times as many as the product's 64 KiB; the
+# workspace holds a descriptor per 4096 keys, so no smaller); reduce-by-key
+# keeps its tiles.  The look-back reads two descriptors per lane (a window
+# of 64 tiles), so this build also runs the multi-descriptor window fold,
+# which must keep sequence order for the non-commutative operators.  The
+# allocation-free entry point is left out: its fixed scratch is sized for
+# the product geometry.
+TINY_TILE_DEFINES = {"PS_ITEMS32": 4, "PS_ITEMS64": 4, "PS_LOOKBACK_K": 2, "PS_RLE_COMPUTE_WARPS": 4}
 
 
 def build_variant(name: str, defines: dict[str, int], exclude: tuple[str, ...] = ("scan_noalloc.cu",),

@@ -1,5 +1,5 @@
-"""Scans, pair scans, select and reduce-by-key from a tiny-tile build of the
-library.
+"""Scans, pair scans, select, reduce-by-key and run-length encoding from a
+tiny-tile build of the library.
 
 A second copy of the library is built with the smallest tile geometry the
 scan and select kernels accept (four elements per thread: tiles of 1024
@@ -191,3 +191,29 @@ def test_reduce_by_key_repeated(tiny):
         assert int(nr.item()) == m, k
         assert torch.equal(uk[:m], rk) and torch.equal(ag[:m], rs), k
     assert _status(tiny, ws) == _lib.PS_OK
+
+
+def test_run_length_encode_repeated(tiny):
+    # this build's run-length encoding has 16 KiB tiles (four compute warps):
+    # four times the tiles, look-backs and output-buffer hand-offs per byte;
+    # runs of mean length 4 (dense tiles), 16 and 256, int32 and int64 keys
+    for kdt, code in ((np.int32, _lib.PS_INT32), (np.int64, _lib.PS_INT64)):
+        ws = torch.zeros(max(int(tiny.ps_reduce_by_key_workspace_size(code, N)), 16), dtype=torch.uint8,
+                         device=DEV)
+        for mean in (4, 16, 256):
+            keys = inputs.run_keys(N, mean, 60 + mean, kdt)
+            want_keys, want_counts = oracle.reduce_by_key(keys, None)
+            m = want_keys.shape[0]
+            kt = torch.from_numpy(keys).to(DEV)
+            uk = torch.empty_like(kt)
+            cnt = torch.empty(N, dtype=torch.int32, device=DEV)
+            nr = torch.zeros(1, dtype=torch.int64, device=DEV)
+            rk = torch.from_numpy(want_keys).to(DEV)
+            rc = torch.from_numpy(np.asarray(want_counts).astype(np.int64)).to(DEV)
+            for k in range(30):
+                st = tiny.ps_run_length_encode(code, kt.data_ptr(), uk.data_ptr(), cnt.data_ptr(), nr.data_ptr(), N,
+                                               ws.data_ptr(), ws.numel(), _stream())
+                assert st == _lib.PS_OK
+                assert int(nr.item()) == m, (kdt, mean, k)
+                assert torch.equal(uk[:m], rk) and torch.equal(cnt[:m].long(), rc), (kdt, mean, k)
+        assert _status(tiny, ws) == _lib.PS_OK
