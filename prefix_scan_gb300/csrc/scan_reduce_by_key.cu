@@ -30,16 +30,16 @@
 // closes, summed within the tile -- after which the stage goes back to the
 // producer.  The walk over each lane's chunk that precedes the scan leaves
 // each head's closing value in the warp's slice of the stage, so the pack
-// visits the heads only.  Only the run closed by the tile's first head reaches back
-// before the tile; its packed value lacks the value the tile's exclusive
-// pair carries.  Look-back warps resolve that pair; a writer warp adds its
-// value to the first run and writes the buffer out as contiguous ranges,
-// then frees the buffer.  A tile with more runs than a buffer holds (a
-// dense tile) is written by the compute warps themselves, one iteration
+// visits the heads only.  Only the run closed by the tile's first head
+// reaches back before the tile; its packed value lacks the value the tile's
+// exclusive pair carries.  Look-back warps resolve that pair; a writer warp
+// adds its value to the first run and writes the buffer out as contiguous
+// ranges, then frees the buffer.  A tile with more runs than a buffer holds
+// (a dense tile) is written by the compute warps themselves, one iteration
 // late: they publish its pair, keep its stage, do the next tile's pass (so
 // that tile's pair is out too), then wait for the dense tile's prefix,
-// re-read its keys and values and pack and write each warp's runs from its
-// slice of the stage.
+// re-read its keys and the closing values, and pack and write each warp's
+// runs from its slice of the stage.
 #include "scan_device.cuh"
 #include "scan_pipeline.cuh"
 #include "scan_trace.cuh"

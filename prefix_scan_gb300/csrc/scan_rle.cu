@@ -120,9 +120,10 @@ static_assert(kLStages >= 2, "a dense tile keeps its stage while the next one is
 #ifndef PS_RLE_WAIT_NS
 #define PS_RLE_WAIT_NS 2000
 #endif
-// Position of packed entry q in an output buffer: XOR-swizzled within each 32
-// entries, so that lanes packing entries 8 apart (every key a head) and
-// lanes reading 32 consecutive entries hit distinct banks.
+// Position of packed entry q in an output buffer or a dense tile's slice:
+// XOR-swizzled within each 32 entries, so that lanes packing a row's runs 8
+// apart (a dense tile's row where every key is a head) and lanes reading 32
+// consecutive entries hit distinct banks.
 __device__ __forceinline__ uint32_t rle_sw(uint32_t q) { return q ^ ((q >> 5) & 7u); }
 __device__ __forceinline__ bool rle_wait(uint64_t *bar, uint32_t parity) {
     return PS_RLE_WAIT_NS ? mbar_wait_suspend(bar, parity, PS_RLE_WAIT_NS) : mbar_wait(bar, parity);
