@@ -24,9 +24,10 @@ look-back off the critical path; these figures say whether it does.
 settings of the kernel (for example the look-back's poll back-off), and
 ``--launch-only K`` only launches the scan K times after one warm-up call
 (no trace read, no summary): the command to put under a profiler when
-comparing such variants.  ``--l2-probe`` and ``--read-probe`` build and run
-the two measurement probes under ``probes/`` instead (one look-back window's
-L2 round trip; HBM read bandwidth by loads and by bulk copies).
+comparing such variants.  ``--l2-probe``, ``--read-probe`` and
+``--link-probe`` build and run the measurement probes under ``probes/``
+instead (one look-back window's L2 round trip; HBM read bandwidth by loads
+and by bulk copies; the host link by copies and by kernels).
 """
 from __future__ import annotations
 
@@ -273,6 +274,17 @@ def run_read_probe() -> None:
     subprocess.run([str(exe)], check=True)
 
 
+def run_link_probe() -> None:
+    """Builds (under _build/) and runs the host-link probe: 1 GiB each way
+    between pinned host memory and the GPU by copies and by kernels."""
+    import subprocess
+    src = Path(__file__).resolve().parent / "probes" / "host_link.cu"
+    exe = nvbuild.BUILD_DIR / "host_link"
+    exe.parent.mkdir(parents=True, exist_ok=True)
+    subprocess.run([nvbuild.nvcc_path(), *nvbuild.ARCH, "-O3", "-std=c++17", "-o", str(exe), str(src)], check=True)
+    subprocess.run([str(exe)], check=True)
+
+
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--workload", action="append", choices=sorted(workloads.BY_NAME), default=[],
@@ -289,6 +301,8 @@ def main(argv=None) -> None:
                     help="build and run the L2 window-latency probe (probes/l2_window_latency.cu)")
     ap.add_argument("--read-probe", action="store_true",
                     help="build and run the read-bandwidth probe (probes/read_bandwidth.cu)")
+    ap.add_argument("--link-probe", action="store_true",
+                    help="build and run the host-link probe (probes/host_link.cu)")
     ap.add_argument("--launch-only", type=int, default=0, metavar="K",
                     help="only launch the scan K times (a build without the trace)")
     args = ap.parse_args(argv)
@@ -297,6 +311,9 @@ def main(argv=None) -> None:
         return
     if args.read_probe:
         run_read_probe()
+        return
+    if args.link_probe:
+        run_link_probe()
         return
     defines = {}
     for d in args.define:
